@@ -1,0 +1,386 @@
+#!/usr/bin/env python
+"""Throughput of one Mixtral-8x7B-shaped MoE FFN layer at decode on GB300.
+
+One step is one pass of the whole path (router GEMM + softmax + top-k,
+permute, expert up-projection, down-projection, combine) over each of the
+decode batches T = 1, 4, 16, 64 of that layer (m=4096, p=14336, E=8, top-2,
+SwiGLU experts, bf16 weights and activations; --weights i8 for the int8
+repeat).  Inputs are seeded synthetic data resident in HBM; two copies of the
+layer's weights alternate between calls, so no call finds the weights the
+previous call read in L2 (every call streams >= 0.7 GB, L2 is 126 MB).
+
+Prints one JSON line: whole-job tokens/s (all ranks), the roofline of the
+dominant kernel (the expert up-projection GEMV) from CUDA events recorded on
+its launch stream during the timed region, an end-to-end figure with host
+buffers, sampled clocks, and the fp64 CPU oracle timed on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--weights bf16|i8]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+TOKENS = (1, 4, 16, 64)
+METRIC = "MoE-layer tokens/s; HBM GB/s (decode) & tensor TFLOPS (batch) vs GB300 peak"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=600)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "i8"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---- clocks --------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [l.strip().split(", ") for l in self.file.read().splitlines() if l.strip()]
+        os.unlink(self.file.name)
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- distributed plumbing (replicas only: no collective on the data path) ----------
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if args.impl == "ours":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif args.impl == "ours":
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---- CPU oracle (baseline leg and the reference arm) ---------------------------------
+def oracle_sample(layer, xs, sample_tokens):
+    """Route every token of each batch and evaluate the experts of the first
+    `sample_tokens[T]` tokens, exactly as the oracle stands."""
+    import oracle
+    n = 0
+    for T, x in xs.items():
+        logits = oracle.router_logits(x, layer.w_router, layer.b_router)
+        ids, w = oracle.topk(logits, layer.shape.k)
+        s = sample_tokens[T]
+        if s:
+            oracle.layer(x, layer.w1, layer.w2, layer.w3, ids, w, oracle.SWIGLU,
+                         tokens=list(range(s)))
+            n += s
+    return n
+
+
+def cpu_threads():
+    try:
+        return int(os.environ.get("OMP_NUM_THREADS") or len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def make_inputs(shape, seed, device):
+    import workloads as wl
+    layer = wl.make_layer(shape, seed=seed, device=device)
+    xs = {T: wl.make_tokens(shape, T, seed=seed + 1, device=device) for T in TOKENS}
+    return layer, xs
+
+
+def workload_config(shape, weights, flush_note):
+    return {"workload": f"mixtral-8x7b moe layer decode, T in {{1,4,16,64}}, {weights} weights",
+            "model": "mixtral-8x7b-shaped single MoE FFN layer", "m": shape.m, "p": shape.p,
+            "E": shape.E, "k": shape.k, "expert": "swiglu", "tokens_per_step": sum(TOKENS),
+            "global_batch": sum(TOKENS), "seq_len": 1, "parallelism": "replicas",
+            "l2": flush_note}
+
+
+def run_reference(args, world, rank):
+    import workloads as wl
+    if rank != 0:
+        return
+    shape = wl.MIXTRAL if args.weights == "bf16" else wl.MIXTRAL.with_weight("i8")
+    import torch
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    layer, xs = make_inputs(wl.MIXTRAL, args.seed, device)
+    sample = {1: 1, 4: 1, 16: 0, 64: 0}   # 2 tokens of experts per step, every token routed
+    for _ in range(args.warmup):
+        oracle_sample(layer, xs, sample)
+    t0 = time.perf_counter()
+    n = 0
+    for _ in range(args.steps):
+        n += oracle_sample(layer, xs, sample)
+    dt = time.perf_counter() - t0
+    value = n / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(shape, args.weights, "n/a (CPU)"),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(),
+                             "kind": "oracle",
+                             "sample": "per step: router + top-k for all 85 tokens of the four "
+                                       "batches, expert MLPs for 1 token of T=1 and 1 of T=4"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---- our arm ----------------------------------------------------------------------------
+def traffic_record(kernel_src):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of the kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_up_traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    if rec.get("source_sha256") != sha:
+        return None
+    return rec
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import mixture_experts_layer_gemm_gb300 as moe
+    import workloads as wl
+    from mixture_experts_layer_gemm_gb300 import build as lib_build
+
+    lib_build.build()
+    shape = wl.MIXTRAL if args.weights == "bf16" else wl.MIXTRAL.with_weight("i8")
+    layer, xs_np = make_inputs(shape, args.seed + rank, f"cuda:{local}")
+    max_t = max(TOKENS)
+    copies = [moe.MoELayer(layer, max_t) for _ in range(2)]
+    dev = torch.device("cuda", local)
+    xs = {T: torch.from_numpy(xs_np[T].view(np.int16).copy()).view(torch.bfloat16).to(dev)
+          for T in TOKENS}
+    ys = {T: torch.empty((T, shape.m), dtype=torch.bfloat16, device=dev) for T in TOKENS}
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for i, T in enumerate(TOKENS):
+            c = copies[i % 2]
+            c.route(xs[T], stream=stream)
+            c.forward(xs[T], ys[T], stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    for c in copies:
+        st, flags = c.sync_check()
+        if st != moe.MOE_OK:
+            raise RuntimeError(f"device flagged routing error bits {flags:#x}")
+        c.set_timing(True)
+        c.timings(reset=True)
+    launches0 = sum(c.stats().kernel_launches for c in copies)
+
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(world, ms)
+    launches = sum(c.stats().kernel_launches for c in copies) - launches0
+    tim = [c.timings(reset=True) for c in copies]
+    for c in copies:
+        c.set_timing(False)
+
+    # algorithmic bytes of the up-projection per call: active experts' W1 and W3,
+    # the token rows read and the hidden rows written
+    wbytes = 1 if args.weights == "i8" else 2
+    bytes_up, bytes_down, active = 0, 0, {}
+    for i, T in enumerate(TOKENS):
+        c = copies[i % 2]
+        c.route(xs[T], stream=stream)
+        torch.cuda.synchronize()
+        n_act = int((c.counts.cpu() > 0).sum())
+        active[T] = n_act
+        scale_up = 2 * shape.p * 4 if args.weights == "i8" else 0
+        scale_dn = shape.m * 4 if args.weights == "i8" else 0
+        bytes_up += n_act * (2 * shape.m * shape.p * wbytes + scale_up) + T * shape.m * 2 \
+            + T * shape.k * shape.p * 2
+        bytes_down += n_act * (shape.m * shape.p * wbytes + scale_dn) + T * shape.k * shape.p * 2
+    up_ms = sum(t["up"][0] for t in tim)
+    up_n = sum(t["up"][1] for t in tim)
+    dn_ms = sum(t["down"][0] for t in tim)
+    phase_ms = {k: sum(t[k][0] for t in tim) / args.steps for k in tim[0]}
+    hbm, tf, tf_sus, src = peaks()
+    achieved = bytes_up * args.steps / (up_ms * 1e-3) / 1e9
+    layer_bytes = bytes_up + bytes_down
+    layer_gbs = layer_bytes * args.steps / (ms * 1e-3) / 1e9
+    trec = traffic_record(os.path.join(ROOT, "mixture_experts_layer_gemm_gb300", "csrc",
+                                       "expert_decode.cu"))
+    roofline = {"kernel": "decode_up (expert up-projection GEMV, W1 and W3 + SiLU*gate)",
+                "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "peak_source": f"{src} (hbm_gbs)",
+                "algorithmic_bytes_per_step": bytes_up,
+                "avg_launch_us": up_ms * 1e3 / max(up_n, 1),
+                "traffic": None if trec is None else trec.get("bytes_per_step")}
+
+    # end to end: pinned host buffers, H2D of x and D2H of y inside the timed region
+    xh = {T: xs[T].cpu().pin_memory() for T in TOKENS}
+    yh = {T: torch.empty((T, shape.m), dtype=torch.bfloat16).pin_memory() for T in TOKENS}
+    xd = {T: torch.empty_like(xs[T]) for T in TOKENS}
+
+    def step_e2e():
+        for i, T in enumerate(TOKENS):
+            c = copies[i % 2]
+            xd[T].copy_(xh[T], non_blocking=True)
+            c.route(xd[T], stream=stream)
+            c.forward(xd[T], ys[T], stream=stream)
+            yh[T].copy_(ys[T], non_blocking=True)
+
+    for _ in range(3):
+        step_e2e()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k_e2e = max(args.steps // 2, 1)
+    e0.record(stream)
+    for _ in range(k_e2e):
+        step_e2e()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1))
+    io_bytes = sum(T * shape.m * 2 for T in TOKENS)
+
+    tokens_step = sum(TOKENS)
+    value = world * tokens_step * args.steps / (ms_max * 1e-3)
+    e2e_value = world * tokens_step * k_e2e / (e2e_ms * 1e-3)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = {1: 1, 4: 4, 16: 16, 64: 16}
+        t0 = time.perf_counter()
+        n = oracle_sample(layer, xs_np, sample)
+        dt = time.perf_counter() - t0
+        cpu = {"value": n / dt, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+               "sample": f"router + top-k for all 85 tokens, expert MLPs for {n} tokens "
+                         "(all of T=1,4,16 and 16 of T=64), fp64, one pass"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "config": workload_config(shape, args.weights,
+                                          "inputs larger than L2: two weight copies alternate"),
+                "roofline": roofline,
+                "layer_hbm": {"achieved": layer_gbs, "unit": "GB/s", "frac": layer_gbs / hbm,
+                              "algorithmic_bytes_per_step": layer_bytes,
+                              "note": "whole step: expert weights + activations / step time"},
+                "phase_ms_per_step": phase_ms, "active_experts": active,
+                "cpu_baseline": cpu,
+                "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
+                        "d2h_bytes_per_step": io_bytes},
+                "gpu_launches": launches, "clocks": clk}
+        print(json.dumps(line), flush=True)
+    for c in copies:
+        c.close()
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

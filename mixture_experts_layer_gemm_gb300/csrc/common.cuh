@@ -1,0 +1,105 @@
+// common.cuh -- device helpers shared by the library's kernels (not by the
+// oracle, which has none of this code).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kMaxExperts = 64;
+constexpr int kMaxTopK = 8;
+
+// Bits of the layer's device error word.
+enum : uint32_t {
+    kErrExpertId = 1u << 0,     // expert id outside [0, E): routed to expert 0
+    kErrDuplicateId = 1u << 1,  // the same expert twice in one token's top-k
+    kErrGatherIndex = 1u << 2,  // gather index outside [0, T*k): access skipped
+    kErrOffsets = 1u << 3,      // offsets not monotone / out of range: clamped
+    kErrWaitTimeout = 1u << 4,  // a bounded device wait gave up
+    kErrTmemAlloc = 1u << 5,    // tensor-memory allocation did not succeed
+};
+
+__device__ __forceinline__ void flag_error(uint32_t *err, uint32_t bits) {
+    if (err) atomicOr(err, bits);
+}
+
+// ---- element conversions --------------------------------------------------
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+
+// ---- memory access ----------------------------------------------------------
+// Streaming 16-byte load of read-once data (expert weights): read-only path,
+// no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(addr));
+    return r;
+}
+
+// ---- legacy warp-level tensor-core MMA -----------------------------------
+// D[16x8] += A[16x16] * B[16x8], bf16 inputs, fp32 accumulate.
+// Fragment ownership (g = lane/4, t = lane%4):
+//   a0 = A[g][2t..2t+1]   a1 = A[g+8][2t..2t+1]
+//   a2 = A[g][2t+8..+9]   a3 = A[g+8][2t+8..+9]
+//   b0 = B[2t..2t+1][g]   b1 = B[2t+8..+9][g]
+//   d0,d1 = D[g][2t..2t+1]  d2,d3 = D[g+8][2t..2t+1]
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four signed int8 values (one 32-bit word, byte 0 first) -> two bf16x2 words
+// holding bytes (0,1) and (2,3).  Every int8 is exactly representable in bf16.
+__device__ __forceinline__ void i8x4_to_bf16x2x2(uint32_t v, uint32_t &lo, uint32_t &hi) {
+    const int32_t s = static_cast<int32_t>(v);
+    const float f0 = static_cast<float>((s << 24) >> 24);
+    const float f1 = static_cast<float>((s << 16) >> 24);
+    const float f2 = static_cast<float>((s << 8) >> 24);
+    const float f3 = static_cast<float>(s >> 24);
+    lo = pack_bf16x2(f0, f1);
+    hi = pack_bf16x2(f2, f3);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+}  // namespace moe

@@ -1,0 +1,108 @@
+// kernels.cuh -- argument blocks and host launchers of the library's kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kExpertTableMax = 64;
+
+// ---- routing -------------------------------------------------------------------
+struct RouterArgs {
+    const void *x;       // [T x m] act type
+    const float *wrt;    // [E x m] router weights, transposed, fp32
+    const float *bias;   // [E] or nullptr
+    int T, m, E, k;
+    int32_t *ids;        // [T*k]
+    float *w;            // [T*k]
+    float *logits;       // [T*E] or nullptr
+};
+
+struct PermuteArgs {
+    const int32_t *ids;  // [T*k]
+    int T, k, E;
+    int32_t *counts, *offsets, *gather, *scatter;
+};
+
+cudaError_t launch_router_topk(const RouterArgs &a, bool act_bf16, cudaStream_t s);
+cudaError_t launch_topk_from_logits(const float *logits, int T, int E, int k, int32_t *ids,
+                                    float *w, cudaStream_t s);
+cudaError_t launch_topk_copy_validate(const int32_t *ids_in, const float *w_in, int T, int E,
+                                      int k, int32_t *ids_out, float *w_out, uint32_t *err,
+                                      cudaStream_t s);
+cudaError_t launch_permute(const PermuteArgs &a, cudaStream_t s);
+
+// ---- expert weights as stored: transposed so the reduction runs along rows ----
+// up:   W1t[e] (and W3t[e]) [p rows x m cols];  down: W2t[e] [m rows x p cols]
+// For int8 weights, s1/s3[e] hold p fp32 scales and s2[e] holds m scales.
+struct ExpertTables {
+    const void *w1[kExpertTableMax];
+    const void *w3[kExpertTableMax];
+    const void *w2[kExpertTableMax];
+    const float *s1[kExpertTableMax];
+    const float *s3[kExpertTableMax];
+    const float *s2[kExpertTableMax];
+};
+
+// Which experts a launch covers: the experts listed in `only` (n_only > 0,
+// paged layers launch per resident expert) or every expert with tokens.
+struct ExpertArgs {
+    const ExpertTables *tab;     // host copy, passed by value to the kernel
+    const void *x;               // [T x m] act type (tokens in token order)
+    const int32_t *gather;       // [T*k]
+    const int32_t *offsets;      // [E+1]
+    const float *topk_w;         // [T*k]
+    int T, k, E, m, p;
+    void *h;                     // [T*k x p] act type (permuted order)
+    float *ypart;                // [splits x T*k x m] fp32 (permuted order)
+    int n_rows_cap;              // T*k capacity of one ypart split
+    float *gate_part;            // [splits_up x T*k x p] fp32 (decode split-K up only)
+    float *up_part;              // same
+    uint32_t *err;
+    int only[kExpertTableMax];
+    int n_only;
+};
+
+enum class WeightType { kF32, kBF16, kI8 };
+
+// Decode regime: weight-streaming expert GEMV on the legacy tensor path.
+// Token tiles of 8 per pass chosen from the mean tokens per expert.
+int decode_token_tiles(int T, int k, int E);
+cudaError_t launch_decode_up(const ExpertArgs &a, WeightType wt, bool gated, int splits,
+                             int num_sms, cudaStream_t s);
+cudaError_t launch_decode_down(const ExpertArgs &a, WeightType wt, int splits, int num_sms,
+                               cudaStream_t s);
+// finish a split-K up projection: h = act(sum_s gate_part) [* sum_s up_part]
+cudaError_t launch_decode_up_finish(const ExpertArgs &a, bool gated, int splits,
+                                    cudaStream_t s);
+
+// fp32 path (SIMT, warp-shuffle reductions)
+cudaError_t launch_simt_up(const ExpertArgs &a, bool gated, cudaStream_t s);
+cudaError_t launch_simt_down(const ExpertArgs &a, cudaStream_t s);
+
+// Combine: y[t] = sum_j sum_s ypart[s][scatter[t*k+j]] in fp32, rounded once.
+struct CombineArgs {
+    const float *ypart;
+    int splits;
+    size_t split_stride;         // elements between splits
+    const int32_t *scatter;
+    int T, k, m;
+    void *y;
+    uint32_t *err;
+};
+cudaError_t launch_combine(const CombineArgs &a, bool act_bf16, cudaStream_t s);
+
+// ---- weight ingestion ------------------------------------------------------------
+// dst[c][r] = src[r][c] for a rows x cols matrix; element size 2 or 4 bytes.
+cudaError_t launch_transpose(const void *src, void *dst, int rows, int cols, int elem_bytes,
+                             cudaStream_t s);
+// Per-row symmetric int8 of a bf16 nrows x len matrix (rows of the transposed
+// weight = columns of the user's matrix): codes [nrows x len], scales [nrows].
+cudaError_t launch_quantize_rows(const void *wt_bf16, int nrows, int len, int8_t *codes,
+                                 float *scales, cudaStream_t s);
+// widen router weights to fp32 and transpose: dst[e][c] = src[c][e]
+cudaError_t launch_router_prep(const void *src, bool bf16, int m, int E, float *dst,
+                               cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,101 @@
+// layer_impl.h -- the layer object behind the opaque moe_layer_t handle.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <vector>
+
+#include "../../include/moe_layer.h"
+#include "kernels.cuh"
+
+struct moe_layer {
+    moe_config_t cfg{};
+    int layer_id = 0;
+    int device = -1;
+    int num_sms = 0;
+    int regime = 0;  // MOE_OPT_REGIME
+
+    // weights (resident copy, or unused for paged layers)
+    float *wrt = nullptr;      // router [E x m] fp32
+    float *bias = nullptr;     // [E] fp32
+    uint8_t *weights = nullptr;
+    size_t expert_stride = 0;  // bytes between experts inside `weights`
+    size_t expert_bytes = 0;   // bytes of one expert's stored weights (no padding)
+    moe::ExpertTables tab{};
+
+    // workspace
+    void *h = nullptr;
+    float *ypart = nullptr;
+    float *gate_part = nullptr, *up_part = nullptr;
+    size_t decode_rows_cap = 0;
+    int split_up_max = 1, split_down_max = 1;
+    size_t workspace_bytes = 0;
+    uint32_t *err_word = nullptr;
+
+    // paged weights
+    moe_pool_t *pool = nullptr;
+    uint8_t *pinned_weights = nullptr;  // E experts x expert_stride, pinned host
+
+    moe_stats_t stats{};
+    // per-launch event timing (MOE_OPT_TIMING)
+    struct Pending {
+        int phase;
+        cudaEvent_t a, b;
+    };
+    bool timing = false;
+    std::vector<cudaEvent_t> event_pool;
+    std::vector<Pending> pending;
+    double phase_ms[MOE_NUM_PHASES] = {};
+    uint64_t phase_launches[MOE_NUM_PHASES] = {};
+    cudaEvent_t get_event();
+
+    cudaEvent_t done = nullptr;
+    cudaStream_t ingest_stream = nullptr;
+    std::vector<void *> allocations;
+
+    ~moe_layer();
+    void *dalloc(size_t bytes, cudaError_t *err);
+};
+
+namespace moe {
+moe_status_t fail(moe_status_t st, const char *fmt, ...);
+moe_status_t cuda_fail(cudaError_t e, const char *where);
+
+ExpertArgs make_expert_args(moe_layer *L, const void *x, const moe_routing_t *r);
+moe_status_t run_experts(moe_layer *L, ExpertArgs &a, int regime, int *splits_out, cudaStream_t s);
+moe_status_t run_combine(moe_layer *L, const moe_routing_t *r, int splits, int n_rows_cap, void *y,
+                         cudaStream_t s);
+
+// Launch one kernel (f returns its cudaError_t) as phase `phase`: counts the
+// launch and, with timing on, brackets it with events on stream s.
+template <typename F>
+moe_status_t launch_phase(moe_layer *L, int phase, cudaStream_t s, const char *what, F &&f) {
+    cudaEvent_t a = nullptr;
+    if (L->timing) {
+        a = L->get_event();
+        if (a) cudaEventRecord(a, s);
+    }
+    const cudaError_t e = f();
+    if (e != cudaSuccess) {
+        if (a) L->event_pool.push_back(a);
+        return cuda_fail(e, what);
+    }
+    if (a) {
+        cudaEvent_t b = L->get_event();
+        if (b) {
+            cudaEventRecord(b, s);
+            L->pending.push_back({phase, a, b});
+        } else {
+            L->event_pool.push_back(a);
+        }
+    }
+    L->stats.kernel_launches += 1;
+    return MOE_OK;
+}
+}  // namespace moe
+
+// paged.cu
+moe_status_t paged_attach(moe_layer *L);
+void paged_detach(moe_layer *L);
+moe_status_t paged_forward(moe_layer *L, const void *x, const moe_routing_t *r, void *y,
+                           cudaStream_t s);

@@ -1,0 +1,628 @@
+// moe_layer.cu -- host side of the C ABI declared in include/moe_layer.h:
+// argument validation, weight ingestion, workspace ownership, regime choice
+// and kernel orchestration on the caller's stream.
+//
+// The layer computes the forward pass the pages describe for one MoE FFN
+// layer (HARMOEny write-up, parts 1 and 3.3; expert shape of part 3.2):
+//   moe_route   : router GEMM + softmax + top-k, then histogram / scan /
+//                 stable permute (the one-device form of the dispatch)
+//   moe_forward : expert up-projection + activation, down-projection scaled by
+//                 the routing weight, weighted un-permute and combine.
+#include <chrono>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "../../include/moe_layer.h"
+#include "common.cuh"
+#include "kernels.cuh"
+#include "layer_impl.h"
+
+using namespace moe;
+
+// ---- error text ----------------------------------------------------------------
+namespace {
+thread_local std::string g_last_error;
+}
+
+namespace moe {
+
+moe_status_t fail(moe_status_t st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+moe_status_t cuda_fail(cudaError_t e, const char *where) {
+    cudaGetLastError();  // clear a non-sticky error
+    if (e == cudaErrorMemoryAllocation)
+        return fail(MOE_ERR_OOM, "%s: %s", where, cudaGetErrorString(e));
+    return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+}  // namespace moe
+
+#define CUDA_TRY(expr)                                      \
+    do {                                                    \
+        cudaError_t e_ = (expr);                            \
+        if (e_ != cudaSuccess) return cuda_fail(e_, #expr); \
+    } while (0)
+
+namespace {
+
+constexpr int kDecodeMaxRows = 512;          // T*k handled with split-K partials
+constexpr size_t kSmemBudgetB = 64 * 1024;   // staged token rows per CTA
+
+size_t act_bytes(moe_dtype_t d) { return d == MOE_F32 ? 4 : 2; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+int splits_for(int K, int nt, int min_splits) {
+    int s = ceil_div(static_cast<long long>(8) * nt * 2 * K, static_cast<long long>(kSmemBudgetB));
+    if (s < min_splits) s = min_splits;
+    return s;
+}
+
+moe_status_t check_config(const moe_config_t *c) {
+    if (!c) return fail(MOE_ERR_INVALID_ARG, "config is NULL");
+    if (c->m <= 0 || c->p <= 0) return fail(MOE_ERR_INVALID_ARG, "m and p must be positive");
+    if (c->E < 1 || c->E > kMaxExperts)
+        return fail(MOE_ERR_INVALID_ARG, "E must be in [1, %d]", kMaxExperts);
+    if (c->k < 1 || c->k > c->E || c->k > kMaxTopK)
+        return fail(MOE_ERR_INVALID_ARG, "k must be in [1, min(E, %d)]", kMaxTopK);
+    if (c->max_tokens < 1 || static_cast<long long>(c->max_tokens) * c->k > (1 << 30))
+        return fail(MOE_ERR_INVALID_ARG, "max_tokens out of range");
+    if (c->act_dtype != MOE_F32 && c->act_dtype != MOE_BF16)
+        return fail(MOE_ERR_INVALID_ARG, "act_dtype must be F32 or BF16");
+    if (c->expert != MOE_EXPERT_RELU2 && c->expert != MOE_EXPERT_SWIGLU)
+        return fail(MOE_ERR_INVALID_ARG, "unknown expert form");
+    if (c->act_dtype == MOE_F32) {
+        if (c->weight_dtype != MOE_F32)
+            return fail(MOE_ERR_UNSUPPORTED, "fp32 activations need fp32 weights");
+        if (c->m % 4) return fail(MOE_ERR_UNSUPPORTED, "fp32 layers need m %% 4 == 0");
+    } else {
+        if (c->weight_dtype != MOE_BF16 && c->weight_dtype != MOE_I8)
+            return fail(MOE_ERR_UNSUPPORTED, "bf16 activations need bf16 or int8 weights");
+        if (c->m % 64 || c->p % 64)
+            return fail(MOE_ERR_UNSUPPORTED, "bf16/int8 layers need m and p multiples of 64");
+    }
+    if (c->paged && c->weight_dtype == MOE_F32)
+        return fail(MOE_ERR_UNSUPPORTED, "paged layers need bf16 or int8 weights");
+    return MOE_OK;
+}
+
+moe_status_t check_routing(const moe_layer_t *L, const moe_routing_t *r) {
+    if (!r) return fail(MOE_ERR_INVALID_ARG, "routing is NULL");
+    if (!r->topk_ids || !r->topk_w || !r->counts || !r->offsets || !r->gather_index ||
+        !r->scatter_index)
+        return fail(MOE_ERR_INVALID_ARG, "a routing table pointer is NULL");
+    (void)L;
+    return MOE_OK;
+}
+
+}  // namespace
+
+// ---- lifetime ---------------------------------------------------------------------
+moe_layer::~moe_layer() {
+    if (device >= 0) cudaSetDevice(device);
+    for (void *p : allocations) cudaFree(p);
+    if (pinned_weights) cudaFreeHost(pinned_weights);
+    for (cudaEvent_t ev : event_pool) cudaEventDestroy(ev);
+    for (auto &pe : pending) {
+        cudaEventDestroy(pe.a);
+        cudaEventDestroy(pe.b);
+    }
+    if (done) cudaEventDestroy(done);
+    if (ingest_stream) cudaStreamDestroy(ingest_stream);
+}
+
+cudaEvent_t moe_layer::get_event() {
+    if (!event_pool.empty()) {
+        cudaEvent_t ev = event_pool.back();
+        event_pool.pop_back();
+        return ev;
+    }
+    cudaEvent_t ev = nullptr;
+    if (cudaEventCreate(&ev) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return ev;
+}
+
+void *moe_layer::dalloc(size_t bytes, cudaError_t *err) {
+    void *p = nullptr;
+    *err = cudaMalloc(&p, bytes ? bytes : 16);
+    if (*err == cudaSuccess) allocations.push_back(p);
+    return p;
+}
+
+static moe_status_t ingest_weights(moe_layer_t *L, const void *w_router, const float *b_router,
+                                   const void *const *w1, const void *const *w2,
+                                   const void *const *w3) {
+    const moe_config_t &c = L->cfg;
+    cudaError_t err;
+    cudaStream_t s = L->ingest_stream;
+    const bool bf16_act = c.act_dtype == MOE_BF16;
+    const size_t ab = act_bytes(c.act_dtype);
+    const size_t src_elem = (c.weight_dtype == MOE_F32) ? 4 : 2;
+    const size_t mp = static_cast<size_t>(c.m) * c.p;
+
+    // router: [m x E] act type -> fp32 [E x m]
+    void *stage_r = L->dalloc(static_cast<size_t>(c.m) * c.E * ab, &err);
+    if (err) return cuda_fail(err, "cudaMalloc(router staging)");
+    L->wrt = static_cast<float *>(L->dalloc(static_cast<size_t>(c.m) * c.E * 4, &err));
+    if (err) return cuda_fail(err, "cudaMalloc(router)");
+    CUDA_TRY(cudaMemcpyAsync(stage_r, w_router, static_cast<size_t>(c.m) * c.E * ab,
+                             cudaMemcpyHostToDevice, s));
+    CUDA_TRY(launch_router_prep(stage_r, bf16_act, c.m, c.E, L->wrt, s));
+    if (c.has_router_bias) {
+        L->bias = static_cast<float *>(L->dalloc(static_cast<size_t>(c.E) * 4, &err));
+        if (err) return cuda_fail(err, "cudaMalloc(bias)");
+        CUDA_TRY(cudaMemcpyAsync(L->bias, b_router, static_cast<size_t>(c.E) * 4,
+                                 cudaMemcpyHostToDevice, s));
+    }
+
+    // experts: one allocation holding every expert's transposed matrices
+    const int nmat = (c.expert == MOE_EXPERT_SWIGLU) ? 3 : 2;
+    const size_t wel = (c.weight_dtype == MOE_I8) ? 1 : src_elem;
+    const size_t mat_bytes = (mp * wel + 255) / 256 * 256;
+    const size_t scale_bytes =
+        (c.weight_dtype == MOE_I8)
+            ? ((static_cast<size_t>(c.p) * (nmat - 1) + c.m) * 4 + 255) / 256 * 256
+            : 0;
+    L->expert_stride = mat_bytes * nmat + scale_bytes;
+    L->expert_bytes = mp * wel * nmat +
+                      (c.weight_dtype == MOE_I8 ? (static_cast<size_t>(c.p) * (nmat - 1) + c.m) * 4 : 0);
+    L->weights = static_cast<uint8_t *>(L->dalloc(L->expert_stride * c.E, &err));
+    if (err) return cuda_fail(err, "cudaMalloc(expert weights)");
+    void *stage = L->dalloc(mp * src_elem, &err);
+    if (err) return cuda_fail(err, "cudaMalloc(weight staging)");
+    void *stage_t = nullptr;
+    if (c.weight_dtype == MOE_I8) {
+        stage_t = L->dalloc(mp * src_elem, &err);
+        if (err) return cuda_fail(err, "cudaMalloc(weight staging)");
+    }
+    for (int e = 0; e < c.E; ++e) {
+        uint8_t *base = L->weights + L->expert_stride * e;
+        uint8_t *m1 = base, *m2 = base + mat_bytes, *m3 = (nmat == 3) ? base + 2 * mat_bytes : nullptr;
+        float *sc = reinterpret_cast<float *>(base + mat_bytes * nmat);
+        float *s1 = sc, *s3 = (nmat == 3) ? sc + c.p : nullptr, *s2 = sc + static_cast<size_t>(c.p) * (nmat - 1);
+        struct Job { const void *src; uint8_t *dst; int rows, cols; float *scales; };
+        Job jobs[3] = {{w1[e], m1, c.m, c.p, s1}, {w2[e], m2, c.p, c.m, s2},
+                       {nmat == 3 ? w3[e] : nullptr, m3, c.m, c.p, s3}};
+        for (int j = 0; j < nmat; ++j) {
+            const Job &jb = jobs[j];
+            // the staging buffer is reused: order the copy after the last kernel
+            CUDA_TRY(cudaMemcpyAsync(stage, jb.src, mp * src_elem, cudaMemcpyHostToDevice, s));
+            if (c.weight_dtype == MOE_I8) {
+                CUDA_TRY(launch_transpose(stage, stage_t, jb.rows, jb.cols, 2, s));
+                CUDA_TRY(launch_quantize_rows(stage_t, jb.cols, jb.rows,
+                                              reinterpret_cast<int8_t *>(jb.dst), jb.scales, s));
+            } else {
+                CUDA_TRY(launch_transpose(stage, jb.dst, jb.rows, jb.cols, static_cast<int>(src_elem), s));
+            }
+        }
+        L->tab.w1[e] = m1;
+        L->tab.w2[e] = m2;
+        L->tab.w3[e] = m3;
+        L->tab.s1[e] = (c.weight_dtype == MOE_I8) ? s1 : nullptr;
+        L->tab.s2[e] = (c.weight_dtype == MOE_I8) ? s2 : nullptr;
+        L->tab.s3[e] = (c.weight_dtype == MOE_I8) ? s3 : nullptr;
+    }
+    CUDA_TRY(cudaStreamSynchronize(s));
+    // staging buffers are not needed after ingestion
+    for (void *p : {stage_r, stage, stage_t}) {
+        if (!p) continue;
+        for (size_t i = 0; i < L->allocations.size(); ++i)
+            if (L->allocations[i] == p) {
+                cudaFree(p);
+                L->allocations.erase(L->allocations.begin() + static_cast<long>(i));
+                break;
+            }
+    }
+    return MOE_OK;
+}
+
+static moe_status_t alloc_workspace(moe_layer_t *L) {
+    const moe_config_t &c = L->cfg;
+    cudaError_t err;
+    const size_t rows = static_cast<size_t>(c.max_tokens) * c.k;
+    const size_t ab = act_bytes(c.act_dtype);
+    L->h = L->dalloc(rows * c.p * ab, &err);
+    if (err) return cuda_fail(err, "cudaMalloc(h)");
+    size_t ypart_rows = rows;
+    L->split_up_max = 1;
+    L->split_down_max = 1;
+    if (c.act_dtype == MOE_BF16) {
+        const int nt_max = 4;
+        L->split_up_max = splits_for(c.m, nt_max, 1);
+        L->split_down_max = splits_for(c.p, nt_max, 4);
+        const size_t drows = rows < kDecodeMaxRows ? rows : kDecodeMaxRows;
+        L->decode_rows_cap = drows;
+        size_t need = static_cast<size_t>(L->split_down_max) * drows;
+        if (rows > kDecodeMaxRows) {
+            // beyond the split-K row cap the decode kernels run one token tile
+            // per pass with 4 down splits and no up split
+            const size_t big = 4 * rows;
+            if (big > need) need = big;
+        }
+        ypart_rows = need;
+        if (L->split_up_max > 1) {
+            const size_t n = static_cast<size_t>(L->split_up_max) * drows * c.p;
+            L->gate_part = static_cast<float *>(L->dalloc(n * 4, &err));
+            if (err) return cuda_fail(err, "cudaMalloc(gate partials)");
+            L->up_part = static_cast<float *>(L->dalloc(n * 4, &err));
+            if (err) return cuda_fail(err, "cudaMalloc(up partials)");
+            L->workspace_bytes += 2 * n * 4;
+        }
+    }
+    L->ypart = static_cast<float *>(L->dalloc(ypart_rows * c.m * 4, &err));
+    if (err) return cuda_fail(err, "cudaMalloc(ypart)");
+    L->err_word = static_cast<uint32_t *>(L->dalloc(4, &err));
+    if (err) return cuda_fail(err, "cudaMalloc(error word)");
+    CUDA_TRY(cudaMemset(L->err_word, 0, 4));
+    L->workspace_bytes += rows * c.p * ab + ypart_rows * c.m * 4;
+    return MOE_OK;
+}
+
+extern "C" moe_status_t moe_layer_create(const moe_config_t *cfg, const void *w_router,
+                                         const float *b_router, const void *const *w1,
+                                         const void *const *w2, const void *const *w3,
+                                         moe_pool_t *pool, int layer_id, moe_layer_t **out) {
+    if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    moe_status_t st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (!w_router || !w1 || !w2) return fail(MOE_ERR_INVALID_ARG, "weight pointer is NULL");
+    if (cfg->has_router_bias && !b_router) return fail(MOE_ERR_INVALID_ARG, "b_router is NULL");
+    const bool gated = cfg->expert == MOE_EXPERT_SWIGLU;
+    if (gated != (w3 != nullptr))
+        return fail(MOE_ERR_INVALID_ARG, "w3 must be given exactly for the SwiGLU form");
+    for (int e = 0; e < cfg->E; ++e)
+        if (!w1[e] || !w2[e] || (gated && !w3[e]))
+            return fail(MOE_ERR_INVALID_ARG, "expert %d weight pointer is NULL", e);
+    if (cfg->paged && !pool) return fail(MOE_ERR_INVALID_ARG, "paged layer needs a pool");
+    if (!cfg->paged && pool) return fail(MOE_ERR_INVALID_ARG, "pool given for a resident layer");
+    if (layer_id < 0) return fail(MOE_ERR_INVALID_ARG, "layer_id must be >= 0");
+
+    moe_layer_t *L = new (std::nothrow) moe_layer();
+    if (!L) return fail(MOE_ERR_OOM, "host allocation failed");
+    L->cfg = *cfg;
+    L->layer_id = layer_id;
+    L->pool = pool;
+    cudaError_t err = cudaGetDevice(&L->device);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device);
+    if (err == cudaSuccess) err = cudaStreamCreateWithFlags(&L->ingest_stream, cudaStreamNonBlocking);
+    if (err == cudaSuccess) err = cudaEventCreateWithFlags(&L->done, cudaEventDisableTiming);
+    if (err != cudaSuccess) {
+        delete L;
+        return cuda_fail(err, "device setup");
+    }
+    std::memset(&L->tab, 0, sizeof L->tab);
+    st = ingest_weights(L, w_router, b_router, w1, w2, w3);
+    if (st == MOE_OK) st = alloc_workspace(L);
+    if (st == MOE_OK && cfg->paged) st = paged_attach(L);
+    if (st != MOE_OK) {
+        std::string keep = g_last_error;
+        delete L;
+        g_last_error = keep;
+        return st;
+    }
+    *out = L;
+    return MOE_OK;
+}
+
+extern "C" moe_status_t moe_destroy(moe_layer_t *L) {
+    if (!L) return MOE_OK;
+    cudaSetDevice(L->device);
+    cudaDeviceSynchronize();
+    if (L->pool) paged_detach(L);
+    delete L;
+    return MOE_OK;
+}
+
+// ---- routing ---------------------------------------------------------------------------
+static moe_status_t run_permute(moe_layer_t *L, int T, moe_routing_t *r, cudaStream_t s) {
+    PermuteArgs pa{r->topk_ids, T, L->cfg.k, L->cfg.E, r->counts, r->offsets, r->gather_index,
+                   r->scatter_index};
+    moe_status_t st = launch_phase(L, MOE_PHASE_PERMUTE, s, "permute", [&] { return launch_permute(pa, s); });
+    if (st != MOE_OK) return st;
+    CUDA_TRY(cudaEventRecord(L->done, s));
+    r->T = T;
+    return MOE_OK;
+}
+
+static moe_status_t check_T(const moe_layer_t *L, int T) {
+    if (T < 0 || T > L->cfg.max_tokens)
+        return fail(MOE_ERR_INVALID_ARG, "T = %d outside [0, max_tokens = %d]", T, L->cfg.max_tokens);
+    return MOE_OK;
+}
+
+extern "C" moe_status_t moe_route(moe_layer_t *L, const void *x, int T, moe_routing_t *r,
+                                  void *stream) {
+    if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    moe_status_t st = check_T(L, T);
+    if (st == MOE_OK) st = check_routing(L, r);
+    if (st != MOE_OK) return st;
+    if (T > 0 && (!x || !aligned16(x))) return fail(MOE_ERR_INVALID_ARG, "x is NULL or not 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    RouterArgs ra{x, L->wrt, L->bias, T, L->cfg.m, L->cfg.E, L->cfg.k, r->topk_ids, r->topk_w,
+                  r->logits};
+    if (T > 0) {
+        st = launch_phase(L, MOE_PHASE_ROUTER, s, "router_topk",
+                          [&] { return launch_router_topk(ra, L->cfg.act_dtype == MOE_BF16, s); });
+        if (st != MOE_OK) return st;
+    }
+    return run_permute(L, T, r, s);
+}
+
+extern "C" moe_status_t moe_route_from_logits(moe_layer_t *L, const float *logits, int T,
+                                              moe_routing_t *r, void *stream) {
+    if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    moe_status_t st = check_T(L, T);
+    if (st == MOE_OK) st = check_routing(L, r);
+    if (st != MOE_OK) return st;
+    if (T > 0 && !logits) return fail(MOE_ERR_INVALID_ARG, "logits is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T > 0) {
+        st = launch_phase(L, MOE_PHASE_ROUTER, s, "topk_from_logits", [&] {
+            return launch_topk_from_logits(logits, T, L->cfg.E, L->cfg.k, r->topk_ids, r->topk_w, s);
+        });
+        if (st != MOE_OK) return st;
+    }
+    return run_permute(L, T, r, s);
+}
+
+extern "C" moe_status_t moe_route_from_topk(moe_layer_t *L, const int32_t *ids, const float *w,
+                                            int T, moe_routing_t *r, void *stream) {
+    if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    moe_status_t st = check_T(L, T);
+    if (st == MOE_OK) st = check_routing(L, r);
+    if (st != MOE_OK) return st;
+    if (T > 0 && (!ids || !w)) return fail(MOE_ERR_INVALID_ARG, "ids or w is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T > 0) {
+        st = launch_phase(L, MOE_PHASE_ROUTER, s, "topk_copy_validate", [&] {
+            return launch_topk_copy_validate(ids, w, T, L->cfg.E, L->cfg.k, r->topk_ids, r->topk_w,
+                                             L->err_word, s);
+        });
+        if (st != MOE_OK) return st;
+    }
+    return run_permute(L, T, r, s);
+}
+
+// ---- forward ---------------------------------------------------------------------------
+namespace moe {
+
+ExpertArgs make_expert_args(moe_layer_t *L, const void *x, const moe_routing_t *r) {
+    ExpertArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.tab = &L->tab;
+    a.x = x;
+    a.gather = r->gather_index;
+    a.offsets = r->offsets;
+    a.topk_w = r->topk_w;
+    a.T = r->T;
+    a.k = L->cfg.k;
+    a.E = L->cfg.E;
+    a.m = L->cfg.m;
+    a.p = L->cfg.p;
+    a.h = L->h;
+    a.ypart = L->ypart;
+    a.gate_part = L->gate_part;
+    a.up_part = L->up_part;
+    a.err = L->err_word;
+    a.n_only = 0;
+    return a;
+}
+
+// Expert MLPs for the experts of `a` (all with tokens, or a.only) into ypart;
+// returns the number of ypart splits written.
+moe_status_t run_experts(moe_layer_t *L, ExpertArgs &a, int regime, int *splits_out,
+                         cudaStream_t s) {
+    const moe_config_t &c = L->cfg;
+    const bool gated = c.expert == MOE_EXPERT_SWIGLU;
+    const int rows = a.T * a.k;
+    if (c.act_dtype == MOE_F32) {
+        a.n_rows_cap = rows;
+        moe_status_t st = launch_phase(L, MOE_PHASE_UP, s, "simt_up", [&] { return launch_simt_up(a, gated, s); });
+        if (st == MOE_OK)
+            st = launch_phase(L, MOE_PHASE_DOWN, s, "simt_down", [&] { return launch_simt_down(a, s); });
+        *splits_out = 1;
+        return st;
+    }
+    (void)regime;
+    const WeightType wt = (c.weight_dtype == MOE_I8) ? WeightType::kI8 : WeightType::kBF16;
+    int nt = decode_token_tiles(a.T, a.k, a.E);
+    int s_up, s_down;
+    if (rows <= static_cast<int>(L->decode_rows_cap)) {
+        s_up = splits_for(c.m, nt, 1);
+        s_down = splits_for(c.p, nt, 4);
+        a.n_rows_cap = static_cast<int>(L->decode_rows_cap);
+    } else {
+        return fail(MOE_ERR_UNSUPPORTED, "decode kernels take T*k <= %d", kDecodeMaxRows);
+    }
+    if (s_up > L->split_up_max || s_down > L->split_down_max)
+        return fail(MOE_ERR_INTERNAL, "split count exceeds workspace");
+    moe_status_t st = launch_phase(L, MOE_PHASE_UP, s, "decode_up",
+                                   [&] { return launch_decode_up(a, wt, gated, s_up, L->num_sms, s); });
+    if (st == MOE_OK && s_up > 1)
+        st = launch_phase(L, MOE_PHASE_UP_FINISH, s, "decode_up_finish",
+                          [&] { return launch_decode_up_finish(a, gated, s_up, s); });
+    if (st == MOE_OK)
+        st = launch_phase(L, MOE_PHASE_DOWN, s, "decode_down",
+                          [&] { return launch_decode_down(a, wt, s_down, L->num_sms, s); });
+    *splits_out = s_down;
+    return st;
+}
+
+moe_status_t run_combine(moe_layer_t *L, const moe_routing_t *r, int splits, int n_rows_cap,
+                         void *y, cudaStream_t s) {
+    CombineArgs ca{L->ypart, splits, static_cast<size_t>(n_rows_cap) * L->cfg.m, r->scatter_index,
+                   r->T, L->cfg.k, L->cfg.m, y, L->err_word};
+    return launch_phase(L, MOE_PHASE_COMBINE, s, "combine",
+                        [&] { return launch_combine(ca, L->cfg.act_dtype == MOE_BF16, s); });
+}
+
+}  // namespace moe
+
+extern "C" moe_status_t moe_forward(moe_layer_t *L, const void *x, const moe_routing_t *r,
+                                    void *y, void *stream) {
+    if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    moe_status_t st = check_routing(L, r);
+    if (st != MOE_OK) return st;
+    st = check_T(L, r->T);
+    if (st != MOE_OK) return st;
+    if (r->T == 0) return MOE_OK;
+    if (!x || !y || !aligned16(x) || !aligned16(y))
+        return fail(MOE_ERR_INVALID_ARG, "x or y is NULL or not 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (L->pool) return paged_forward(L, x, r, y, s);
+    ExpertArgs a = make_expert_args(L, x, r);
+    int splits = 1;
+    st = run_experts(L, a, L->regime, &splits, s);
+    if (st != MOE_OK) return st;
+    st = run_combine(L, r, splits, a.n_rows_cap, y, s);
+    if (st != MOE_OK) return st;
+    CUDA_TRY(cudaEventRecord(L->done, s));
+    return MOE_OK;
+}
+
+// ---- options, info, stats, checks ----------------------------------------------------
+extern "C" moe_status_t moe_layer_set_option(moe_layer_t *L, moe_option_t opt, int value) {
+    if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (opt == MOE_OPT_REGIME) {
+        if (value < 0 || value > 2) return fail(MOE_ERR_INVALID_ARG, "regime must be 0, 1 or 2");
+        L->regime = value;
+        return MOE_OK;
+    }
+    if (opt == MOE_OPT_TIMING) {
+        if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "timing must be 0 or 1");
+        L->timing = value != 0;
+        return MOE_OK;
+    }
+    return fail(MOE_ERR_INVALID_ARG, "unknown option %d", int(opt));
+}
+
+extern "C" moe_status_t moe_layer_timings(moe_layer_t *L, moe_timings_t *out, int reset) {
+    if (!L || !out) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    cudaSetDevice(L->device);
+    for (auto &pe : L->pending) {
+        CUDA_TRY(cudaEventSynchronize(pe.b));
+        float ms = 0.0f;
+        CUDA_TRY(cudaEventElapsedTime(&ms, pe.a, pe.b));
+        L->phase_ms[pe.phase] += ms;
+        L->phase_launches[pe.phase] += 1;
+        L->event_pool.push_back(pe.a);
+        L->event_pool.push_back(pe.b);
+    }
+    L->pending.clear();
+    for (int i = 0; i < MOE_NUM_PHASES; ++i) {
+        out->ms[i] = L->phase_ms[i];
+        out->launches[i] = L->phase_launches[i];
+        if (reset) {
+            L->phase_ms[i] = 0.0;
+            L->phase_launches[i] = 0;
+        }
+    }
+    return MOE_OK;
+}
+
+extern "C" moe_status_t moe_layer_info(const moe_layer_t *L, moe_layer_info_t *out) {
+    if (!L || !out) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    std::memset(out, 0, sizeof *out);
+    out->expert_bytes = L->expert_bytes;
+    out->weight_bytes = L->expert_bytes * L->cfg.E;
+    out->workspace_bytes = L->workspace_bytes;
+    out->decode_splits_up = L->split_up_max;
+    out->decode_splits_down = L->split_down_max;
+    out->num_sms = L->num_sms;
+    return MOE_OK;
+}
+
+extern "C" moe_status_t moe_layer_stats(moe_layer_t *L, moe_stats_t *out) {
+    if (!L || !out) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    *out = L->stats;
+    return MOE_OK;
+}
+
+extern "C" moe_status_t moe_layer_sync_check(moe_layer_t *L, int timeout_ms, uint32_t *flags) {
+    if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (flags) *flags = 0;
+    cudaSetDevice(L->device);
+    const auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+        cudaError_t q = cudaEventQuery(L->done);
+        if (q == cudaSuccess) break;
+        if (q != cudaErrorNotReady) return cuda_fail(q, "cudaEventQuery");
+        const auto el = std::chrono::duration_cast<std::chrono::milliseconds>(
+            std::chrono::steady_clock::now() - t0);
+        if (timeout_ms >= 0 && el.count() > timeout_ms)
+            return fail(MOE_ERR_TIMEOUT, "layer work not finished after %d ms", timeout_ms);
+        std::this_thread::sleep_for(std::chrono::microseconds(50));
+    }
+    uint32_t word = 0;
+    CUDA_TRY(cudaMemcpy(&word, L->err_word, 4, cudaMemcpyDeviceToHost));
+    if (word) {
+        CUDA_TRY(cudaMemset(L->err_word, 0, 4));
+        if (flags) *flags = word;
+        return fail(MOE_ERR_INVALID_ARG, "device flagged bad routing data (bits 0x%x)", word);
+    }
+    return MOE_OK;
+}
+
+extern "C" moe_status_t moe_layer_read_expert(const moe_layer_t *L, int expert, int which,
+                                              void *values, float *scales) {
+    if (!L || !values) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    const moe_config_t &c = L->cfg;
+    if (expert < 0 || expert >= c.E) return fail(MOE_ERR_INVALID_ARG, "expert out of range");
+    if (which < 1 || which > 3 || (which == 3 && c.expert != MOE_EXPERT_SWIGLU))
+        return fail(MOE_ERR_INVALID_ARG, "which must be 1, 2 or (SwiGLU) 3");
+    if (c.weight_dtype == MOE_I8 && !scales) return fail(MOE_ERR_INVALID_ARG, "scales is NULL");
+    if (L->pool) return fail(MOE_ERR_UNSUPPORTED, "read_expert on a paged layer");
+    cudaSetDevice(L->device);
+    const void *src = which == 1 ? L->tab.w1[expert] : which == 2 ? L->tab.w2[expert] : L->tab.w3[expert];
+    const float *ssrc = which == 1 ? L->tab.s1[expert] : which == 2 ? L->tab.s2[expert] : L->tab.s3[expert];
+    // stored transposed: rows = outputs, cols = reduction
+    const int out_rows = (which == 2) ? c.m : c.p, red = (which == 2) ? c.p : c.m;
+    const size_t el = (c.weight_dtype == MOE_I8) ? 1 : (c.weight_dtype == MOE_F32 ? 4 : 2);
+    std::vector<uint8_t> buf(static_cast<size_t>(out_rows) * red * el);
+    CUDA_TRY(cudaDeviceSynchronize());
+    CUDA_TRY(cudaMemcpy(buf.data(), src, buf.size(), cudaMemcpyDeviceToHost));
+    uint8_t *dst = static_cast<uint8_t *>(values);
+    for (int o = 0; o < out_rows; ++o)
+        for (int i = 0; i < red; ++i)
+            std::memcpy(dst + (static_cast<size_t>(i) * out_rows + o) * el,
+                        buf.data() + (static_cast<size_t>(o) * red + i) * el, el);
+    if (c.weight_dtype == MOE_I8)
+        CUDA_TRY(cudaMemcpy(scales, ssrc, static_cast<size_t>(out_rows) * 4, cudaMemcpyDeviceToHost));
+    return MOE_OK;
+}
+
+extern "C" const char *moe_status_string(moe_status_t s) {
+    switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported";
+    case MOE_ERR_OOM: return "out of memory";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "timeout";
+    case MOE_ERR_INTERNAL: return "internal error";
+    }
+    return "unknown status";
+}
+
+extern "C" const char *moe_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" int moe_version(void) { return 100; }

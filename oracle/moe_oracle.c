@@ -204,18 +204,21 @@ int moe_oracle_quantize_cols(const void *w, int w_dtype, int rows, int cols,
                              int8_t *q, float *scale) {
     if (!w || !q || !scale || rows <= 0 || cols <= 0 || w_dtype == OR_I8)
         return OR_BAD_ARG;
-    for (int c = 0; c < cols; ++c) {
-        float amax = 0.0f;
-        for (int r = 0; r < rows; ++r) {
+    /* column maxima, scanning the matrix row by row */
+    for (int c = 0; c < cols; ++c) scale[c] = 0.0f;
+    for (int r = 0; r < rows; ++r) {
+        for (int c = 0; c < cols; ++c) {
             float v = (float)elem(w, w_dtype, (size_t)r * cols + c);
             if (!isfinite(v)) return OR_NONFINITE;
-            if (fabsf(v) > amax) amax = fabsf(v);
+            if (fabsf(v) > scale[c]) scale[c] = fabsf(v);
         }
-        float s = (amax == 0.0f) ? 1.0f : (float)((double)amax / 127.0);
-        scale[c] = s;
-        for (int r = 0; r < rows; ++r) {
+    }
+    for (int c = 0; c < cols; ++c)
+        scale[c] = (scale[c] == 0.0f) ? 1.0f : (float)((double)scale[c] / 127.0);
+    for (int r = 0; r < rows; ++r) {
+        for (int c = 0; c < cols; ++c) {
             float v = (float)elem(w, w_dtype, (size_t)r * cols + c);
-            float ratio = (float)((double)v / (double)s);
+            float ratio = (float)((double)v / (double)scale[c]);
             double code = rint((double)ratio); /* default mode: half to even */
             if (code > 127.0) code = 127.0;
             if (code < -127.0) code = -127.0;

@@ -1,0 +1,94 @@
+"""The C-ABI library loads without a GPU, exports every entry point that
+include/moe_layer.h declares, and rejects bad arguments before touching the
+device.  Host-only arithmetic (the expert-cache geometry) is checked against
+the expert-cache article's own numbers.  No compute call runs here."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import mixture_experts_layer_gemm_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def _declared_functions():
+    src = open(moe.HEADER_PATH).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_function():
+    declared = _declared_functions()
+    assert len(declared) >= 15, declared
+    L = moe.lib()
+    missing = [n for n in declared if not hasattr(L, n)]
+    assert not missing, missing
+    # and the binding wraps each of them under the same name
+    assert sorted(moe.exported_names()) == declared
+
+
+def test_status_strings_and_version():
+    assert moe.moe_status_string(moe.MOE_OK) == "ok"
+    assert moe.moe_status_string(moe.MOE_ERR_TIMEOUT) == "timeout"
+    assert moe.moe_version() >= 100
+
+
+def test_create_rejects_bad_configs_before_touching_the_device():
+    L = moe.lib()
+    out = ctypes.c_void_p()
+    assert L.moe_layer_create(None, None, None, None, None, None, None, 0,
+                              ctypes.byref(out)) == moe.MOE_ERR_INVALID_ARG
+    bad = [
+        dict(E=0), dict(E=65), dict(k=0), dict(k=9), dict(m=0), dict(max_tokens=0),
+    ]
+    for change in bad:
+        c = dict(m=128, p=256, E=8, k=2, max_tokens=16, act_dtype=moe.MOE_F32,
+                 weight_dtype=moe.MOE_F32, expert=moe.MOE_EXPERT_RELU2, has_router_bias=0, paged=0)
+        c.update(change)
+        cfg = moe.moe_config_t(**c)
+        st = L.moe_layer_create(ctypes.byref(cfg), None, None, None, None, None, None, 0,
+                                ctypes.byref(out))
+        assert st == moe.MOE_ERR_INVALID_ARG, change
+    # valid shape but unsupported type combinations
+    for act, wt in [(moe.MOE_F32, moe.MOE_BF16), (moe.MOE_BF16, moe.MOE_F32),
+                    (moe.MOE_F32, moe.MOE_I8)]:
+        cfg = moe.moe_config_t(128, 256, 8, 2, 16, act, wt, moe.MOE_EXPERT_RELU2, 0, 0)
+        st = L.moe_layer_create(ctypes.byref(cfg), None, None, None, None, None, None, 0,
+                                ctypes.byref(out))
+        assert st == moe.MOE_ERR_UNSUPPORTED
+    cfg = moe.moe_config_t(100, 256, 8, 2, 16, moe.MOE_BF16, moe.MOE_BF16, moe.MOE_EXPERT_RELU2, 0, 0)
+    assert L.moe_layer_create(ctypes.byref(cfg), None, None, None, None, None, None, 0,
+                              ctypes.byref(out)) == moe.MOE_ERR_UNSUPPORTED
+    assert "64" in moe.moe_last_error()
+
+
+def test_calls_on_null_layer_are_rejected():
+    L = moe.lib()
+    r = moe.moe_routing_t()
+    assert L.moe_route(None, None, 1, ctypes.byref(r), None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_forward(None, None, ctypes.byref(r), None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_layer_set_option(None, 1, 0) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_destroy(None) == moe.MOE_OK
+
+
+def test_pool_geometry_matches_expert_cache_article():
+    """Expert-cache article, sections 2.2 and 5.1 (binary units)."""
+    cases = json.load(open(os.path.join(GOLDEN, "expert_cache_geometry.json")))["cases"]
+    MiB = 1 << 20
+    for c in cases:
+        n, slots = moe.moe_pool_geometry(int(c["available_mib"] * MiB), int(c["expert_mib"] * MiB),
+                                         c["ways"])
+        assert (n, slots) == (c["n_index"], c["usable_slots"]), c["note"]
+
+
+def test_pool_geometry_for_the_mixtral_slot_budget():
+    # a 16 GiB budget of 336 MiB bf16 Mixtral experts (3 x 4096 x 14336 x 2 bytes), 4-way
+    expert = 3 * 4096 * 14336 * 2
+    assert expert == 336 * (1 << 20)
+    assert moe.moe_pool_geometry(16 << 30, expert, 4) == (12, 48)
+    with pytest.raises(moe.MoeError):
+        moe.moe_pool_geometry(expert * 3, expert, 4)  # not even one set

@@ -1,0 +1,298 @@
+"""GPU parity of the whole MoE-layer path against the fp64 oracle, through the
+C ABI, on seeded inputs at sizes the oracle finishes in seconds (several
+tiles, ragged tails) plus the edge cases of the method.
+
+Bars: routing ids, counts, offsets and permutation bit-exact (top-k decided
+on the same fp32 logits, ties to the lower id; with the router fused in, only
+tokens whose oracle logits are closer than the fp32 accumulation bound may
+differ); outputs within a max-over-tokens relative L2 error of 1e-5 (fp32),
+1e-2 (bf16 weights), 3e-2 (int8 weights against the original weights) and
+1e-2 (int8 against the oracle's own dequantised weights)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_layer_gemm_gb300 as moe
+import oracle
+import workloads as wl
+from gpu_util import (TOL, Run, f64, max_token_rel_l2, near_tie_tokens, oracle_quantized,
+                      to_device)
+
+pytestmark = pytest.mark.gpu
+
+SWIGLU_BF16 = wl.LayerShape("small-swiglu-bf16", m=512, p=1024, E=8, k=2, expert=wl.SWIGLU,
+                            act="bf16", weight="bf16")
+RELU_BF16 = dataclasses.replace(SWIGLU_BF16, name="small-relu-bf16", expert=wl.RELU2)
+ODD_BF16 = wl.LayerShape("odd-swiglu-bf16", m=320, p=192, E=5, k=3, expert=wl.SWIGLU, act="bf16",
+                         weight="bf16")
+WIDE_E = wl.LayerShape("e64-swiglu-bf16", m=256, p=256, E=64, k=4, expert=wl.SWIGLU, act="bf16",
+                       weight="bf16")
+_KIND = {wl.RELU2: oracle.RELU2, wl.SWIGLU: oracle.SWIGLU}
+
+_layers = {}
+
+
+def get_layer(shape, seed=0):
+    key = (shape, seed)
+    if key not in _layers:
+        _layers[key] = wl.make_layer(shape, seed)
+    return _layers[key]
+
+
+def check_routing(run, layer, x):
+    """Routing parity; returns the (ids, weights) the oracle should use."""
+    s = layer.shape
+    logits, mag = oracle.router_logits(x, layer.w_router, layer.b_router, with_abssum=True)
+    oids, ow = oracle.topk(logits, s.k)
+    ties = near_tie_tokens(logits, mag, s.m, s.k)
+    keep = np.ones(run.T, bool)
+    keep[ties] = False
+    assert len(ties) <= max(1, run.T // 50), f"{len(ties)} near-tie tokens"
+    np.testing.assert_array_equal(run.ids[keep], oids[keep])
+    np.testing.assert_allclose(run.w[keep], ow[keep], rtol=0, atol=5e-5)
+    if run.logits is not None:
+        delta = 8.0 * s.m * 2.0 ** -24 * mag + 1e-30
+        assert np.all(np.abs(run.logits - logits) <= delta)
+    check_permutation(run, s.E)
+    ids = np.where(keep[:, None], oids, run.ids)
+    w = np.where(keep[:, None], ow, run.w.astype(np.float64))
+    return ids, w
+
+
+def check_permutation(run, E):
+    c, o, g, sc = oracle.permute(run.ids, E)
+    np.testing.assert_array_equal(run.counts, c)
+    np.testing.assert_array_equal(run.offsets, o)
+    np.testing.assert_array_equal(run.gather, g)
+    np.testing.assert_array_equal(run.scatter, sc)
+
+
+def oracle_y(layer, x, ids, w, quantized=None):
+    s = layer.shape
+    if quantized is None:
+        return oracle.layer(x, layer.w1, layer.w2, layer.w3, ids, w, _KIND[s.expert])
+    q = quantized
+    return oracle.layer(x, q["w1"], q["w2"], q["w3"], ids, w, _KIND[s.expert],
+                        scales=(q["s1"], q["s2"], q["s3"]))
+
+
+def run_and_check(shape, T, seed=0, regime=moe.REGIME_AUTO, locality=0.0, max_tokens=None):
+    layer = get_layer(shape, seed)
+    x = wl.make_tokens(shape, T, seed=seed + 1, locality=locality)
+    ml = moe.MoELayer(layer, max_tokens or max(T, 1), with_logits=True)
+    ml.set_regime(regime)
+    run = Run(ml, x)
+    assert ml.sync_check()[0] == moe.MOE_OK
+    ids, w = check_routing(run, layer, x)
+    y_ref = oracle_y(layer, x, ids, w)
+    rel, glob = max_token_rel_l2(run.y_np, y_ref)
+    tol = TOL[shape.weight]
+    if shape.weight == "i8":
+        qref = oracle_y(layer, x, ids, w, oracle_quantized(layer))
+        rel_q, _ = max_token_rel_l2(run.y_np, qref)
+        assert rel_q <= 1e-2, (rel_q, rel)
+    assert rel <= tol, (rel, glob)
+    ml.close()
+    return run, rel
+
+
+# ---- config 1: the tiny fp32 layer, exactly as specified -----------------------------
+def test_tiny_fp32_layer_matches_oracle():
+    run, rel = run_and_check(wl.TINY_FP32, 16, seed=0)
+    assert rel <= 1e-5
+
+
+@pytest.mark.parametrize("T", [1, 3, 16, 40])
+def test_tiny_fp32_other_batch_sizes(T):
+    run_and_check(wl.TINY_FP32, T, seed=2)
+
+
+# ---- top-k on the oracle's logits: bit-exact ----------------------------------------
+@pytest.mark.parametrize("E,k", [(8, 2), (16, 2), (64, 4), (5, 1), (8, 8)])
+def test_topk_from_oracle_logits_is_bit_exact(E, k):
+    shape = wl.LayerShape(f"topk-{E}-{k}", m=64, p=64, E=E, k=k, expert=wl.RELU2, act="bf16",
+                          weight="bf16")
+    layer = get_layer(shape, seed=3)
+    T = 300
+    r = np.random.default_rng(E * 100 + k)
+    x = wl.make_tokens(shape, T, seed=4)
+    logits = oracle.router_logits(x, layer.w_router).astype(np.float32)
+    # exact ties: whole rows of equal values, and small integers
+    logits[:20] = 0.5
+    logits[20:60] = r.integers(-2, 3, size=(40, E)).astype(np.float32)
+    ml = moe.MoELayer(layer, T)
+    run = Run(ml, x, routing="logits", logits=logits)
+    oids, ow = oracle.topk(logits.astype(np.float64), k)
+    np.testing.assert_array_equal(run.ids, oids)
+    np.testing.assert_allclose(run.w, ow, rtol=2e-6, atol=1e-7)
+    np.testing.assert_allclose(run.w.sum(axis=1), 1.0, atol=1e-5)
+    check_permutation(run, E)
+    ml.close()
+
+
+def test_fused_router_selection_equals_oracle_topk_on_gpu_logits():
+    """The fused kernel's choice is exactly top-k of the fp32 logits it wrote."""
+    layer = get_layer(SWIGLU_BF16, seed=5)
+    x = wl.make_tokens(SWIGLU_BF16, 257, seed=6)
+    ml = moe.MoELayer(layer, 257, with_logits=True)
+    run = Run(ml, x)
+    oids, ow = oracle.topk(run.logits.astype(np.float64), SWIGLU_BF16.k)
+    np.testing.assert_array_equal(run.ids, oids)
+    np.testing.assert_allclose(run.w, ow, rtol=2e-6, atol=1e-7)
+    ml.close()
+
+
+# ---- bf16 layers through the decode kernels ------------------------------------------
+@pytest.mark.parametrize("T", [1, 4, 16, 37, 64, 200])
+def test_swiglu_bf16_decode(T):
+    run_and_check(SWIGLU_BF16, T, seed=7, regime=moe.REGIME_DECODE)
+
+
+@pytest.mark.parametrize("T", [1, 23, 64])
+def test_relu_bf16_decode(T):
+    run_and_check(RELU_BF16, T, seed=8, regime=moe.REGIME_DECODE)
+
+
+@pytest.mark.parametrize("T", [2, 33, 100])
+def test_odd_shapes_bf16(T):
+    """m=320, p=192, E=5, k=3: splits that do not divide the reduction evenly."""
+    run_and_check(ODD_BF16, T, seed=9, regime=moe.REGIME_DECODE)
+
+
+def test_64_experts_top4():
+    run_and_check(WIDE_E, 50, seed=10)
+
+
+def test_router_bias_skews_routing():
+    shape = SWIGLU_BF16.with_zipf(1.2)
+    run, _ = run_and_check(shape, 120, seed=11)
+    assert run.counts[0] == run.counts.max()
+
+
+def test_temporal_locality_tokens():
+    run, _ = run_and_check(SWIGLU_BF16, 64, seed=12, locality=0.5)
+
+
+# ---- int8 weights ------------------------------------------------------------------------
+I8 = SWIGLU_BF16.with_weight("i8")
+
+
+def test_int8_codes_and_scales_bit_exact():
+    layer = get_layer(I8, seed=13)
+    ml = moe.MoELayer(layer, 4)
+    q = oracle_quantized(layer)
+    s = I8
+    for e in (0, 3, 7):
+        for which, key, shp in ((1, "w1", (s.m, s.p)), (2, "w2", (s.p, s.m)), (3, "w3", (s.m, s.p))):
+            codes, scales = moe.moe_layer_read_expert(ml.handle, e, which, shp, np.int8)
+            np.testing.assert_array_equal(codes, q[key][e])
+            np.testing.assert_array_equal(scales, q["s" + key[1]][e])
+    info = ml.info()
+    assert info.expert_bytes == 3 * s.m * s.p + (2 * s.p + s.m) * 4
+    ml.close()
+
+
+@pytest.mark.parametrize("T", [1, 16, 64])
+def test_int8_decode(T):
+    run_and_check(I8, T, seed=14)
+
+
+# ---- edge cases ------------------------------------------------------------------------
+def test_zero_tokens():
+    layer = get_layer(SWIGLU_BF16, seed=15)
+    ml = moe.MoELayer(layer, 8)
+    x = torch.zeros((0, SWIGLU_BF16.m), dtype=torch.bfloat16, device="cuda")
+    ml.counts.fill_(-1)
+    ml.offsets.fill_(-1)
+    ml.route(x, T=0)
+    y = torch.empty((0, SWIGLU_BF16.m), dtype=torch.bfloat16, device="cuda")
+    ml.forward(x, y)
+    torch.cuda.synchronize()
+    assert ml.counts.cpu().tolist() == [0] * 8
+    assert ml.offsets.cpu().tolist() == [0] * 9
+    ml.close()
+
+
+def test_all_tokens_to_two_experts_multi_pass():
+    """Every token picks experts (0, 1): q = T for both, many token passes."""
+    layer = get_layer(SWIGLU_BF16, seed=16)
+    T = 45
+    x = wl.make_tokens(SWIGLU_BF16, T, seed=17)
+    ids = np.tile(np.array([[1, 0]], np.int32), (T, 1))
+    w = np.tile(np.array([[0.7, 0.3]], np.float32), (T, 1))
+    ml = moe.MoELayer(layer, T)
+    ml.set_regime(moe.REGIME_DECODE)
+    run = Run(ml, x, routing="topk", ids=ids, w=w)
+    assert ml.sync_check()[0] == moe.MOE_OK
+    check_permutation(run, 8)
+    np.testing.assert_array_equal(run.ids, ids)
+    y_ref = oracle_y(layer, x, ids, w.astype(np.float64))
+    rel, _ = max_token_rel_l2(run.y_np, y_ref)
+    assert rel <= 1e-2
+    ml.close()
+
+
+def test_bad_topk_ids_are_flagged_not_faulted():
+    layer = get_layer(SWIGLU_BF16, seed=18)
+    T = 6
+    x = wl.make_tokens(SWIGLU_BF16, T, seed=19)
+    ids = np.array([[0, 1], [8, 2], [-1, 3], [4, 4], [5, 6], [7, 0]], np.int32)
+    w = np.full((T, 2), 0.5, np.float32)
+    ml = moe.MoELayer(layer, T)
+    run = Run(ml, x, routing="topk", ids=ids, w=w)
+    st, flags = ml.sync_check()
+    assert st == moe.MOE_ERR_INVALID_ARG
+    assert flags & 1 and flags & 2  # out-of-range id, repeated id
+    assert run.ids[1, 0] == 0 and run.ids[2, 0] == 0  # sent to expert 0
+    assert ml.sync_check()[0] == moe.MOE_OK  # the word was cleared
+    check_permutation(run, 8)
+    ml.close()
+
+
+def test_t_equals_max_tokens_and_reuse():
+    layer = get_layer(SWIGLU_BF16, seed=20)
+    ml = moe.MoELayer(layer, 24, with_logits=True)
+    for T in (24, 3, 24):
+        x = wl.make_tokens(SWIGLU_BF16, T, seed=21 + T)
+        run = Run(ml, x)
+        ids, w = check_routing(run, layer, x)
+        rel, _ = max_token_rel_l2(run.y_np, oracle_y(layer, x, ids, w))
+        assert rel <= 1e-2
+    with pytest.raises(moe.MoeError):
+        ml.route(to_device(wl.make_tokens(SWIGLU_BF16, 25, seed=1)))
+    ml.close()
+
+
+def test_single_expert_top1_is_a_dense_mlp():
+    shape = wl.LayerShape("dense", m=256, p=512, E=1, k=1, expert=wl.SWIGLU, act="bf16",
+                          weight="bf16")
+    run, _ = run_and_check(shape, 12, seed=22)
+    assert (run.ids == 0).all() and np.all(run.w == 1.0)
+
+
+def test_deterministic_bitwise():
+    layer = get_layer(SWIGLU_BF16, seed=23)
+    x = wl.make_tokens(SWIGLU_BF16, 64, seed=24)
+    ml = moe.MoELayer(layer, 64)
+    a = Run(ml, x).y_np.copy()
+    b = Run(ml, x).y_np.copy()
+    np.testing.assert_array_equal(a, b)
+    ml.close()
+
+
+def test_identical_experts_output_is_routing_independent():
+    """All experts equal and weights summing to one: y = expert(x) whatever
+    the routing (a property that holds at any size)."""
+    base = get_layer(SWIGLU_BF16, seed=25)
+    same = wl.Layer(SWIGLU_BF16, base.w_router, None, [base.w1[0]] * 8, [base.w2[0]] * 8,
+                    [base.w3[0]] * 8)
+    x = wl.make_tokens(SWIGLU_BF16, 20, seed=26)
+    ml = moe.MoELayer(same, 20)
+    run = Run(ml, x)
+    y1 = oracle.layer(x, [base.w1[0]], [base.w2[0]], [base.w3[0]], np.zeros((20, 1), np.int32),
+                      np.ones((20, 1)), oracle.SWIGLU)
+    rel, _ = max_token_rel_l2(run.y_np, y1)
+    assert rel <= 1e-2
+    ml.close()

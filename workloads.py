@@ -81,9 +81,10 @@ PHI_TOKENS = (1, 8, 64, 512, 4096)
 
 
 def zipf_bias(E: int, s: float) -> np.ndarray:
-    """b_e = ln P(e), P(e) proportional to (e+1)^-s (expert 0 hottest)."""
+    """b_e = ln P(e), P(e) proportional to (e+1)^-s (expert 0 hottest), as the
+    fp32 values both the library and the oracle receive."""
     w = np.array([(e + 1.0) ** (-s) for e in range(E)], dtype=np.float64)
-    return np.log(w / w.sum())
+    return np.log(w / w.sum()).astype(np.float32)
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:
