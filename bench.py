@@ -43,7 +43,17 @@ def parse():
     ap.add_argument("--weights", default="bf16", choices=["bf16", "i8"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--tokens", default="1,4,16,64",
+                    help="decode batches per step (profiling runs use one)")
+    ap.add_argument("--copies", type=int, default=2, help="weight copies that alternate")
+    ap.add_argument("--shape", default="mixtral", choices=["mixtral", "phi", "small"],
+                    help="mixtral (the benchmark), phi (Phi-3.5-MoE), small (profiling: "
+                         "m=4096, p=3584, E=8, 0.7 GB of weights)")
+    args = ap.parse_args()
+    global TOKENS
+    TOKENS = tuple(int(t) for t in args.tokens.split(","))
+    return args
 
 
 def peaks():
@@ -167,9 +177,19 @@ def make_inputs(shape, seed, device):
     return layer, xs
 
 
+def shape_of(args):
+    import dataclasses
+
+    import workloads as wl
+    base = {"mixtral": wl.MIXTRAL, "phi": wl.PHI35,
+            "small": dataclasses.replace(wl.MIXTRAL, name="profile-small", p=3584)}[args.shape]
+    return base if args.weights == "bf16" else base.with_weight("i8")
+
+
 def workload_config(shape, weights, flush_note):
-    return {"workload": f"mixtral-8x7b moe layer decode, T in {{1,4,16,64}}, {weights} weights",
-            "model": "mixtral-8x7b-shaped single MoE FFN layer", "m": shape.m, "p": shape.p,
+    ts = ",".join(str(t) for t in TOKENS)
+    return {"workload": f"{shape.name} moe layer decode, T in {{{ts}}}, {weights} weights",
+            "model": f"{shape.name}-shaped single MoE FFN layer", "m": shape.m, "p": shape.p,
             "E": shape.E, "k": shape.k, "expert": "swiglu", "tokens_per_step": sum(TOKENS),
             "global_batch": sum(TOKENS), "seq_len": 1, "parallelism": "replicas",
             "l2": flush_note}
@@ -179,10 +199,10 @@ def run_reference(args, world, rank):
     import workloads as wl
     if rank != 0:
         return
-    shape = wl.MIXTRAL if args.weights == "bf16" else wl.MIXTRAL.with_weight("i8")
+    shape = shape_of(args)
     import torch
     device = "cuda" if torch.cuda.is_available() else "cpu"
-    layer, xs = make_inputs(wl.MIXTRAL, args.seed, device)
+    layer, xs = make_inputs(shape, args.seed, device)
     sample = {1: 1, 4: 1, 16: 0, 64: 0}   # 2 tokens of experts per step, every token routed
     for _ in range(args.warmup):
         oracle_sample(layer, xs, sample)
@@ -229,10 +249,10 @@ def run_ours(args, world, rank, local):
     from mixture_experts_layer_gemm_gb300 import build as lib_build
 
     lib_build.build()
-    shape = wl.MIXTRAL if args.weights == "bf16" else wl.MIXTRAL.with_weight("i8")
+    shape = shape_of(args)
     layer, xs_np = make_inputs(shape, args.seed + rank, f"cuda:{local}")
     max_t = max(TOKENS)
-    copies = [moe.MoELayer(layer, max_t) for _ in range(2)]
+    copies = [moe.MoELayer(layer, max_t) for _ in range(max(args.copies, 1))]
     dev = torch.device("cuda", local)
     xs = {T: torch.from_numpy(xs_np[T].view(np.int16).copy()).view(torch.bfloat16).to(dev)
           for T in TOKENS}
@@ -241,7 +261,7 @@ def run_ours(args, world, rank, local):
 
     def step():
         for i, T in enumerate(TOKENS):
-            c = copies[i % 2]
+            c = copies[i % len(copies)]
             c.route(xs[T], stream=stream)
             c.forward(xs[T], ys[T], stream=stream)
 
@@ -281,7 +301,7 @@ def run_ours(args, world, rank, local):
     wbytes = 1 if args.weights == "i8" else 2
     bytes_up, bytes_down, active = 0, 0, {}
     for i, T in enumerate(TOKENS):
-        c = copies[i % 2]
+        c = copies[i % len(copies)]
         c.route(xs[T], stream=stream)
         torch.cuda.synchronize()
         n_act = int((c.counts.cpu() > 0).sum())
@@ -315,33 +335,35 @@ def run_ours(args, world, rank, local):
 
     def step_e2e():
         for i, T in enumerate(TOKENS):
-            c = copies[i % 2]
+            c = copies[i % len(copies)]
             xd[T].copy_(xh[T], non_blocking=True)
             c.route(xd[T], stream=stream)
             c.forward(xd[T], ys[T], stream=stream)
             yh[T].copy_(ys[T], non_blocking=True)
 
-    for _ in range(3):
-        step_e2e()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     k_e2e = max(args.steps // 2, 1)
-    e0.record(stream)
-    for _ in range(k_e2e):
-        step_e2e()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1))
+    e2e_ms = None
+    if not args.no_e2e:
+        for _ in range(3):
+            step_e2e()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k_e2e):
+            step_e2e()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(world, e0.elapsed_time(e1))
     io_bytes = sum(T * shape.m * 2 for T in TOKENS)
 
     tokens_step = sum(TOKENS)
     value = world * tokens_step * args.steps / (ms_max * 1e-3)
-    e2e_value = world * tokens_step * k_e2e / (e2e_ms * 1e-3)
+    e2e_value = world * tokens_step * k_e2e / (e2e_ms * 1e-3) if e2e_ms else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sample = {1: 1, 4: 4, 16: 16, 64: 16}
+        sample = {T: min(T, 16) for T in TOKENS}
         t0 = time.perf_counter()
         n = oracle_sample(layer, xs_np, sample)
         dt = time.perf_counter() - t0

@@ -4,133 +4,125 @@
 // matmuls are bound by reading the weights once from HBM (DeepSpeed-Inference
 // article, part 1: small-batch inference is limited by the bandwidth of
 // reading the weights; the expert-cache article, section 1: a Mixtral expert
-// takes 0.3 ms on an RTX 4090, i.e. one pass over its ~340 MB).  The kernel
-// follows the three parts of SBI-GeMM (DeepSpeed-Inference article, part 3):
-//   1. tiling: a work unit is 16 weight rows (outputs) of one expert, so the
-//      reduction stays inside the unit; where the outputs alone would not give
-//      every SM enough units, the reduction dimension is split across units too
-//      (the two-kernel variant) and a second pass adds the partial sums;
-//   2. reduction: the 8 warps of a CTA each reduce one slice of the unit's
-//      reduction range; their partial tiles are written to shared memory in a
-//      transposed layout that puts the 8 partials of one output next to each
-//      other, and one thread per output adds them;
-//   3. full cache lines: weights are stored transposed at create time (each
-//      output's reduction run is contiguous), and every lane reads 16 bytes
-//      per load -- 8 bf16 or 16 int8 values -- so each warp load covers whole
-//      32-byte sectors.
-// Different from the pages: the per-warp dot products run on the warp-level
-// tensor-core MMA (m16n8k16, bf16 in, fp32 accumulate) with the tokens on the
-// N side, because from about four tokens per expert on, CUDA-core FMAs cannot
-// keep pace with GB300's HBM.  Since a dot product does not depend on the
-// order of its terms, each lane's 16-byte run of weights and the matching
-// 16-byte run of the token row are assigned to the fragment slots of two
-// (bf16) or four (int8) MMAs with the same permutation of the reduction
-// index, so both operands come from contiguous vector loads.
-// int8 weights are widened to bf16 in registers (exact) and the per-output
-// scale is applied after the dot product.
+// takes 0.3 ms on an RTX 4090, one pass over its ~340 MB).  The kernel follows
+// SBI-GeMM (DeepSpeed-Inference article, part 3):
+//   1. tiling along the outputs: a work unit is 128 stored weight rows of one
+//      expert (8 row-groups of 16, one per consumer warp), so the reduction
+//      stays inside the unit; where the outputs alone would not give every SM
+//      enough units, the reduction range is split across units too (the
+//      two-kernel variant) and a later pass adds the partial sums in a fixed
+//      order (the up-projection finish kernel, or the combine);
+//   2. reduction: inside a warp the tensor-core MMA reduces across lanes, and
+//      each warp owns its 16 rows, so no cross-warp reduction is needed;
+//   3. full cache lines: weights are stored transposed and tiled at create
+//      time (packing.h), so the 8 row-groups of one reduction block are one
+//      contiguous 16 KB run, and a warp's 16-byte-per-lane shared-memory read
+//      covers one 512-byte atom without bank conflicts.
+// GB300-specific design:
+//   - one producer thread streams each unit's 16 KB weight stages from HBM
+//     with bulk asynchronous copies (the TMA engine) into a 6-stage
+//     shared-memory ring guarded by mbarriers, so up to 96 KB per SM are in
+//     flight whatever the register budget;
+//   - the per-warp dot products run on the warp-level tensor-core MMA
+//     (m16n8k16, bf16 in, fp32 accumulate) with the tokens on the N side:
+//     from about four tokens per expert on, CUDA-core FMAs cannot keep pace
+//     with HBM.  A dot product does not depend on the order of its terms, so
+//     lane (g, t) takes the 16-byte run t of weight rows g and g+8 and the
+//     16-byte run t of its token row, and feeds them to two (bf16) or four
+//     (int8) MMAs under one shared permutation of the reduction index;
+//   - the token rows of the current expert and split are staged once in
+//     shared memory and reused by every unit of that expert;
+//   - int8 weights are widened to bf16 in registers (exact) and the
+//     per-output scale is applied after the dot product.
+// Every wait is bounded; a wait that gives up sets kErrWaitTimeout in the
+// layer's error word and the CTA drains its copies in flight and returns.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "packing.h"
 
 namespace moe {
 
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;  // + one producer warp
+constexpr int kStages = 6;
+constexpr int kBlocksPerStage = 8;
+constexpr int kStageBytes = kBlocksPerStage * kBlockBytes;  // 16 KB
 constexpr int kRowsPerUnit = 16;
-constexpr int kUnroll = 8;
+constexpr uint32_t kBarConsumers = 1;  // named barrier id for the consumer warps
 
 template <WeightType WT>
 struct WTraits;
 template <>
 struct WTraits<WeightType::kBF16> {
-    static constexpr int kStep = 32;    // reduction elements per warp step
-    static constexpr int kPad = 64;     // smem row padding (bank-conflict-free B reads)
     static constexpr int kElem = 2;
+    static constexpr int kBK = 64;      // reduction elements per 2 KB block
+    static constexpr int kPad = 64;     // staged token-row padding: conflict-free B reads
 };
 template <>
 struct WTraits<WeightType::kI8> {
-    static constexpr int kStep = 64;
-    static constexpr int kPad = 16;
     static constexpr int kElem = 1;
+    static constexpr int kBK = 128;
+    static constexpr int kPad = 16;
 };
 
 enum Phase { kUp = 0, kDown = 1 };
 
 struct DecodeGeom {
     int K;          // reduction length (m for up, p for down)
-    int splits;     // split of the reduction across units
-    int nsteps;     // K / kStep
-    int kr_max;     // largest split in elements, rounded up to 64
+    int rg;         // row-groups of 16 stored rows
+    int rg8;        // units along the rows: ceil(rg / 8)
+    int splits;     // split of the K-blocks across units
+    int nkb;        // K / BK
     int row_bytes;  // smem stride of one staged token row
-    int rg;         // row groups (units along the output) per expert
+    int bstage_bytes;
 };
 
-__device__ __forceinline__ int split_begin(int nsteps, int splits, int ks) {
-    return static_cast<int>((static_cast<long long>(nsteps) * ks) / splits);
+__device__ __forceinline__ int split_begin(int n, int splits, int ks) {
+    return static_cast<int>((static_cast<long long>(n) * ks) / splits);
 }
 
-// Load one step of A (weights) for rows g and g+8 of the unit.
-template <WeightType WT>
-__device__ __forceinline__ void load_a(const uint8_t *row_g, const uint8_t *row_g8, int kelem,
-                                       uint4 &ra, uint4 &rb) {
-    ra = ld_stream_v4(row_g + static_cast<size_t>(kelem) * WTraits<WT>::kElem);
-    rb = ld_stream_v4(row_g8 + static_cast<size_t>(kelem) * WTraits<WT>::kElem);
-}
+struct Unit {
+    int e, ks, g8, nrg, off, end, kb0, kb1;
+    bool ok;
+};
 
-// One warp step: A fragments from the loaded weight runs, B fragments from the
-// staged token rows (smem), MMAs into acc.
-template <WeightType WT, int NT>
-__device__ __forceinline__ void mma_step(float (&acc)[NT][4], const uint4 &ra, const uint4 &rb,
-                                         uint32_t bsm, int row_bytes, int g, int t, int kcol) {
-    if constexpr (WT == WeightType::kBF16) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const uint4 xb = lds_v4(bsm + (nt * 8 + g) * row_bytes + (kcol + 8 * t) * 2);
-            mma_bf16_16816(acc[nt], ra.x, rb.x, ra.y, rb.y, xb.x, xb.y);
-            mma_bf16_16816(acc[nt], ra.z, rb.z, ra.w, rb.w, xb.z, xb.w);
-        }
-    } else {
-        uint32_t al[4], ah[4], bl[4], bh[4];
-        const uint32_t va[4] = {ra.x, ra.y, ra.z, ra.w};
-        const uint32_t vb[4] = {rb.x, rb.y, rb.z, rb.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            i8x4_to_bf16x2x2(va[i], al[i], ah[i]);
-            i8x4_to_bf16x2x2(vb[i], bl[i], bh[i]);
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const uint32_t base = bsm + (nt * 8 + g) * row_bytes + (kcol + 16 * t) * 2;
-            const uint4 x0 = lds_v4(base);
-            const uint4 x1 = lds_v4(base + 16);
-            mma_bf16_16816(acc[nt], al[0], bl[0], ah[0], bh[0], x0.x, x0.y);
-            mma_bf16_16816(acc[nt], al[1], bl[1], ah[1], bh[1], x0.z, x0.w);
-            mma_bf16_16816(acc[nt], al[2], bl[2], ah[2], bh[2], x1.x, x1.y);
-            mma_bf16_16816(acc[nt], al[3], bl[3], ah[3], bh[3], x1.z, x1.w);
-        }
-    }
+__device__ __forceinline__ Unit decode_unit(long long u, const int *s_act, const DecodeGeom &geo,
+                                            const ExpertArgs &a, int rows_total) {
+    Unit U;
+    U.g8 = static_cast<int>(u % geo.rg8);
+    U.ks = static_cast<int>((u / geo.rg8) % geo.splits);
+    U.e = s_act[static_cast<int>(u / (static_cast<long long>(geo.rg8) * geo.splits))];
+    U.nrg = min(8, geo.rg - 8 * U.g8);
+    U.off = a.offsets[U.e];
+    U.end = a.offsets[U.e + 1];
+    U.ok = !(U.off < 0 || U.end > rows_total || U.end < U.off);
+    U.kb0 = split_begin(geo.nkb, geo.splits, U.ks);
+    U.kb1 = split_begin(geo.nkb, geo.splits, U.ks + 1);
+    return U;
 }
 
 template <WeightType WT, int PHASE, bool GATED, int NT>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const ExpertTables tab, const ExpertArgs a, const DecodeGeom geo) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int kTok = 8 * NT;                  // tokens per pass
-    constexpr int kOut = kRowsPerUnit * kTok;     // outputs of one unit-pass
-    constexpr int kStep = WTraits<WT>::kStep;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr int kTok = 8 * NT;  // tokens per pass
+    constexpr int kBK = WTraits<WT>::kBK;
+    __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
     __shared__ int s_act[kMaxExperts];
     __shared__ int s_nact;
+    __shared__ volatile int s_abort;
 
-    uint8_t *bstage = smem;
-    float *red = reinterpret_cast<float *>(smem + static_cast<size_t>(kTok) * geo.row_bytes);
+    uint8_t *ring = smem;
+    uint8_t *bstage = smem + kStages * kStageBytes;
     const uint32_t bsm = smem_u32(bstage);
+    const uint32_t ring_sm = smem_u32(ring);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, t = lane & 3;
     const int rows_total = a.T * a.k;
 
-    // active expert list (in expert order)
     if (tid == 0) {
         int n = 0;
         if (a.n_only > 0) {
@@ -140,165 +132,232 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (a.offsets[e + 1] > a.offsets[e]) s_act[n++] = e;
         }
         s_nact = n;
+        s_abort = 0;
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&empty_bar[i], kConsumerWarps);
+        }
+        fence_barrier_init();
     }
     __syncthreads();
-    const int nact = s_nact;
-    const long long units = static_cast<long long>(nact) * geo.splits * geo.rg;
+    const long long units = static_cast<long long>(s_nact) * geo.splits * geo.rg8;
 
+    if (warp == kConsumerWarps) {
+        // ================= producer: stream weight stages into the ring ==========
+        // A slot is re-armed only after all consumer warps released it, which
+        // they do only after seeing its copy land; so at any time each slot
+        // has at most one phase in flight, the last one issued.
+        uint32_t last_parity[kStages];
+        bool used[kStages];
+        for (int i = 0; i < kStages; ++i) used[i] = false;
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (long long u = blockIdx.x; u < units && !s_abort; u += gridDim.x) {
+                const Unit U = decode_unit(u, s_act, geo, a, rows_total);
+                if (!U.ok) continue;
+                const uint8_t *w = static_cast<const uint8_t *>(PHASE == kUp ? tab.w1[U.e] : tab.w2[U.e]);
+                const uint32_t bytes = static_cast<uint32_t>(U.nrg) * kBlockBytes;
+                const int q = U.end - U.off;
+                for (int tp = 0; tp * kTok < q && !s_abort; ++tp) {
+                    for (int kb = U.kb0; kb < U.kb1; ++kb) {
+                        if (!mbar_wait(&empty_bar[stage], phase ^ 1u)) {
+                            flag_error(a.err, kErrWaitTimeout);
+                            s_abort = 1;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full_bar[stage], bytes);
+                        const size_t blk = static_cast<size_t>(kb) * geo.rg + 8 * U.g8;
+                        bulk_g2s(ring + stage * kStageBytes, w + blk * kBlockBytes, bytes,
+                                 &full_bar[stage]);
+                        used[stage] = true;
+                        last_parity[stage] = phase;
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        __syncthreads();  // consumers are done
+        if (lane == 0) {
+            // no copy may be in flight when the CTA exits (matters on the abort path)
+            for (int i = 0; i < kStages; ++i)
+                if (used[i]) mbar_wait(&full_bar[i], last_parity[i]);
+        }
+        return;
+    }
+
+    // ================= consumers: warp w owns row-group 8*g8 + w of each unit ======
+    const int g = lane >> 2, t = lane & 3;
+    int stage = 0;
+    uint32_t phase = 0;
     int staged_e = -1, staged_ks = -1, staged_tp = -1;
     for (long long u = blockIdx.x; u < units; u += gridDim.x) {
-        const int rg = static_cast<int>(u % geo.rg);
-        const int ks = static_cast<int>((u / geo.rg) % geo.splits);
-        const int e = s_act[static_cast<int>(u / (static_cast<long long>(geo.rg) * geo.splits))];
-        int off = a.offsets[e], end = a.offsets[e + 1];
-        if (off < 0 || end > rows_total || end < off) {  // corrupt tables: skip the expert
+        // one decision for all consumer warps: the named barriers need all of them
+        if (named_sync_or(kBarConsumers, kConsumers, s_abort)) break;
+        const Unit U = decode_unit(u, s_act, geo, a, rows_total);
+        if (!U.ok) {
             if (tid == 0) flag_error(a.err, kErrOffsets);
             continue;
         }
-        const int q = end - off;
-        const int s0 = split_begin(geo.nsteps, geo.splits, ks);
-        const int s1 = split_begin(geo.nsteps, geo.splits, ks + 1);
-        const int kbase = s0 * kStep;                    // first reduction element of the split
-        const int kcount = (s1 - s0) * kStep;
-        // weight rows of this unit
-        const uint8_t *row_g, *row_g8;
-        {
-            const size_t K = static_cast<size_t>(geo.K) * WTraits<WT>::kElem;
-            if (PHASE == kUp) {
-                const uint8_t *w1 = static_cast<const uint8_t *>(tab.w1[e]);
-                if (GATED) {
-                    const uint8_t *w3 = static_cast<const uint8_t *>(tab.w3[e]);
-                    row_g = w1 + static_cast<size_t>(rg * 8 + g) * K;
-                    row_g8 = w3 + static_cast<size_t>(rg * 8 + g) * K;
-                } else {
-                    row_g = w1 + static_cast<size_t>(rg * 16 + g) * K;
-                    row_g8 = w1 + static_cast<size_t>(rg * 16 + 8 + g) * K;
-                }
-            } else {
-                const uint8_t *w2 = static_cast<const uint8_t *>(tab.w2[e]);
-                row_g = w2 + static_cast<size_t>(rg * 16 + g) * K;
-                row_g8 = w2 + static_cast<size_t>(rg * 16 + 8 + g) * K;
-            }
-            row_g += static_cast<size_t>(kbase) * WTraits<WT>::kElem;
-            row_g8 += static_cast<size_t>(kbase) * WTraits<WT>::kElem;
-        }
-        const int lane_k = (WT == WeightType::kBF16) ? 8 * t : 16 * t;
-        // this warp's slice of the split's steps
-        const int nst = s1 - s0;
-        const int w0 = s0 + (nst * warp) / kWarps, w1e = s0 + (nst * (warp + 1)) / kWarps;
-
+        const int q = U.end - U.off;
+        const int kbase = U.kb0 * kBK;                 // first reduction element of the split
+        const int kcount = (U.kb1 - U.kb0) * kBK;
+        const bool mine = warp < U.nrg;
+        const int rg = 8 * U.g8 + warp;
         for (int tp = 0; tp * kTok < q; ++tp) {
-            // ---- stage the token rows of this pass (bf16) into shared memory
-            if (staged_e != e || staged_ks != ks || staged_tp != tp) {
-                __syncthreads();
-                const int vec_per_row = kcount / 8;  // 16-byte vectors
-                for (int idx = tid; idx < kTok * vec_per_row; idx += kThreads) {
+            // ---- stage this pass's token rows (bf16) in shared memory
+            if (staged_e != U.e || staged_ks != U.ks || staged_tp != tp) {
+                named_sync(kBarConsumers, kConsumers);
+                const int vec_per_row = kcount / 8;
+                for (int idx = tid; idx < kTok * vec_per_row; idx += kConsumers) {
                     const int r = idx / vec_per_row, v = idx - r * vec_per_row;
-                    const int pos = off + tp * kTok + r;
+                    const int pos = U.off + tp * kTok + r;
                     uint4 val = make_uint4(0, 0, 0, 0);
-                    if (pos < end) {
-                        const uint16_t *src;
+                    if (pos < U.end) {
                         if (PHASE == kUp) {
                             const int fi = a.gather[pos];
                             if (fi >= 0 && fi < rows_total) {
-                                src = static_cast<const uint16_t *>(a.x) +
-                                      static_cast<size_t>(fi / a.k) * geo.K;
+                                const uint16_t *src = static_cast<const uint16_t *>(a.x) +
+                                                      static_cast<size_t>(fi / a.k) * geo.K;
                                 val = ld_nc_v4(src + kbase + v * 8);
                             } else if (v == 0) {
                                 flag_error(a.err, kErrGatherIndex);
                             }
                         } else {
-                            src = static_cast<const uint16_t *>(a.h) + static_cast<size_t>(pos) * geo.K;
+                            const uint16_t *src =
+                                static_cast<const uint16_t *>(a.h) + static_cast<size_t>(pos) * geo.K;
                             val = ld_nc_v4(src + kbase + v * 8);
                         }
                     }
                     *reinterpret_cast<uint4 *>(bstage + static_cast<size_t>(r) * geo.row_bytes + v * 16) = val;
                 }
-                staged_e = e;
-                staged_ks = ks;
+                staged_e = U.e;
+                staged_ks = U.ks;
                 staged_tp = tp;
-                __syncthreads();
+                named_sync(kBarConsumers, kConsumers);
             }
-            // ---- stream this warp's weight slice
             float acc[NT][4];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
-            for (int s = w0; s < w1e; s += kUnroll) {
-                uint4 ra[kUnroll], rb[kUnroll];
-#pragma unroll
-                for (int i = 0; i < kUnroll; ++i)
-                    if (s + i < w1e) load_a<WT>(row_g, row_g8, (s + i - s0) * kStep + lane_k, ra[i], rb[i]);
-#pragma unroll
-                for (int i = 0; i < kUnroll; ++i)
-                    if (s + i < w1e)
-                        mma_step<WT, NT>(acc, ra[i], rb[i], bsm, geo.row_bytes, g, t, (s + i - s0) * kStep);
-            }
-            // ---- transposed partial tile: red[out * 8 + warp]
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int c0 = nt * 8 + 2 * t;
-                red[((g)*kTok + c0) * kWarps + warp] = acc[nt][0];
-                red[((g)*kTok + c0 + 1) * kWarps + warp] = acc[nt][1];
-                red[((g + 8) * kTok + c0) * kWarps + warp] = acc[nt][2];
-                red[((g + 8) * kTok + c0 + 1) * kWarps + warp] = acc[nt][3];
-            }
-            __syncthreads();
-            // ---- one thread per output adds the 8 partials, then the epilogue
-            auto rsum = [&](int o) {
-                const float4 p0 = *reinterpret_cast<const float4 *>(red + o * kWarps);
-                const float4 p1 = *reinterpret_cast<const float4 *>(red + o * kWarps + 4);
-                return ((p0.x + p0.y) + (p0.z + p0.w)) + ((p1.x + p1.y) + (p1.z + p1.w));
-            };
-            if (PHASE == kUp && GATED) {
-                for (int o = tid; o < 8 * kTok; o += kThreads) {
-                    const int tok = o >> 3, r = o & 7;
-                    const int pos = off + tp * kTok + tok;
-                    if (pos < end) {
-                        const int n = rg * 8 + r;
-                        float gv = rsum(r * kTok + tok), uv = rsum((r + 8) * kTok + tok);
-                        if (WT == WeightType::kI8) {
-                            gv *= tab.s1[e][n];
-                            uv *= tab.s3[e][n];
-                        }
-                        if (geo.splits == 1) {
-                            static_cast<__nv_bfloat16 *>(a.h)[static_cast<size_t>(pos) * a.p + n] =
-                                __float2bfloat16_rn(silu(gv) * uv);
-                        } else {
-                            const size_t o2 = (static_cast<size_t>(ks) * a.n_rows_cap + pos) * a.p + n;
-                            a.gate_part[o2] = gv;
-                            a.up_part[o2] = uv;
-                        }
+
+            // ---- consume the unit's weight stages: block `warp` of each stage
+            for (int kb = U.kb0; kb < U.kb1; ++kb) {
+                bool have = false;
+                if (!s_abort) {
+                    have = mbar_wait(&full_bar[stage], phase);
+                    if (!have) {
+                        if (lane == 0) flag_error(a.err, kErrWaitTimeout);
+                        s_abort = 1;
                     }
                 }
-            } else {
-                for (int o = tid; o < kRowsPerUnit * kTok; o += kThreads) {
-                    const int tok = o >> 4, r = o & 15;
-                    const int pos = off + tp * kTok + tok;
-                    if (pos < end) {
-                        float v = rsum(r * kTok + tok);
-                        const int n = rg * 16 + r;
-                        if (PHASE == kUp) {
-                            if (WT == WeightType::kI8) v *= tab.s1[e][n];
-                            if (geo.splits == 1) {
-                                static_cast<__nv_bfloat16 *>(a.h)[static_cast<size_t>(pos) * a.p + n] =
-                                    __float2bfloat16_rn(fmaxf(v, 0.0f));
-                            } else {
-                                a.gate_part[(static_cast<size_t>(ks) * a.n_rows_cap + pos) * a.p + n] = v;
+                if (have && mine) {
+                    const uint32_t blk = ring_sm + stage * kStageBytes + warp * kBlockBytes;
+#pragma unroll
+                    for (int sh = 0; sh < 2; ++sh) {
+                        const uint32_t atom = blk + sh * 512 + atom_chunk_offset(g, t);
+                        const uint4 ra = lds_v4(atom);         // row g
+                        const uint4 rb = lds_v4(atom + 1024);  // row g + 8
+                        const int kcol = (kb - U.kb0) * kBK + sh * (kBK / 2);  // in the staged rows
+                        if constexpr (WT == WeightType::kBF16) {
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                const uint4 xb =
+                                    lds_v4(bsm + (nt * 8 + g) * geo.row_bytes + (kcol + 8 * t) * 2);
+                                mma_bf16_16816(acc[nt], ra.x, rb.x, ra.y, rb.y, xb.x, xb.y);
+                                mma_bf16_16816(acc[nt], ra.z, rb.z, ra.w, rb.w, xb.z, xb.w);
                             }
                         } else {
-                            if (WT == WeightType::kI8) v *= tab.s2[e][n];
+                            uint32_t al[4], ah[4], bl[4], bh[4];
+                            const uint32_t va[4] = {ra.x, ra.y, ra.z, ra.w};
+                            const uint32_t vb[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                i8x4_to_bf16x2x2(va[i], al[i], ah[i]);
+                                i8x4_to_bf16x2x2(vb[i], bl[i], bh[i]);
+                            }
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                const uint32_t xa = bsm + (nt * 8 + g) * geo.row_bytes + (kcol + 16 * t) * 2;
+                                const uint4 x0 = lds_v4(xa);
+                                const uint4 x1 = lds_v4(xa + 16);
+                                mma_bf16_16816(acc[nt], al[0], bl[0], ah[0], bh[0], x0.x, x0.y);
+                                mma_bf16_16816(acc[nt], al[1], bl[1], ah[1], bh[1], x0.z, x0.w);
+                                mma_bf16_16816(acc[nt], al[2], bl[2], ah[2], bh[2], x1.x, x1.y);
+                                mma_bf16_16816(acc[nt], al[3], bl[3], ah[3], bh[3], x1.z, x1.w);
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                if (have && lane == 0) mbar_arrive(&empty_bar[stage]);
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            // ---- epilogue straight from the MMA fragments of this warp's 16 rows:
+            // acc[nt][0..1] = (row g, tokens nt*8+2t, +1), acc[nt][2..3] = row g + 8
+            if (mine && !s_abort) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int pos = U.off + tp * kTok + nt * 8 + 2 * t + h2;
+                        if (pos >= U.end) continue;
+                        float v0 = acc[nt][h2], v8 = acc[nt][2 + h2];
+                        if (PHASE == kUp && GATED) {
+                            const int n = rg * 8 + g;  // feature: gate row g, up row g + 8
+                            if (WT == WeightType::kI8) {
+                                v0 *= tab.s1[U.e][n];
+                                v8 *= tab.s3[U.e][n];
+                            }
+                            if (geo.splits == 1) {
+                                static_cast<__nv_bfloat16 *>(a.h)[static_cast<size_t>(pos) * a.p + n] =
+                                    __float2bfloat16_rn(silu(v0) * v8);
+                            } else {
+                                const size_t o = (static_cast<size_t>(U.ks) * a.n_rows_cap + pos) * a.p + n;
+                                a.gate_part[o] = v0;
+                                a.up_part[o] = v8;
+                            }
+                        } else if (PHASE == kUp) {
+                            const int n0 = rg * 16 + g, n8 = n0 + 8;
+                            if (WT == WeightType::kI8) {
+                                v0 *= tab.s1[U.e][n0];
+                                v8 *= tab.s1[U.e][n8];
+                            }
+                            if (geo.splits == 1) {
+                                __nv_bfloat16 *hr = static_cast<__nv_bfloat16 *>(a.h) + static_cast<size_t>(pos) * a.p;
+                                hr[n0] = __float2bfloat16_rn(fmaxf(v0, 0.0f));
+                                hr[n8] = __float2bfloat16_rn(fmaxf(v8, 0.0f));
+                            } else {
+                                float *gp = a.gate_part + (static_cast<size_t>(U.ks) * a.n_rows_cap + pos) * a.p;
+                                gp[n0] = v0;
+                                gp[n8] = v8;
+                            }
+                        } else {
+                            const int n0 = rg * 16 + g, n8 = n0 + 8;
+                            if (WT == WeightType::kI8) {
+                                v0 *= tab.s2[U.e][n0];
+                                v8 *= tab.s2[U.e][n8];
+                            }
                             const int fi = a.gather[pos];
                             const float wgt = (fi >= 0 && fi < rows_total) ? a.topk_w[fi] : 0.0f;
-                            a.ypart[(static_cast<size_t>(ks) * a.n_rows_cap + pos) * a.m + n] = wgt * v;
+                            float *yr = a.ypart + (static_cast<size_t>(U.ks) * a.n_rows_cap + pos) * a.m;
+                            yr[n0] = wgt * v0;
+                            yr[n8] = wgt * v8;
                         }
                     }
                 }
             }
-            __syncthreads();
         }
     }
+    __syncthreads();
 }
 
 // h = act(sum_s gate_part[s]) [* sum_s up_part[s]] for split-K up projections.
@@ -320,45 +379,45 @@ __global__ void up_finish_kernel(const ExpertArgs a, int splits) {
 }
 
 template <WeightType WT>
-DecodeGeom make_geom(int K, int splits, int nt, int rg) {
+DecodeGeom make_geom(int K, int rows, int splits, int nt) {
     DecodeGeom g;
     g.K = K;
+    g.rg = rows / kRowsPerUnit;
+    g.rg8 = (g.rg + 7) / 8;
     g.splits = splits;
-    g.nsteps = K / WTraits<WT>::kStep;
-    const int max_steps = (g.nsteps + splits - 1) / splits;
-    const int kr = max_steps * WTraits<WT>::kStep;
-    g.kr_max = (kr + 63) / 64 * 64;
-    g.row_bytes = g.kr_max * 2 + WTraits<WT>::kPad;
-    g.rg = rg;
-    (void)nt;
+    g.nkb = K / WTraits<WT>::kBK;
+    const int max_kb = (g.nkb + splits - 1) / splits;
+    const int kr = max_kb * WTraits<WT>::kBK;
+    const int kr64 = (kr + 63) / 64 * 64;
+    g.row_bytes = kr64 * 2 + WTraits<WT>::kPad;
+    g.bstage_bytes = (8 * nt * g.row_bytes + 15) / 16 * 16;
     return g;
 }
 
 template <WeightType WT, int PHASE, bool GATED, int NT>
-cudaError_t launch_one(const ExpertArgs &a, int K, int splits, int rg, int num_sms,
+cudaError_t launch_one(const ExpertArgs &a, int K, int rows, int splits, int num_sms,
                        cudaStream_t s) {
-    const DecodeGeom geo = make_geom<WT>(K, splits, NT, rg);
-    const size_t smem = static_cast<size_t>(8 * NT) * geo.row_bytes +
-                        static_cast<size_t>(kRowsPerUnit * 8 * NT) * kWarps * sizeof(float);
+    const DecodeGeom geo = make_geom<WT>(K, rows, splits, NT);
+    const size_t smem = static_cast<size_t>(kStages) * kStageBytes + geo.bstage_bytes;
     auto kern = decode_kernel<WT, PHASE, GATED, NT>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    int per_sm = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
-    if (err != cudaSuccess) return err;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    kern<<<num_sms * per_sm, kThreads, smem, s>>>(*a.tab, a, geo);
+    static int configured_smem = 0;  // per instantiation
+    if (static_cast<int>(smem) > configured_smem) {
+        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
+        if (err != cudaSuccess) return err;
+        configured_smem = static_cast<int>(smem);
+    }
+    kern<<<num_sms, kThreads, smem, s>>>(*a.tab, a, geo);
     return cudaGetLastError();
 }
 
 template <WeightType WT, int PHASE, bool GATED>
-cudaError_t dispatch_nt(const ExpertArgs &a, int nt, int K, int splits, int rg, int num_sms,
+cudaError_t dispatch_nt(const ExpertArgs &a, int nt, int K, int rows, int splits, int num_sms,
                         cudaStream_t s) {
     switch (nt) {
-    case 1: return launch_one<WT, PHASE, GATED, 1>(a, K, splits, rg, num_sms, s);
-    case 2: return launch_one<WT, PHASE, GATED, 2>(a, K, splits, rg, num_sms, s);
-    default: return launch_one<WT, PHASE, GATED, 4>(a, K, splits, rg, num_sms, s);
+    case 1: return launch_one<WT, PHASE, GATED, 1>(a, K, rows, splits, num_sms, s);
+    case 2: return launch_one<WT, PHASE, GATED, 2>(a, K, rows, splits, num_sms, s);
+    default: return launch_one<WT, PHASE, GATED, 4>(a, K, rows, splits, num_sms, s);
     }
 }
 
@@ -376,21 +435,20 @@ int decode_token_tiles(int T, int k, int E) {
 cudaError_t launch_decode_up(const ExpertArgs &a, WeightType wt, bool gated, int splits,
                              int num_sms, cudaStream_t s) {
     const int nt = decode_token_tiles(a.T, a.k, a.E);
-    const int rg = gated ? a.p / 8 : a.p / 16;
+    const int rows = gated ? 2 * a.p : a.p;
     if (wt == WeightType::kBF16)
-        return gated ? dispatch_nt<WeightType::kBF16, kUp, true>(a, nt, a.m, splits, rg, num_sms, s)
-                     : dispatch_nt<WeightType::kBF16, kUp, false>(a, nt, a.m, splits, rg, num_sms, s);
-    return gated ? dispatch_nt<WeightType::kI8, kUp, true>(a, nt, a.m, splits, rg, num_sms, s)
-                 : dispatch_nt<WeightType::kI8, kUp, false>(a, nt, a.m, splits, rg, num_sms, s);
+        return gated ? dispatch_nt<WeightType::kBF16, kUp, true>(a, nt, a.m, rows, splits, num_sms, s)
+                     : dispatch_nt<WeightType::kBF16, kUp, false>(a, nt, a.m, rows, splits, num_sms, s);
+    return gated ? dispatch_nt<WeightType::kI8, kUp, true>(a, nt, a.m, rows, splits, num_sms, s)
+                 : dispatch_nt<WeightType::kI8, kUp, false>(a, nt, a.m, rows, splits, num_sms, s);
 }
 
 cudaError_t launch_decode_down(const ExpertArgs &a, WeightType wt, int splits, int num_sms,
                                cudaStream_t s) {
     const int nt = decode_token_tiles(a.T, a.k, a.E);
-    const int rg = a.m / 16;
     if (wt == WeightType::kBF16)
-        return dispatch_nt<WeightType::kBF16, kDown, false>(a, nt, a.p, splits, rg, num_sms, s);
-    return dispatch_nt<WeightType::kI8, kDown, false>(a, nt, a.p, splits, rg, num_sms, s);
+        return dispatch_nt<WeightType::kBF16, kDown, false>(a, nt, a.p, a.m, splits, num_sms, s);
+    return dispatch_nt<WeightType::kI8, kDown, false>(a, nt, a.p, a.m, splits, num_sms, s);
 }
 
 cudaError_t launch_decode_up_finish(const ExpertArgs &a, bool gated, int splits, cudaStream_t s) {

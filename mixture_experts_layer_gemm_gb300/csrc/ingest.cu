@@ -4,6 +4,7 @@
 // the router to fp32, and quantise to per-column symmetric int8.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "packing.h"
 
 namespace moe {
 
@@ -48,6 +49,32 @@ __global__ void quantize_rows_kernel(const uint16_t *__restrict__ wt, int nrows,
     }
 }
 
+// Pack a transposed matrix (rows x K, K contiguous; elem_bytes 1 or 2) into
+// the blocked layout of packing.h.  With src3 given (SwiGLU up-projection),
+// stored row 16q + r takes row 8q + r of src1 for r < 8 and row 8q + r - 8 of
+// src3 otherwise.  One thread moves one 16-byte run.
+__global__ void pack_kernel(const uint8_t *__restrict__ src1, const uint8_t *__restrict__ src3,
+                            int rows, int K, int elem_bytes, uint8_t *__restrict__ dst) {
+    const int per16 = 16 / elem_bytes;
+    const long long runs_per_row = K / per16;
+    const long long n = static_cast<long long>(rows) * runs_per_row;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int r = static_cast<int>(i / runs_per_row);
+        const int k = static_cast<int>(i % runs_per_row) * per16;
+        const uint8_t *src;
+        if (src3) {
+            const int q = r / 16, rr = r % 16;
+            src = (rr < 8 ? src1 + static_cast<size_t>(q * 8 + rr) * K * elem_bytes
+                          : src3 + static_cast<size_t>(q * 8 + rr - 8) * K * elem_bytes);
+        } else {
+            src = src1 + static_cast<size_t>(r) * K * elem_bytes;
+        }
+        const uint4 v = *reinterpret_cast<const uint4 *>(src + static_cast<size_t>(k) * elem_bytes);
+        *reinterpret_cast<uint4 *>(dst + packed_offset(r, k, rows, elem_bytes)) = v;
+    }
+}
+
 template <typename T>
 __global__ void router_prep_kernel(const T *src, int m, int E, float *dst) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -80,6 +107,17 @@ cudaError_t launch_quantize_rows(const void *wt_bf16, int nrows, int len, int8_t
     const int warps = 8;
     quantize_rows_kernel<<<(nrows + warps - 1) / warps, 32 * warps, 0, s>>>(
         static_cast<const uint16_t *>(wt_bf16), nrows, len, codes, scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack(const void *src1, const void *src3, int rows, int K, int elem_bytes,
+                        void *dst, cudaStream_t s) {
+    const long long n = static_cast<long long>(rows) * K * elem_bytes / 16;
+    long long blocks = (n + 255) / 256;
+    if (blocks > 8192) blocks = 8192;
+    pack_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        static_cast<const uint8_t *>(src1), static_cast<const uint8_t *>(src3), rows, K, elem_bytes,
+        static_cast<uint8_t *>(dst));
     return cudaGetLastError();
 }
 

@@ -33,8 +33,10 @@ cudaError_t launch_topk_copy_validate(const int32_t *ids_in, const float *w_in, 
                                       cudaStream_t s);
 cudaError_t launch_permute(const PermuteArgs &a, cudaStream_t s);
 
-// ---- expert weights as stored: transposed so the reduction runs along rows ----
-// up:   W1t[e] (and W3t[e]) [p rows x m cols];  down: W2t[e] [m rows x p cols]
+// ---- expert weights as stored ---------------------------------------------------
+// fp32 layers: w1/w3[e] = W1^T/W3^T [p x m], w2[e] = W2^T [m x p], row-major.
+// bf16 / int8 layers: packed (packing.h): w1[e] = U (gate and up rows
+// interleaved for SwiGLU), w2[e] = D = W2^T; w3 unused.
 // For int8 weights, s1/s3[e] hold p fp32 scales and s2[e] holds m scales.
 struct ExpertTables {
     const void *w1[kExpertTableMax];
@@ -101,6 +103,9 @@ cudaError_t launch_transpose(const void *src, void *dst, int rows, int cols, int
 // weight = columns of the user's matrix): codes [nrows x len], scales [nrows].
 cudaError_t launch_quantize_rows(const void *wt_bf16, int nrows, int len, int8_t *codes,
                                  float *scales, cudaStream_t s);
+// Pack transposed rows into the blocked layout of packing.h (src3: SwiGLU up).
+cudaError_t launch_pack(const void *src1, const void *src3, int rows, int K, int elem_bytes,
+                        void *dst, cudaStream_t s);
 // widen router weights to fp32 and transpose: dst[e][c] = src[c][e]
 cudaError_t launch_router_prep(const void *src, bool bf16, int m, int E, float *dst,
                                cudaStream_t s);

@@ -21,6 +21,7 @@
 #include "common.cuh"
 #include "kernels.cuh"
 #include "layer_impl.h"
+#include "packing.h"
 
 using namespace moe;
 
@@ -67,10 +68,46 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
+constexpr int kSplitUpMax = 4, kSplitDownMax = 16;
+
+// Smallest split of a K-long reduction whose staged token rows (8 * nt rows of
+// K / splits bf16) fit the shared-memory budget.
 int splits_for(int K, int nt, int min_splits) {
     int s = ceil_div(static_cast<long long>(8) * nt * 2 * K, static_cast<long long>(kSmemBudgetB));
     if (s < min_splits) s = min_splits;
     return s;
+}
+
+// Expected number of distinct experts that T tokens choose under uniform
+// routing, E (1 - (1 - k/E)^T): exactly k for one token.
+int expected_active(int T, int k, int E) {
+    double miss = 1.0;
+    for (int t = 0; t < T && miss > 1e-9; ++t) miss *= 1.0 - static_cast<double>(k) / E;
+    int n = static_cast<int>(E * (1.0 - miss) + 0.5);
+    return n < k ? k : (n > E ? E : n);
+}
+
+// Reduction split for a decode projection: at least what the staging budget
+// needs, then the smallest count (up to max_s) whose units -- n_active
+// experts x splits x ceil(rows / 128) -- fill the SMs in nearly whole waves.
+int choose_splits(int K, int bk, int rows, int nt, int n_active, int num_sms, int max_s) {
+    const int nkb = K / bk;
+    const int rg8 = (rows / 16 + 7) / 8;
+    int s0 = splits_for(K, nt, 1);
+    if (s0 > max_s) s0 = max_s;
+    int best = s0;
+    double best_eff = -1.0;
+    for (int S = s0; S <= max_s && S <= nkb; ++S) {
+        const long long units = static_cast<long long>(n_active) * S * rg8;
+        const long long waves = (units + num_sms - 1) / num_sms;
+        const double eff = static_cast<double>(units) / static_cast<double>(waves * num_sms);
+        if (eff >= 0.92) return S;
+        if (eff > best_eff) {
+            best_eff = eff;
+            best = S;
+        }
+    }
+    return best;
 }
 
 moe_status_t check_config(const moe_config_t *c) {
@@ -95,6 +132,8 @@ moe_status_t check_config(const moe_config_t *c) {
             return fail(MOE_ERR_UNSUPPORTED, "bf16 activations need bf16 or int8 weights");
         if (c->m % 64 || c->p % 64)
             return fail(MOE_ERR_UNSUPPORTED, "bf16/int8 layers need m and p multiples of 64");
+        if (c->weight_dtype == MOE_I8 && (c->m % 128 || c->p % 128))
+            return fail(MOE_ERR_UNSUPPORTED, "int8 layers need m and p multiples of 128");
     }
     if (c->paged && c->weight_dtype == MOE_F32)
         return fail(MOE_ERR_UNSUPPORTED, "paged layers need bf16 or int8 weights");
@@ -147,6 +186,18 @@ void *moe_layer::dalloc(size_t bytes, cudaError_t *err) {
     return p;
 }
 
+static size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+static void free_one(moe_layer_t *L, void *p) {
+    if (!p) return;
+    for (size_t i = 0; i < L->allocations.size(); ++i)
+        if (L->allocations[i] == p) {
+            cudaFree(p);
+            L->allocations.erase(L->allocations.begin() + static_cast<long>(i));
+            return;
+        }
+}
+
 static moe_status_t ingest_weights(moe_layer_t *L, const void *w_router, const float *b_router,
                                    const void *const *w1, const void *const *w2,
                                    const void *const *w3) {
@@ -154,6 +205,8 @@ static moe_status_t ingest_weights(moe_layer_t *L, const void *w_router, const f
     cudaError_t err;
     cudaStream_t s = L->ingest_stream;
     const bool bf16_act = c.act_dtype == MOE_BF16;
+    const bool gated = c.expert == MOE_EXPERT_SWIGLU;
+    const bool i8 = c.weight_dtype == MOE_I8;
     const size_t ab = act_bytes(c.act_dtype);
     const size_t src_elem = (c.weight_dtype == MOE_F32) ? 4 : 2;
     const size_t mp = static_cast<size_t>(c.m) * c.p;
@@ -173,64 +226,88 @@ static moe_status_t ingest_weights(moe_layer_t *L, const void *w_router, const f
                                  cudaMemcpyHostToDevice, s));
     }
 
-    // experts: one allocation holding every expert's transposed matrices
-    const int nmat = (c.expert == MOE_EXPERT_SWIGLU) ? 3 : 2;
-    const size_t wel = (c.weight_dtype == MOE_I8) ? 1 : src_elem;
-    const size_t mat_bytes = (mp * wel + 255) / 256 * 256;
-    const size_t scale_bytes =
-        (c.weight_dtype == MOE_I8)
-            ? ((static_cast<size_t>(c.p) * (nmat - 1) + c.m) * 4 + 255) / 256 * 256
-            : 0;
-    L->expert_stride = mat_bytes * nmat + scale_bytes;
-    L->expert_bytes = mp * wel * nmat +
-                      (c.weight_dtype == MOE_I8 ? (static_cast<size_t>(c.p) * (nmat - 1) + c.m) * 4 : 0);
+    // experts: one allocation holding every expert's stored matrices
+    const int nmat = gated ? 3 : 2;
+    const size_t wel = i8 ? 1 : src_elem;
+    const int rows_u = gated ? 2 * c.p : c.p;
+    size_t u_bytes, d_bytes, scale_bytes = 0;
+    if (c.weight_dtype == MOE_F32) {  // W1^T, W2^T, W3^T row-major
+        u_bytes = round256(mp * wel) * (gated ? 2 : 1);
+        d_bytes = round256(mp * wel);
+    } else {  // packed U and D
+        u_bytes = round256(static_cast<size_t>(rows_u) * c.m * wel);
+        d_bytes = round256(mp * wel);
+        if (i8) scale_bytes = round256((static_cast<size_t>(c.p) * (nmat - 1) + c.m) * 4);
+    }
+    L->expert_stride = u_bytes + d_bytes + scale_bytes;
+    L->expert_bytes = mp * wel * nmat + (i8 ? (static_cast<size_t>(c.p) * (nmat - 1) + c.m) * 4 : 0);
     L->weights = static_cast<uint8_t *>(L->dalloc(L->expert_stride * c.E, &err));
     if (err) return cuda_fail(err, "cudaMalloc(expert weights)");
     void *stage = L->dalloc(mp * src_elem, &err);
     if (err) return cuda_fail(err, "cudaMalloc(weight staging)");
-    void *stage_t = nullptr;
-    if (c.weight_dtype == MOE_I8) {
-        stage_t = L->dalloc(mp * src_elem, &err);
+    void *t1 = nullptr, *t3 = nullptr, *q1 = nullptr, *q3 = nullptr;
+    if (c.weight_dtype != MOE_F32) {
+        t1 = L->dalloc(mp * 2, &err);
+        if (!err && gated) t3 = L->dalloc(mp * 2, &err);
+        if (!err && i8) q1 = L->dalloc(mp, &err);
+        if (!err && i8 && gated) q3 = L->dalloc(mp, &err);
         if (err) return cuda_fail(err, "cudaMalloc(weight staging)");
     }
     for (int e = 0; e < c.E; ++e) {
         uint8_t *base = L->weights + L->expert_stride * e;
-        uint8_t *m1 = base, *m2 = base + mat_bytes, *m3 = (nmat == 3) ? base + 2 * mat_bytes : nullptr;
-        float *sc = reinterpret_cast<float *>(base + mat_bytes * nmat);
-        float *s1 = sc, *s3 = (nmat == 3) ? sc + c.p : nullptr, *s2 = sc + static_cast<size_t>(c.p) * (nmat - 1);
-        struct Job { const void *src; uint8_t *dst; int rows, cols; float *scales; };
-        Job jobs[3] = {{w1[e], m1, c.m, c.p, s1}, {w2[e], m2, c.p, c.m, s2},
-                       {nmat == 3 ? w3[e] : nullptr, m3, c.m, c.p, s3}};
-        for (int j = 0; j < nmat; ++j) {
-            const Job &jb = jobs[j];
-            // the staging buffer is reused: order the copy after the last kernel
-            CUDA_TRY(cudaMemcpyAsync(stage, jb.src, mp * src_elem, cudaMemcpyHostToDevice, s));
-            if (c.weight_dtype == MOE_I8) {
-                CUDA_TRY(launch_transpose(stage, stage_t, jb.rows, jb.cols, 2, s));
-                CUDA_TRY(launch_quantize_rows(stage_t, jb.cols, jb.rows,
-                                              reinterpret_cast<int8_t *>(jb.dst), jb.scales, s));
-            } else {
-                CUDA_TRY(launch_transpose(stage, jb.dst, jb.rows, jb.cols, static_cast<int>(src_elem), s));
+        uint8_t *U = base, *D = base + u_bytes;
+        float *sc = reinterpret_cast<float *>(base + u_bytes + d_bytes);
+        float *s1 = i8 ? sc : nullptr;
+        float *s3 = (i8 && gated) ? sc + c.p : nullptr;
+        float *s2 = i8 ? sc + static_cast<size_t>(c.p) * (nmat - 1) : nullptr;
+        // the staging buffers are reused: every step is ordered on stream s
+        if (c.weight_dtype == MOE_F32) {
+            uint8_t *W1t = U, *W3t = gated ? U + round256(mp * wel) : nullptr;
+            CUDA_TRY(cudaMemcpyAsync(stage, w1[e], mp * 4, cudaMemcpyHostToDevice, s));
+            CUDA_TRY(launch_transpose(stage, W1t, c.m, c.p, 4, s));
+            if (gated) {
+                CUDA_TRY(cudaMemcpyAsync(stage, w3[e], mp * 4, cudaMemcpyHostToDevice, s));
+                CUDA_TRY(launch_transpose(stage, W3t, c.m, c.p, 4, s));
             }
+            CUDA_TRY(cudaMemcpyAsync(stage, w2[e], mp * 4, cudaMemcpyHostToDevice, s));
+            CUDA_TRY(launch_transpose(stage, D, c.p, c.m, 4, s));
+            L->tab.w1[e] = W1t;
+            L->tab.w3[e] = W3t;
+            L->tab.w2[e] = D;
+            continue;
         }
-        L->tab.w1[e] = m1;
-        L->tab.w2[e] = m2;
-        L->tab.w3[e] = m3;
-        L->tab.s1[e] = (c.weight_dtype == MOE_I8) ? s1 : nullptr;
-        L->tab.s2[e] = (c.weight_dtype == MOE_I8) ? s2 : nullptr;
-        L->tab.s3[e] = (c.weight_dtype == MOE_I8) ? s3 : nullptr;
+        // up: W1^T (and W3^T) [p x m] -> packed U (gate/up rows interleaved per 8)
+        CUDA_TRY(cudaMemcpyAsync(stage, w1[e], mp * 2, cudaMemcpyHostToDevice, s));
+        CUDA_TRY(launch_transpose(stage, t1, c.m, c.p, 2, s));
+        if (gated) {
+            CUDA_TRY(cudaMemcpyAsync(stage, w3[e], mp * 2, cudaMemcpyHostToDevice, s));
+            CUDA_TRY(launch_transpose(stage, t3, c.m, c.p, 2, s));
+        }
+        if (i8) {
+            CUDA_TRY(launch_quantize_rows(t1, c.p, c.m, static_cast<int8_t *>(q1), s1, s));
+            if (gated) CUDA_TRY(launch_quantize_rows(t3, c.p, c.m, static_cast<int8_t *>(q3), s3, s));
+            CUDA_TRY(launch_pack(q1, gated ? q3 : nullptr, rows_u, c.m, 1, U, s));
+        } else {
+            CUDA_TRY(launch_pack(t1, gated ? t3 : nullptr, rows_u, c.m, 2, U, s));
+        }
+        // down: W2^T [m x p] -> packed D
+        CUDA_TRY(cudaMemcpyAsync(stage, w2[e], mp * 2, cudaMemcpyHostToDevice, s));
+        CUDA_TRY(launch_transpose(stage, t1, c.p, c.m, 2, s));
+        if (i8) {
+            CUDA_TRY(launch_quantize_rows(t1, c.m, c.p, static_cast<int8_t *>(q1), s2, s));
+            CUDA_TRY(launch_pack(q1, nullptr, c.m, c.p, 1, D, s));
+        } else {
+            CUDA_TRY(launch_pack(t1, nullptr, c.m, c.p, 2, D, s));
+        }
+        L->tab.w1[e] = U;
+        L->tab.w2[e] = D;
+        L->tab.w3[e] = nullptr;
+        L->tab.s1[e] = s1;
+        L->tab.s2[e] = s2;
+        L->tab.s3[e] = s3;
     }
     CUDA_TRY(cudaStreamSynchronize(s));
-    // staging buffers are not needed after ingestion
-    for (void *p : {stage_r, stage, stage_t}) {
-        if (!p) continue;
-        for (size_t i = 0; i < L->allocations.size(); ++i)
-            if (L->allocations[i] == p) {
-                cudaFree(p);
-                L->allocations.erase(L->allocations.begin() + static_cast<long>(i));
-                break;
-            }
-    }
+    for (void *p : {stage_r, stage, t1, t3, q1, q3}) free_one(L, p);
     return MOE_OK;
 }
 
@@ -245,18 +322,14 @@ static moe_status_t alloc_workspace(moe_layer_t *L) {
     L->split_up_max = 1;
     L->split_down_max = 1;
     if (c.act_dtype == MOE_BF16) {
-        const int nt_max = 4;
-        L->split_up_max = splits_for(c.m, nt_max, 1);
-        L->split_down_max = splits_for(c.p, nt_max, 4);
+        L->split_up_max = kSplitUpMax;
+        L->split_down_max = kSplitDownMax;
         const size_t drows = rows < kDecodeMaxRows ? rows : kDecodeMaxRows;
         L->decode_rows_cap = drows;
+        // decode: split_down_max partial rows per permuted row (T*k <= the cap);
+        // batch: one fp32 row per permuted row
         size_t need = static_cast<size_t>(L->split_down_max) * drows;
-        if (rows > kDecodeMaxRows) {
-            // beyond the split-K row cap the decode kernels run one token tile
-            // per pass with 4 down splits and no up split
-            const size_t big = 4 * rows;
-            if (big > need) need = big;
-        }
+        if (rows > need) need = rows;
         ypart_rows = need;
         if (L->split_up_max > 1) {
             const size_t n = static_cast<size_t>(L->split_up_max) * drows * c.p;
@@ -447,8 +520,11 @@ moe_status_t run_experts(moe_layer_t *L, ExpertArgs &a, int regime, int *splits_
     int nt = decode_token_tiles(a.T, a.k, a.E);
     int s_up, s_down;
     if (rows <= static_cast<int>(L->decode_rows_cap)) {
-        s_up = splits_for(c.m, nt, 1);
-        s_down = splits_for(c.p, nt, 4);
+        const int bk = (c.weight_dtype == MOE_I8) ? 128 : 64;
+        const int n_act = expected_active(a.T, a.k, a.E);
+        const int rows_up = gated ? 2 * c.p : c.p;
+        s_up = choose_splits(c.m, bk, rows_up, nt, n_act, L->num_sms, L->split_up_max);
+        s_down = choose_splits(c.p, bk, c.m, nt, n_act, L->num_sms, L->split_down_max);
         a.n_rows_cap = static_cast<int>(L->decode_rows_cap);
     } else {
         return fail(MOE_ERR_UNSUPPORTED, "decode kernels take T*k <= %d", kDecodeMaxRows);
@@ -587,26 +663,40 @@ extern "C" moe_status_t moe_layer_read_expert(const moe_layer_t *L, int expert, 
     if (!L || !values) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
     const moe_config_t &c = L->cfg;
     if (expert < 0 || expert >= c.E) return fail(MOE_ERR_INVALID_ARG, "expert out of range");
-    if (which < 1 || which > 3 || (which == 3 && c.expert != MOE_EXPERT_SWIGLU))
+    const bool gated = c.expert == MOE_EXPERT_SWIGLU;
+    if (which < 1 || which > 3 || (which == 3 && !gated))
         return fail(MOE_ERR_INVALID_ARG, "which must be 1, 2 or (SwiGLU) 3");
     if (c.weight_dtype == MOE_I8 && !scales) return fail(MOE_ERR_INVALID_ARG, "scales is NULL");
     if (L->pool) return fail(MOE_ERR_UNSUPPORTED, "read_expert on a paged layer");
     cudaSetDevice(L->device);
-    const void *src = which == 1 ? L->tab.w1[expert] : which == 2 ? L->tab.w2[expert] : L->tab.w3[expert];
-    const float *ssrc = which == 1 ? L->tab.s1[expert] : which == 2 ? L->tab.s2[expert] : L->tab.s3[expert];
-    // stored transposed: rows = outputs, cols = reduction
-    const int out_rows = (which == 2) ? c.m : c.p, red = (which == 2) ? c.p : c.m;
-    const size_t el = (c.weight_dtype == MOE_I8) ? 1 : (c.weight_dtype == MOE_F32 ? 4 : 2);
-    std::vector<uint8_t> buf(static_cast<size_t>(out_rows) * red * el);
     CUDA_TRY(cudaDeviceSynchronize());
-    CUDA_TRY(cudaMemcpy(buf.data(), src, buf.size(), cudaMemcpyDeviceToHost));
+    // user orientation: W1/W3 are m x p (out = columns = p), W2 is p x m
+    const int out_n = (which == 2) ? c.m : c.p, red = (which == 2) ? c.p : c.m;
     uint8_t *dst = static_cast<uint8_t *>(values);
-    for (int o = 0; o < out_rows; ++o)
+    if (c.weight_dtype == MOE_F32) {
+        const void *src = which == 1 ? L->tab.w1[expert] : which == 2 ? L->tab.w2[expert] : L->tab.w3[expert];
+        std::vector<float> buf(static_cast<size_t>(out_n) * red);
+        CUDA_TRY(cudaMemcpy(buf.data(), src, buf.size() * 4, cudaMemcpyDeviceToHost));
+        float *o = reinterpret_cast<float *>(dst);
+        for (int n = 0; n < out_n; ++n)
+            for (int i = 0; i < red; ++i) o[static_cast<size_t>(i) * out_n + n] = buf[static_cast<size_t>(n) * red + i];
+        return MOE_OK;
+    }
+    const int el = (c.weight_dtype == MOE_I8) ? 1 : 2;
+    const int rows = (which == 2) ? c.m : (gated ? 2 * c.p : c.p);
+    const void *src = (which == 2) ? L->tab.w2[expert] : L->tab.w1[expert];
+    std::vector<uint8_t> buf(static_cast<size_t>(rows) * red * el);
+    CUDA_TRY(cudaMemcpy(buf.data(), src, buf.size(), cudaMemcpyDeviceToHost));
+    for (int n = 0; n < out_n; ++n) {
+        const int row = (which == 2) ? n : (!gated ? n : (which == 1 ? up_row_gate(n) : up_row_up(n)));
         for (int i = 0; i < red; ++i)
-            std::memcpy(dst + (static_cast<size_t>(i) * out_rows + o) * el,
-                        buf.data() + (static_cast<size_t>(o) * red + i) * el, el);
-    if (c.weight_dtype == MOE_I8)
-        CUDA_TRY(cudaMemcpy(scales, ssrc, static_cast<size_t>(out_rows) * 4, cudaMemcpyDeviceToHost));
+            std::memcpy(dst + (static_cast<size_t>(i) * out_n + n) * el,
+                        buf.data() + packed_offset(row, i, rows, el), el);
+    }
+    if (c.weight_dtype == MOE_I8) {
+        const float *ssrc = which == 1 ? L->tab.s1[expert] : which == 2 ? L->tab.s2[expert] : L->tab.s3[expert];
+        CUDA_TRY(cudaMemcpy(scales, ssrc, static_cast<size_t>(out_n) * 4, cudaMemcpyDeviceToHost));
+    }
     return MOE_OK;
 }
 

@@ -52,67 +52,91 @@ __device__ __forceinline__ void select_topk(const float (&l)[EMAX], int E, int k
         if (j < k) w[j] = w[j] / denom;
 }
 
-// One warp per token.  x: [T x m] (fp32 or bf16); wrt: router weights
-// transposed to [E x m] fp32 (exact copy of the given values).
+// One CTA per group of 8 tokens.  The 256 threads split the hidden dimension
+// into 16-byte chunks (chunk c goes to thread c mod 256), so even a single
+// token spreads its m x E router products over the whole CTA.  For each token
+// every thread adds its products in sequence, a warp-shuffle tree adds the 32
+// lane sums, and one thread per (token, expert) adds the 8 warp sums in warp
+// order: a fixed, deterministic order.  Then warp w selects the top-k of
+// token w.  x: [T x m] (fp32 or bf16); wrt: router weights transposed to
+// [E x m] fp32 (an exact copy of the given values).
+constexpr int kRouterTokens = 8;
+
 template <typename ActT, int EMAX>
 __global__ void __launch_bounds__(256) router_topk_kernel(RouterArgs a) {
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (t >= a.T) return;
-    float acc[EMAX];
-#pragma unroll
-    for (int e = 0; e < EMAX; ++e) acc[e] = 0.0f;
+    __shared__ float s_part[kRouterTokens][8][EMAX];
+    __shared__ float s_logit[kRouterTokens][EMAX];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t0 = blockIdx.x * kRouterTokens;
+    const int ntok = min(kRouterTokens, a.T - t0);
+    constexpr int kVec = 16 / sizeof(ActT);  // elements per 16-byte chunk
+    const int nchunks = a.m / kVec;
 
-    constexpr int kVec = 16 / sizeof(ActT);  // elements per 16-byte load
-    const ActT *xr = static_cast<const ActT *>(a.x) + static_cast<size_t>(t) * a.m;
-    for (int c = lane * kVec; c < a.m; c += 32 * kVec) {
-        const uint4 raw = ld_nc_v4(xr + c);
-        float xv[kVec];
-        if constexpr (sizeof(ActT) == 2) {
-            const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+    for (int tk = 0; tk < ntok; ++tk) {
+        const ActT *xr = static_cast<const ActT *>(a.x) + static_cast<size_t>(t0 + tk) * a.m;
+        float acc[EMAX];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                xv[2 * i] = bf16lo(u[i]);
-                xv[2 * i + 1] = bf16hi(u[i]);
+        for (int e = 0; e < EMAX; ++e) acc[e] = 0.0f;
+        for (int ch = tid; ch < nchunks; ch += 256) {
+            const int c = ch * kVec;
+            const uint4 raw = ld_nc_v4(xr + c);
+            float xv[kVec];
+            if constexpr (sizeof(ActT) == 2) {
+                const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    xv[2 * i] = bf16lo(u[i]);
+                    xv[2 * i + 1] = bf16hi(u[i]);
+                }
+            } else {
+                xv[0] = __uint_as_float(raw.x);
+                xv[1] = __uint_as_float(raw.y);
+                xv[2] = __uint_as_float(raw.z);
+                xv[3] = __uint_as_float(raw.w);
             }
-        } else {
-            xv[0] = __uint_as_float(raw.x);
-            xv[1] = __uint_as_float(raw.y);
-            xv[2] = __uint_as_float(raw.z);
-            xv[3] = __uint_as_float(raw.w);
-        }
 #pragma unroll
-        for (int e = 0; e < EMAX; ++e) {
-            if (e < a.E) {
-                const float *wr = a.wrt + static_cast<size_t>(e) * a.m + c;
+            for (int e = 0; e < EMAX; ++e) {
+                if (e < a.E) {
+                    const float *wr = a.wrt + static_cast<size_t>(e) * a.m + c;
 #pragma unroll
-                for (int i = 0; i < kVec; i += 4) {
-                    const float4 wv = __ldg(reinterpret_cast<const float4 *>(wr + i));
-                    acc[e] = fmaf(xv[i], wv.x, acc[e]);
-                    acc[e] = fmaf(xv[i + 1], wv.y, acc[e]);
-                    acc[e] = fmaf(xv[i + 2], wv.z, acc[e]);
-                    acc[e] = fmaf(xv[i + 3], wv.w, acc[e]);
+                    for (int i = 0; i < kVec; i += 4) {
+                        const float4 wv = __ldg(reinterpret_cast<const float4 *>(wr + i));
+                        acc[e] = fmaf(xv[i], wv.x, acc[e]);
+                        acc[e] = fmaf(xv[i + 1], wv.y, acc[e]);
+                        acc[e] = fmaf(xv[i + 2], wv.z, acc[e]);
+                        acc[e] = fmaf(xv[i + 3], wv.w, acc[e]);
+                    }
                 }
             }
         }
-    }
 #pragma unroll
-    for (int e = 0; e < EMAX; ++e) {
-        acc[e] = warp_sum(acc[e]);
-        if (a.bias && e < a.E) acc[e] += a.bias[e];
+        for (int e = 0; e < EMAX; ++e) {
+            const float v = warp_sum(acc[e]);
+            if (lane == 0 && e < a.E) s_part[tk][warp][e] = v;
+        }
     }
-    if (a.logits) {
+    __syncthreads();
+    for (int i = tid; i < ntok * a.E; i += 256) {
+        const int tk = i / a.E, e = i % a.E;
+        float v = 0.0f;
 #pragma unroll
-        for (int e = 0; e < EMAX; ++e)
-            if (e < a.E && lane == (e & 31)) a.logits[static_cast<size_t>(t) * a.E + e] = acc[e];
+        for (int w = 0; w < 8; ++w) v += s_part[tk][w][e];
+        if (a.bias) v += a.bias[e];
+        s_logit[tk][e] = v;
+        if (a.logits) a.logits[static_cast<size_t>(t0 + tk) * a.E + e] = v;
     }
-    int ids[kMaxTopK];
-    float w[kMaxTopK];
-    select_topk<EMAX>(acc, a.E, a.k, ids, w);
-    if (lane < a.k) {
+    __syncthreads();
+    if (warp < ntok) {
+        const int t = t0 + warp;
+        float l[EMAX];
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) l[e] = (e < a.E) ? s_logit[warp][e] : 0.0f;
+        int ids[kMaxTopK];
+        float w[kMaxTopK];
+        select_topk<EMAX>(l, a.E, a.k, ids, w);
 #pragma unroll
         for (int j = 0; j < kMaxTopK; ++j)
-            if (j == lane) {
+            if (j < a.k && lane == j) {
                 a.ids[static_cast<size_t>(t) * a.k + j] = ids[j];
                 a.w[static_cast<size_t>(t) * a.k + j] = w[j];
             }
@@ -242,8 +266,7 @@ __global__ void __launch_bounds__(1024) permute_kernel(PermuteArgs a) {
 // ---- launchers ----------------------------------------------------------------
 template <typename ActT>
 static cudaError_t launch_router_t(const RouterArgs &a, cudaStream_t s) {
-    const int warps = 8;
-    dim3 grid((a.T + warps - 1) / warps), block(32 * warps);
+    dim3 grid((a.T + kRouterTokens - 1) / kRouterTokens), block(256);
     if (a.E <= 8)
         router_topk_kernel<ActT, 8><<<grid, block, 0, s>>>(a);
     else if (a.E <= 16)
