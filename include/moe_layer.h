@@ -164,6 +164,30 @@ moe_status_t moe_route_from_topk(moe_layer_t *layer, const int32_t *ids, const f
 moe_status_t moe_forward(moe_layer_t *layer, const void *x, const moe_routing_t *r,
                          void *y, void *stream);
 
+/* Forward pass that allocates nothing and uses no layer workspace.
+ * No counterpart in the source paper: this entry point exists for callers
+ * that cannot call cudaMalloc while they run -- a serving engine whose own
+ * allocator holds all free device memory, a latency-critical loop that cannot
+ * take cudaMalloc's implicit synchronisation, code that runs where allocating
+ * is not allowed.  Such a caller creates the layer up front and then calls
+ * this instead of moe_forward.
+ *   Same arguments, same kernels and same results as moe_forward in the decode
+ *   regime, but its scratch (expert hidden rows and split-reduction partial
+ *   sums) lives in a 16 MiB array compiled into the library, one per device,
+ *   held until the process exits.  No cudaMalloc, cudaFree or other
+ *   allocating routine is called.
+ *   Limits: resident bf16/int8 layers only; T*k at most 512 and the scratch
+ *   need (about T*k*(2p + 4*m*splits) bytes) at most 16 MiB -- e.g. T <= 16
+ *   for a Mixtral-shaped layer.  Larger requests return MOE_ERR_INVALID_ARG
+ *   with both sizes in moe_last_error().
+ *   The first call on a device looks up the array's device address with that
+ *   device current; make it before any stream capture begins.
+ *   Every call on a device uses the same array: calls whose GPU work overlaps
+ *   (other streams, other host threads) race on it and must be serialised.
+ *   Nothing needs clearing between calls. */
+moe_status_t moe_forward_static_scratch(moe_layer_t *layer, const void *x, const moe_routing_t *r,
+                                        void *y, void *stream);
+
 /* Options.
  *   MOE_OPT_REGIME: 0 = automatic (default), 1 = always the decode kernels,
  *     2 = always the batch kernels (bf16 weights only).

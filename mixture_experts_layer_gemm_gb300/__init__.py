@@ -87,6 +87,7 @@ _SIGNATURES = {
     "moe_route_from_logits": [_vp, _vp, _i, ctypes.POINTER(moe_routing_t), _vp],
     "moe_route_from_topk": [_vp, _vp, _vp, _i, ctypes.POINTER(moe_routing_t), _vp],
     "moe_forward": [_vp, _vp, ctypes.POINTER(moe_routing_t), _vp, _vp],
+    "moe_forward_static_scratch": [_vp, _vp, ctypes.POINTER(moe_routing_t), _vp, _vp],
     "moe_layer_set_option": [_vp, _i, _i],
     "moe_layer_info": [_vp, ctypes.POINTER(moe_layer_info_t)],
     "moe_layer_stats": [_vp, ctypes.POINTER(moe_stats_t)],
@@ -192,6 +193,13 @@ def moe_route_from_topk(handle, ids, w, T, routing: moe_routing_t, stream=None):
 
 def moe_forward(handle, x, routing: moe_routing_t, y, stream=None):
     _check(lib().moe_forward(handle, _ptr(x), ctypes.byref(routing), _ptr(y), _stream_ptr(stream)))
+
+
+def moe_forward_static_scratch(handle, x, routing: moe_routing_t, y, stream=None):
+    """moe_forward's decode path with its scratch in the library's static
+    device array: for callers that cannot allocate device memory."""
+    _check(lib().moe_forward_static_scratch(handle, _ptr(x), ctypes.byref(routing), _ptr(y),
+                                            _stream_ptr(stream)))
 
 
 def moe_layer_set_option(handle, opt, value):

@@ -65,6 +65,7 @@ ExpertArgs make_expert_args(moe_layer *L, const void *x, const moe_routing_t *r)
 moe_status_t run_experts(moe_layer *L, ExpertArgs &a, int regime, int *splits_out, cudaStream_t s);
 moe_status_t run_combine(moe_layer *L, const moe_routing_t *r, int splits, int n_rows_cap, void *y,
                          cudaStream_t s);
+void decode_plan(const moe_layer *L, int T, int *nt, int *s_up, int *s_down);
 
 // Launch one kernel (f returns its cudaError_t) as phase `phase`: counts the
 // launch and, with timing on, brackets it with events on stream s.
