@@ -142,14 +142,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     const long long units = static_cast<long long>(s_nact) * geo.splits * geo.rg8;
 
+    // A slot is re-armed only after all consumer warps released it, which they
+    // do only after seeing its copy land; so at any time each slot has at most
+    // one phase in flight, the last one issued.
+    uint32_t last_parity[kStages];
+    bool used[kStages];
+    for (int i = 0; i < kStages; ++i) used[i] = false;
     if (warp == kConsumerWarps) {
         // ================= producer: stream weight stages into the ring ==========
-        // A slot is re-armed only after all consumer warps released it, which
-        // they do only after seeing its copy land; so at any time each slot
-        // has at most one phase in flight, the last one issued.
-        uint32_t last_parity[kStages];
-        bool used[kStages];
-        for (int i = 0; i < kStages; ++i) used[i] = false;
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
@@ -180,16 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        __syncwarp();
-        __syncthreads();  // consumers are done
-        if (lane == 0) {
-            // no copy may be in flight when the CTA exits (matters on the abort path)
-            for (int i = 0; i < kStages; ++i)
-                if (used[i]) mbar_wait(&full_bar[i], last_parity[i]);
-        }
-        return;
-    }
-
+    } else {
     // ================= consumers: warp w owns row-group 8*g8 + w of each unit ======
     const int g = lane >> 2, t = lane & 3;
     int stage = 0;
@@ -248,9 +239,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // ---- consume the unit's weight stages: block `warp` of each stage
             for (int kb = U.kb0; kb < U.kb1; ++kb) {
+                // warp-uniform: the MMAs below need the whole warp
                 bool have = false;
-                if (!s_abort) {
-                    have = mbar_wait(&full_bar[stage], phase);
+                if (!__any_sync(0xffffffffu, s_abort)) {
+                    have = __all_sync(0xffffffffu, mbar_wait(&full_bar[stage], phase));
                     if (!have) {
                         if (lane == 0) flag_error(a.err, kErrWaitTimeout);
                         s_abort = 1;
@@ -357,7 +349,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
+    }
+    // one barrier for producer and consumers; then no copy may still be in
+    // flight when the CTA exits (matters on the abort path)
+    __syncwarp();
     __syncthreads();
+    if (warp == kConsumerWarps && lane == 0)
+        for (int i = 0; i < kStages; ++i)
+            if (used[i]) mbar_wait(&full_bar[i], last_parity[i]);
 }
 
 // h = act(sum_s gate_part[s]) [* sum_s up_part[s]] for split-K up projections.

@@ -1,0 +1,399 @@
+// expert_tc.cu -- grouped expert GEMM on the 5th-generation tensor cores
+// (tcgen05 + tensor memory), for the batch regime and for decode batches
+// with many tokens per expert.
+//
+// Where the time goes: with hundreds of tokens per expert the expert matmuls
+// are compute-bound (DeepSpeed-Inference article, part 1: batch inference is
+// limited by compute; MoE-Lightning note, Hierarchical Roofline Model: the
+// FFN's intensity grows with the batch).  The pages hand this regime to a
+// vendor GEMM left unfused (DeepSpeed-Inference article, part 4); here it is a
+// grouped GEMM over the experts' ragged token segments with the activation
+// (SiLU(gate) * up) and the routing-weight scale fused into the epilogue.
+//
+// Orientation (weights on the M side): D[weight row, token] = sum_k W[row, k] x[token, k].
+//   A = 128 stored weight rows x 64 reduction elements: one contiguous 16 KB
+//       run of the packed layout (packing.h), already in the 64-byte-swizzled
+//       K-major form, fetched with one bulk copy;
+//   B = N tokens x 64 elements of the permuted activations (x_perm for the
+//       up projection, h for the down projection), fetched by a tensor-map
+//       copy with the 128-byte swizzle; rows past an expert's segment belong
+//       to the next expert or are zero-filled past the buffer, and are masked
+//       in the epilogue;
+//   D = 128 TMEM lanes x N fp32 columns, two buffers so that the epilogue of
+//       one tile overlaps the main loop of the next.
+// Tiles: (expert, reduction split, 128-row block, token tile), token tile
+// fastest so that concurrent CTAs share the weight block through L2.
+// Warp roles (192 threads, one persistent CTA per SM): warp 0 = producer (one
+// thread issues the copies), warp 1 = tensor-memory owner and MMA issuer (one
+// thread), warps 2-5 = epilogue (one TMEM lane per thread).
+// The SwiGLU up-projection's stored rows interleave 8 gate and 8 up rows, so a
+// thread holding a gate row finds the matching up row 8 lanes away.
+// Every wait is bounded; a wait that gives up sets kErrWaitTimeout in the
+// layer's error word and the CTA drains its copies and MMAs and returns.
+#include "common.cuh"
+#include "kernels.cuh"
+#include "packing.h"
+#include "tc.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kTcThreads = 192;
+constexpr int kEpiWarps = 4;
+constexpr int kATileBytes = 16384;  // 128 rows x 64 bf16
+constexpr int kMaxTcStages = 8;
+constexpr int kTcSmemBudget = 200 * 1024;
+
+enum Phase { kUp = 0, kDown = 1 };
+
+struct TcGeom {
+    int K;          // reduction length
+    int rg;         // row-groups of 16 stored rows
+    int n_rb;       // 128-row blocks
+    int nkb;        // K / 64
+    int splits;     // reduction splits
+    int N;          // token tile
+    int stages;
+    int b_bytes;    // N * 128
+    int tmem_cols;  // power of two >= 2N
+    uint32_t idesc;
+};
+
+struct TcTile {
+    int e, ks, rb, tt, off, q, kb0, kb1;
+};
+
+__device__ __forceinline__ TcTile tc_tile(long long u, const long long *prefix, const int *act,
+                                          const int *offs, const int *qs, int nact, const TcGeom &g) {
+    int i = 0;
+    while (i + 1 < nact && u >= prefix[i + 1]) ++i;
+    const long long local = u - prefix[i];
+    const int ntt = (qs[i] + g.N - 1) / g.N;
+    TcTile t;
+    t.e = act[i];
+    t.off = offs[i];
+    t.q = qs[i];
+    t.tt = static_cast<int>(local % ntt);
+    const long long rest = local / ntt;
+    t.rb = static_cast<int>(rest % g.n_rb);
+    t.ks = static_cast<int>(rest / g.n_rb);
+    t.kb0 = static_cast<int>((static_cast<long long>(g.nkb) * t.ks) / g.splits);
+    t.kb1 = static_cast<int>((static_cast<long long>(g.nkb) * (t.ks + 1)) / g.splits);
+    return t;
+}
+
+template <int PHASE, bool GATED>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_kernel(const ExpertTables tab, const ExpertArgs a, const TcGeom geo,
+              const __grid_constant__ CUtensorMap bmap) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint64_t full_bar[kMaxTcStages], empty_bar[kMaxTcStages];
+    __shared__ uint64_t tfull_bar[2], tempty_bar[2], done_bar;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_act[kMaxExperts], s_off[kMaxExperts], s_q[kMaxExperts];
+    __shared__ long long s_prefix[kMaxExperts + 1];
+    __shared__ int s_nact;
+    __shared__ volatile int s_abort;
+
+    // 1024-byte aligned operand area (swizzle atoms are address-based)
+    const uint32_t raw_s = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    uint8_t *a_slots = smem;
+    uint8_t *b_slots = smem + geo.stages * kATileBytes;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rows_total = a.T * a.k;
+
+    if (tid == 0) {
+        int n = 0;
+        long long acc = 0;
+        s_prefix[0] = 0;
+        for (int e = 0; e < a.E; ++e) {
+            const int off = a.offsets[e], end = a.offsets[e + 1];
+            if (off < 0 || end > rows_total || end < off) {
+                flag_error(a.err, kErrOffsets);
+                continue;
+            }
+            const int q = end - off;
+            bool take = q > 0;
+            if (a.n_only > 0) {
+                take = false;
+                for (int i = 0; i < a.n_only; ++i) take |= (a.only[i] == e && q > 0);
+            }
+            if (!take) continue;
+            s_act[n] = e;
+            s_off[n] = off;
+            s_q[n] = q;
+            acc += static_cast<long long>(geo.splits) * geo.n_rb * ((q + geo.N - 1) / geo.N);
+            s_prefix[++n] = acc;
+        }
+        s_nact = n;
+        s_abort = 0;
+        for (int i = 0; i < geo.stages; ++i) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&empty_bar[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull_bar[i], 1);
+            mbar_init(&tempty_bar[i], kEpiWarps);
+        }
+        mbar_init(&done_bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(&s_tmem, geo.tmem_cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = s_tmem;
+    const int nact = s_nact;
+    const long long total = nact ? s_prefix[nact] : 0;
+
+    uint32_t last_parity[kMaxTcStages];
+    bool used[kMaxTcStages];
+    for (int i = 0; i < kMaxTcStages; ++i) used[i] = false;
+    if (warp == 0) {
+        // ======================= producer =======================================
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (long long u = blockIdx.x; u < total && !s_abort; u += gridDim.x) {
+                const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
+                const uint8_t *w = static_cast<const uint8_t *>(PHASE == kUp ? tab.w1[t.e] : tab.w2[t.e]);
+                const int brow = t.off + t.tt * geo.N;
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                    if (!mbar_wait(&empty_bar[stage], phase ^ 1u)) {
+                        flag_error(a.err, kErrWaitTimeout);
+                        s_abort = 1;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full_bar[stage], kATileBytes + geo.b_bytes);
+                    const size_t blk = static_cast<size_t>(kb) * geo.rg + 8 * t.rb;
+                    bulk_g2s(a_slots + stage * kATileBytes, w + blk * kBlockBytes, kATileBytes,
+                             &full_bar[stage]);
+                    tma_load_2d(b_slots + stage * geo.b_bytes, &bmap, kb * 64, brow, &full_bar[stage]);
+                    used[stage] = true;
+                    last_parity[stage] = phase;
+                    if (++stage == geo.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ======================= MMA issuer =====================================
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int ntile = 0;
+            for (long long u = blockIdx.x; u < total && !s_abort; u += gridDim.x, ++ntile) {
+                const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
+                const int buf = ntile & 1;
+                const uint32_t use_parity = (ntile >> 1) & 1;
+                if (!mbar_wait(&tempty_bar[buf], use_parity ^ 1u)) {
+                    flag_error(a.err, kErrWaitTimeout);
+                    s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(buf * geo.N);
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                    if (!mbar_wait(&full_bar[stage], phase)) {
+                        flag_error(a.err, kErrWaitTimeout);
+                        s_abort = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t abase = smem_u32(a_slots + stage * kATileBytes);
+                    const uint32_t bbase = smem_u32(b_slots + stage * geo.b_bytes);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = smem_desc(abase + (kk >> 1) * 512 + (kk & 1) * 32, 16, 1024,
+                                                      kLayoutSw64);
+                        const uint64_t bd = smem_desc(bbase + kk * 32, 16, 1024, kLayoutSw128);
+                        tc_mma(d, ad, bd, geo.idesc, (kb > t.kb0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&empty_bar[stage]);  // slot free once these MMAs have read it
+                    if (++stage == geo.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                tc_commit(&tfull_bar[buf]);  // accumulator ready
+            }
+            tc_commit(&done_bar);  // every MMA this thread issued has completed
+            if (!mbar_wait(&done_bar, 0)) flag_error(a.err, kErrWaitTimeout);
+        }
+    } else {
+        // ======================= epilogue =======================================
+        const int lq = warp & 3;            // TMEM lane quarter this warp may access
+        const int row_in_tile = lq * 32 + lane;
+        int ntile = 0;
+        for (long long u = blockIdx.x; u < total; u += gridDim.x, ++ntile) {
+            // warp-uniform decisions: tcgen05.ld below needs the whole warp
+            if (__any_sync(0xffffffffu, s_abort)) break;
+            const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
+            const int buf = ntile & 1;
+            const uint32_t use_parity = (ntile >> 1) & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&tfull_bar[buf], use_parity))) {
+                if (lane == 0) flag_error(a.err, kErrWaitTimeout);
+                s_abort = 1;
+                break;
+            }
+            tc_fence_after();
+            const int R = t.rb * 128 + row_in_tile;  // stored weight row of this thread
+            const int tok0 = t.tt * geo.N;
+            for (int c0 = 0; c0 < geo.N; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(tmem_base + (static_cast<uint32_t>(lq * 32) << 16) +
+                              static_cast<uint32_t>(buf * geo.N + c0),
+                          v);
+                tmem_ld_wait();
+                if (PHASE == kUp && GATED) {
+                    const int r16 = R & 15;
+                    const int f = (R >> 4) * 8 + (r16 & 7);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float gv = __uint_as_float(v[j]);
+                        const float uv = __shfl_down_sync(0xffffffffu, gv, 8);
+                        const int tok = tok0 + c0 + j;
+                        if (r16 < 8 && tok < t.q) {
+                            const int pos = t.off + tok;
+                            if (geo.splits == 1) {
+                                static_cast<__nv_bfloat16 *>(a.h)[static_cast<size_t>(pos) * a.p + f] =
+                                    __float2bfloat16_rn(silu(gv) * uv);
+                            } else {
+                                const size_t o = (static_cast<size_t>(t.ks) * a.n_rows_cap + pos) * a.p + f;
+                                a.gate_part[o] = gv;
+                                a.up_part[o] = uv;
+                            }
+                        }
+                    }
+                } else if (PHASE == kUp) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int tok = tok0 + c0 + j;
+                        if (tok < t.q) {
+                            const int pos = t.off + tok;
+                            const float hv = __uint_as_float(v[j]);
+                            if (geo.splits == 1)
+                                static_cast<__nv_bfloat16 *>(a.h)[static_cast<size_t>(pos) * a.p + R] =
+                                    __float2bfloat16_rn(fmaxf(hv, 0.0f));
+                            else
+                                a.gate_part[(static_cast<size_t>(t.ks) * a.n_rows_cap + pos) * a.p + R] = hv;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int tok = tok0 + c0 + j;
+                        if (tok < t.q) {
+                            const int pos = t.off + tok;
+                            const int fi = a.gather[pos];
+                            const float wgt = (fi >= 0 && fi < rows_total) ? a.topk_w[fi] : 0.0f;
+                            a.ypart[(static_cast<size_t>(t.ks) * a.n_rows_cap + pos) * a.m + R] =
+                                wgt * __uint_as_float(v[j]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+        }
+    }
+    // one barrier for every role; then no copy may still be in flight and the
+    // tensor memory is released
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0 && lane == 0)
+        for (int i = 0; i < geo.stages; ++i)
+            if (used[i]) mbar_wait(&full_bar[i], last_parity[i]);
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, geo.tmem_cols);
+    }
+}
+
+// x_perm[pos] = x[gather[pos] / k] for the permuted rows (16-byte vectors).
+__global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ gather,
+                                   int rows, int k, int m, uint16_t *__restrict__ xp, uint32_t *err) {
+    const int vec = m / 8;
+    const long long n = static_cast<long long>(rows) * vec;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int pos = static_cast<int>(i / vec), v = static_cast<int>(i % vec);
+        const int fi = gather[pos];
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (fi >= 0 && fi < rows)
+            val = ld_nc_v4(x + static_cast<size_t>(fi / k) * m + v * 8);
+        else if (v == 0)
+            flag_error(err, kErrGatherIndex);
+        *reinterpret_cast<uint4 *>(xp + static_cast<size_t>(pos) * m + v * 8) = val;
+    }
+}
+
+template <int PHASE, bool GATED>
+cudaError_t launch_tc_t(const ExpertArgs &a, const TcGeom &g, const CUtensorMap &bmap, int num_sms,
+                        cudaStream_t s) {
+    const size_t smem = 1024 + static_cast<size_t>(g.stages) * (kATileBytes + g.b_bytes);
+    auto kern = tc_kernel<PHASE, GATED>;
+    static int configured = 0;
+    if (static_cast<int>(smem) > configured) {
+        const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     static_cast<int>(smem));
+        if (err != cudaSuccess) return err;
+        configured = static_cast<int>(smem);
+    }
+    kern<<<num_sms, kTcThreads, smem, s>>>(*a.tab, a, g, bmap);
+    return cudaGetLastError();
+}
+
+TcGeom make_tc_geom(int K, int rows, int splits, int N) {
+    TcGeom g;
+    g.K = K;
+    g.rg = rows / 16;
+    g.n_rb = rows / 128;
+    g.nkb = K / 64;
+    g.splits = splits;
+    g.N = N;
+    g.b_bytes = N * 128;
+    int st = kTcSmemBudget / (kATileBytes + g.b_bytes);
+    g.stages = st > kMaxTcStages ? kMaxTcStages : st;
+    int cols = 32;
+    while (cols < 2 * N) cols <<= 1;
+    g.tmem_cols = cols;
+    g.idesc = idesc_bf16_f32(128, N);
+    return g;
+}
+
+}  // namespace
+
+cudaError_t launch_gather_rows(const void *x, const int32_t *gather, int rows, int k, int m,
+                               void *x_perm, uint32_t *err, cudaStream_t s) {
+    const long long n = static_cast<long long>(rows) * (m / 8);
+    if (n == 0) return cudaSuccess;
+    long long blocks = (n + 255) / 256;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    gather_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        static_cast<const uint16_t *>(x), gather, rows, k, m, static_cast<uint16_t *>(x_perm), err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tc_up(const ExpertArgs &a, bool gated, int splits, int N, const CUtensorMap &xmap,
+                         int num_sms, cudaStream_t s) {
+    const TcGeom g = make_tc_geom(a.m, gated ? 2 * a.p : a.p, splits, N);
+    return gated ? launch_tc_t<kUp, true>(a, g, xmap, num_sms, s)
+                 : launch_tc_t<kUp, false>(a, g, xmap, num_sms, s);
+}
+
+cudaError_t launch_tc_down(const ExpertArgs &a, int splits, int N, const CUtensorMap &hmap,
+                           int num_sms, cudaStream_t s) {
+    const TcGeom g = make_tc_geom(a.p, a.m, splits, N);
+    return launch_tc_t<kDown, false>(a, g, hmap, num_sms, s);
+}
+
+}  // namespace moe

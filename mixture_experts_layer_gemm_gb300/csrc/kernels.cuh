@@ -1,6 +1,7 @@
 // kernels.cuh -- argument blocks and host launchers of the library's kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -78,6 +79,16 @@ cudaError_t launch_decode_down(const ExpertArgs &a, WeightType wt, int splits, i
 // finish a split-K up projection: h = act(sum_s gate_part) [* sum_s up_part]
 cudaError_t launch_decode_up_finish(const ExpertArgs &a, bool gated, int splits,
                                     cudaStream_t s);
+
+// Tensor-core (tcgen05) grouped GEMM: weights on the M side (128-row blocks),
+// N tokens per tile (16..256, multiple of 16); the tensor map fetches the
+// permuted activations (x_perm for up, h for down) in N x 64 boxes.
+cudaError_t launch_gather_rows(const void *x, const int32_t *gather, int rows, int k, int m,
+                               void *x_perm, uint32_t *err, cudaStream_t s);
+cudaError_t launch_tc_up(const ExpertArgs &a, bool gated, int splits, int N, const CUtensorMap &xmap,
+                         int num_sms, cudaStream_t s);
+cudaError_t launch_tc_down(const ExpertArgs &a, int splits, int N, const CUtensorMap &hmap,
+                           int num_sms, cudaStream_t s);
 
 // fp32 path (SIMT, warp-shuffle reductions)
 cudaError_t launch_simt_up(const ExpertArgs &a, bool gated, cudaStream_t s);

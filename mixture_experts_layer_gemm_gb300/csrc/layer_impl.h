@@ -25,6 +25,10 @@ struct moe_layer {
 
     // workspace
     void *h = nullptr;
+    void *x_perm = nullptr;  // [max_tokens*k x m] bf16: token rows in expert order (tensor-core path)
+    // tensor maps over x_perm and h for token tiles N = 16, 32, 64, 128, 256
+    bool tmap_ok[5] = {};
+    CUtensorMap tmap_x[5], tmap_h[5];
     float *ypart = nullptr;
     float *gate_part = nullptr, *up_part = nullptr;
     size_t decode_rows_cap = 0;

@@ -17,6 +17,8 @@
 #include <thread>
 #include <vector>
 
+#include <cudaTypedefs.h>
+
 #include "../../include/moe_layer.h"
 #include "common.cuh"
 #include "kernels.cuh"
@@ -69,6 +71,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
 constexpr int kSplitUpMax = 4, kSplitDownMax = 16;
+constexpr int kTcMinMeanTokens = 6;  // mean tokens per expert above which the tensor-core path runs
 
 // Smallest split of a K-long reduction whose staged token rows (8 * nt rows of
 // K / splits bf16) fit the shared-memory budget.
@@ -340,6 +343,11 @@ static moe_status_t alloc_workspace(moe_layer_t *L) {
             L->workspace_bytes += 2 * n * 4;
         }
     }
+    if (c.act_dtype == MOE_BF16 && c.weight_dtype == MOE_BF16) {
+        L->x_perm = L->dalloc(rows * c.m * 2, &err);
+        if (err) return cuda_fail(err, "cudaMalloc(x_perm)");
+        L->workspace_bytes += rows * c.m * 2;
+    }
     L->ypart = static_cast<float *>(L->dalloc(ypart_rows * c.m * 4, &err));
     if (err) return cuda_fail(err, "cudaMalloc(ypart)");
     L->err_word = static_cast<uint32_t *>(L->dalloc(4, &err));
@@ -500,6 +508,117 @@ ExpertArgs make_expert_args(moe_layer_t *L, const void *x, const moe_routing_t *
     return a;
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (the
+// library does not link the driver library itself).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+        }
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// 2D bf16 map over a [rows x K] row-major buffer, N x 64 boxes, 128-byte swizzle.
+static moe_status_t make_row_map(CUtensorMap *map, void *base, int K, size_t rows, int N) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(N)};
+    const cuuint32_t es[2] = {1u, 1u};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+    return MOE_OK;
+}
+
+static int tc_tile_n(int mean_q) {
+    if (mean_q <= 12) return 16;
+    if (mean_q <= 24) return 32;
+    if (mean_q <= 48) return 64;
+    if (mean_q <= 96) return 128;
+    return 256;
+}
+
+static moe_status_t tc_maps(moe_layer_t *L, int N, const CUtensorMap **xm, const CUtensorMap **hm) {
+    int idx = 0;
+    while ((16 << idx) < N) ++idx;
+    if (!L->tmap_ok[idx]) {
+        const size_t rows = static_cast<size_t>(L->cfg.max_tokens) * L->cfg.k;
+        moe_status_t st = make_row_map(&L->tmap_x[idx], L->x_perm, L->cfg.m, rows, N);
+        if (st == MOE_OK) st = make_row_map(&L->tmap_h[idx], L->h, L->cfg.p, rows, N);
+        if (st != MOE_OK) return st;
+        L->tmap_ok[idx] = true;
+    }
+    *xm = &L->tmap_x[idx];
+    *hm = &L->tmap_h[idx];
+    return MOE_OK;
+}
+
+// Splits of the reduction for tensor-core launches: the smallest count (up to
+// max_s and the K-block count) whose tiles fill the SMs in near-whole waves.
+static int tc_splits(int nkb, int rows, int N, int mean_q, int n_active, int num_sms, int max_s) {
+    const long long ntt = (mean_q + N - 1) / N;
+    int best = 1;
+    double best_eff = -1.0;
+    for (int S = 1; S <= max_s && S <= nkb; ++S) {
+        const long long tiles = static_cast<long long>(n_active) * S * (rows / 128) * ntt;
+        const long long waves = (tiles + num_sms - 1) / num_sms;
+        const double eff = static_cast<double>(tiles) / static_cast<double>(waves * num_sms);
+        if (eff >= 0.92) return S;
+        if (eff > best_eff) {
+            best_eff = eff;
+            best = S;
+        }
+    }
+    return best;
+}
+
+// Tensor-core path: gather the token rows into expert order, then the grouped
+// GEMMs (up with the activation fused, down with the routing weight fused).
+static moe_status_t run_experts_tc(moe_layer_t *L, ExpertArgs &a, int *splits_out, cudaStream_t s) {
+    const moe_config_t &c = L->cfg;
+    const bool gated = c.expert == MOE_EXPERT_SWIGLU;
+    const int rows = a.T * a.k;
+    const int mean_q = (rows + c.E - 1) / c.E;
+    const int N = tc_tile_n(mean_q);
+    const int rows_up = gated ? 2 * c.p : c.p;
+    int s_up = 1, s_down = 1;
+    if (rows <= static_cast<int>(L->decode_rows_cap)) {
+        const int n_act = expected_active(a.T, a.k, a.E);
+        s_up = tc_splits(c.m / 64, rows_up, N, mean_q, n_act, L->num_sms, L->split_up_max);
+        s_down = tc_splits(c.p / 64, c.m, N, mean_q, n_act, L->num_sms, L->split_down_max);
+        a.n_rows_cap = static_cast<int>(L->decode_rows_cap);
+    } else {
+        a.n_rows_cap = rows;
+    }
+    const CUtensorMap *xm = nullptr, *hm = nullptr;
+    moe_status_t st = tc_maps(L, N, &xm, &hm);
+    if (st != MOE_OK) return st;
+    st = launch_phase(L, MOE_PHASE_GATHER, s, "gather_rows", [&] {
+        return launch_gather_rows(a.x, a.gather, rows, a.k, c.m, L->x_perm, L->err_word, s);
+    });
+    if (st == MOE_OK)
+        st = launch_phase(L, MOE_PHASE_UP, s, "tc_up",
+                          [&] { return launch_tc_up(a, gated, s_up, N, *xm, L->num_sms, s); });
+    if (st == MOE_OK && s_up > 1)
+        st = launch_phase(L, MOE_PHASE_UP_FINISH, s, "up_finish",
+                          [&] { return launch_decode_up_finish(a, gated, s_up, s); });
+    if (st == MOE_OK)
+        st = launch_phase(L, MOE_PHASE_DOWN, s, "tc_down",
+                          [&] { return launch_tc_down(a, s_down, N, *hm, L->num_sms, s); });
+    *splits_out = s_down;
+    return st;
+}
+
 // Expert MLPs for the experts of `a` (all with tokens, or a.only) into ypart;
 // returns the number of ypart splits written.
 moe_status_t run_experts(moe_layer_t *L, ExpertArgs &a, int regime, int *splits_out,
@@ -515,7 +634,20 @@ moe_status_t run_experts(moe_layer_t *L, ExpertArgs &a, int regime, int *splits_
         *splits_out = 1;
         return st;
     }
-    (void)regime;
+    // regime: the weight-streaming GEMV while experts see few tokens, the
+    // tensor-core grouped GEMM beyond (bf16 weights; rows in 128-row blocks)
+    const int mean_q = (rows + c.E - 1) / c.E;
+    const bool tc_shape = c.weight_dtype == MOE_BF16 && L->x_perm &&
+                          (gated ? (2 * c.p) % 128 : c.p % 128) == 0 && c.m % 128 == 0;
+    const bool fits_decode = rows <= static_cast<int>(L->decode_rows_cap);
+    bool use_tc = false;
+    if (regime == 2) {
+        if (!tc_shape) return fail(MOE_ERR_UNSUPPORTED, "batch kernels need bf16 weights and 128-row blocks");
+        use_tc = true;
+    } else if (regime == 0) {
+        use_tc = tc_shape && (mean_q > kTcMinMeanTokens || !fits_decode);
+    }
+    if (use_tc) return run_experts_tc(L, a, splits_out, s);
     const WeightType wt = (c.weight_dtype == MOE_I8) ? WeightType::kI8 : WeightType::kBF16;
     int nt = decode_token_tiles(a.T, a.k, a.E);
     int s_up, s_down;

@@ -87,3 +87,22 @@ def test_phi35_decode(phi, T, locality):
         same = [t for t in range(1, T) if np.array_equal(x[t], x[t - 1])]
         assert same and all(np.array_equal(run.ids[t], run.ids[t - 1]) for t in same)
     ml.close()
+
+
+@pytest.mark.parametrize("T", [512, 2048, 8192])
+def test_mixtral_batch_zipf(mixtral, T):
+    """Batch / prefill with Zipf(1.2) expert popularity (router bias)."""
+    shape = wl.MIXTRAL.with_zipf(1.2)
+    layer = wl.Layer(shape, mixtral.w_router, wl.zipf_bias(shape.E, 1.2), mixtral.w1, mixtral.w2,
+                     mixtral.w3)
+    ml = moe.MoELayer(layer, T, with_logits=True)
+    run = _check(ml, layer, T, seed=400 + T, n_sample=8, tol=1e-2)
+    assert run.counts[0] == run.counts.max()
+    ml.close()
+
+
+@pytest.mark.parametrize("T", [512, 4096])
+def test_phi35_batch(phi, T):
+    ml = moe.MoELayer(phi, T, with_logits=True)
+    _check(ml, phi, T, seed=500 + T, n_sample=8, tol=1e-2)
+    ml.close()

@@ -157,6 +157,37 @@ def test_relu_bf16_decode(T):
     run_and_check(RELU_BF16, T, seed=8, regime=moe.REGIME_DECODE)
 
 
+# ---- bf16 layers through the tensor-core (tcgen05) grouped GEMM ------------------------
+@pytest.mark.parametrize("T", [1, 5, 16, 37, 64, 200, 700])
+def test_swiglu_bf16_tensor_core(T):
+    run_and_check(SWIGLU_BF16, T, seed=27, regime=moe.REGIME_BATCH)
+
+
+@pytest.mark.parametrize("T", [3, 90, 640])
+def test_relu_bf16_tensor_core(T):
+    run_and_check(RELU_BF16, T, seed=28, regime=moe.REGIME_BATCH)
+
+
+def test_zipf_batch_auto_regime():
+    """A skewed batch with more than the decode row cap: the automatic choice
+    is the tensor-core path, with hot and cold experts of very uneven size."""
+    run, _ = run_and_check(SWIGLU_BF16.with_zipf(1.2), 900, seed=29)
+    assert run.counts[0] > 4 * run.counts[-1]
+
+
+def test_tensor_core_and_decode_paths_agree():
+    layer = get_layer(SWIGLU_BF16, seed=30)
+    x = wl.make_tokens(SWIGLU_BF16, 48, seed=31)
+    ys = []
+    for regime in (moe.REGIME_DECODE, moe.REGIME_BATCH):
+        ml = moe.MoELayer(layer, 48)
+        ml.set_regime(regime)
+        ys.append(f64(Run(ml, x).y_np))
+        ml.close()
+    rel = np.linalg.norm(ys[0] - ys[1], axis=1) / np.linalg.norm(ys[1], axis=1)
+    assert rel.max() <= 1e-2
+
+
 @pytest.mark.parametrize("T", [2, 33, 100])
 def test_odd_shapes_bf16(T):
     """m=320, p=192, E=5, k=3: splits that do not divide the reduction evenly."""
