@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--tokens", default="1,4,16,64",
                     help="decode batches per step (profiling runs use one)")
     ap.add_argument("--copies", type=int, default=2, help="weight copies that alternate")
+    ap.add_argument("--zipf", type=float, default=None,
+                    help="router bias making expert popularity Zipf(s) (batch workloads)")
     ap.add_argument("--shape", default="mixtral", choices=["mixtral", "phi", "small"],
                     help="mixtral (the benchmark), phi (Phi-3.5-MoE), small (profiling: "
                          "m=4096, p=3584, E=8, 0.7 GB of weights)")
@@ -183,12 +185,15 @@ def shape_of(args):
     import workloads as wl
     base = {"mixtral": wl.MIXTRAL, "phi": wl.PHI35,
             "small": dataclasses.replace(wl.MIXTRAL, name="profile-small", p=3584)}[args.shape]
+    if args.zipf is not None:
+        base = base.with_zipf(args.zipf)
     return base if args.weights == "bf16" else base.with_weight("i8")
 
 
 def workload_config(shape, weights, flush_note):
     ts = ",".join(str(t) for t in TOKENS)
-    return {"workload": f"{shape.name} moe layer decode, T in {{{ts}}}, {weights} weights",
+    regime = "decode" if max(TOKENS) <= 64 else "batch"
+    return {"workload": f"{shape.name} moe layer {regime}, T in {{{ts}}}, {weights} weights",
             "model": f"{shape.name}-shaped single MoE FFN layer", "m": shape.m, "p": shape.p,
             "E": shape.E, "k": shape.k, "expert": "swiglu", "tokens_per_step": sum(TOKENS),
             "global_batch": sum(TOKENS), "seq_len": 1, "parallelism": "replicas",
@@ -296,37 +301,89 @@ def run_ours(args, world, rank, local):
     for c in copies:
         c.set_timing(False)
 
-    # algorithmic bytes of the up-projection per call: active experts' W1 and W3,
-    # the token rows read and the hidden rows written
+    # ---- algorithmic work per call (SURVEY-style per-unit figures) -------------------
+    # up: active experts' W1 and W3 (+ int8 scales), token rows read, hidden rows written;
+    #     flops 2 * (2 m p) per routed (token, slot) for SwiGLU (2 m p for ReLU)
+    # down: active experts' W2 (+ scales), hidden rows read; flops 2 m p per (token, slot)
     wbytes = 1 if args.weights == "i8" else 2
-    bytes_up, bytes_down, active = 0, 0, {}
+    n_up = 2 if shape.has_w3 else 1
+    work, active = {}, {}
     for i, T in enumerate(TOKENS):
         c = copies[i % len(copies)]
         c.route(xs[T], stream=stream)
         torch.cuda.synchronize()
         n_act = int((c.counts.cpu() > 0).sum())
         active[T] = n_act
-        scale_up = 2 * shape.p * 4 if args.weights == "i8" else 0
+        scale_up = n_up * shape.p * 4 if args.weights == "i8" else 0
         scale_dn = shape.m * 4 if args.weights == "i8" else 0
-        bytes_up += n_act * (2 * shape.m * shape.p * wbytes + scale_up) + T * shape.m * 2 \
-            + T * shape.k * shape.p * 2
-        bytes_down += n_act * (shape.m * shape.p * wbytes + scale_dn) + T * shape.k * shape.p * 2
+        rows = T * shape.k
+        work[T] = {
+            "up_bytes": n_act * (n_up * shape.m * shape.p * wbytes + scale_up) + T * shape.m * 2
+            + rows * shape.p * 2,
+            "down_bytes": n_act * (shape.m * shape.p * wbytes + scale_dn) + rows * shape.p * 2,
+            "up_flops": 2.0 * n_up * shape.m * shape.p * rows,
+            "down_flops": 2.0 * shape.m * shape.p * rows,
+            "path": "tensor-core" if (rows + shape.E - 1) // shape.E > 6 and args.weights == "bf16"
+            else "gemv"}
+    bytes_up = sum(w["up_bytes"] for w in work.values())
+    bytes_down = sum(w["down_bytes"] for w in work.values())
+    flops_up = sum(w["up_flops"] for w in work.values())
     up_ms = sum(t["up"][0] for t in tim)
     up_n = sum(t["up"][1] for t in tim)
-    dn_ms = sum(t["down"][0] for t in tim)
     phase_ms = {k: sum(t[k][0] for t in tim) / args.steps for k in tim[0]}
     hbm, tf, tf_sus, src = peaks()
-    achieved = bytes_up * args.steps / (up_ms * 1e-3) / 1e9
     layer_bytes = bytes_up + bytes_down
     layer_gbs = layer_bytes * args.steps / (ms * 1e-3) / 1e9
+    layer_tf = (flops_up + sum(w["down_flops"] for w in work.values())) * args.steps / (ms * 1e-3) / 1e12
+
+    # per-T breakdown: each batch alone, event-timed per launch
+    per_t = {}
+    for i, T in enumerate(TOKENS):
+        for c in copies:
+            c.timings(reset=True)
+            c.set_timing(True)
+        for it in range(20):
+            c = copies[it % len(copies)]
+            c.route(xs[T], stream=stream)
+            c.forward(xs[T], ys[T], stream=stream)
+        torch.cuda.synchronize()
+        tt = [c.timings(reset=True) for c in copies]
+        for c in copies:
+            c.set_timing(False)
+        u_ms = sum(t["up"][0] for t in tt) / 20
+        d_ms = sum(t["down"][0] for t in tt) / 20
+        tot = sum(sum(v[0] for v in t.values()) for t in tt) / 20
+        w = work[T]
+        per_t[str(T)] = {"path": w["path"], "active_experts": active[T], "layer_us": tot * 1e3,
+                         "up_us": u_ms * 1e3, "down_us": d_ms * 1e3,
+                         "up_gbs": w["up_bytes"] / (u_ms * 1e-3) / 1e9,
+                         "down_gbs": w["down_bytes"] / (d_ms * 1e-3) / 1e9,
+                         "up_tflops": w["up_flops"] / (u_ms * 1e-3) / 1e12,
+                         "down_tflops": w["down_flops"] / (d_ms * 1e-3) / 1e12}
+
+    # the dominant kernel: the expert up-projection; HBM-bound while the batch is
+    # weight-streaming, tensor-bound once most of the work runs on the tensor-core path
+    tensor_bound = sum(w["up_flops"] for w in work.values() if w["path"] == "tensor-core") > \
+        0.5 * flops_up and max(TOKENS) >= 256
     trec = traffic_record(os.path.join(ROOT, "mixture_experts_layer_gemm_gb300", "csrc",
                                        "expert_decode.cu"))
-    roofline = {"kernel": "decode_up (expert up-projection GEMV, W1 and W3 + SiLU*gate)",
-                "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "peak_source": f"{src} (hbm_gbs)",
-                "algorithmic_bytes_per_step": bytes_up,
-                "avg_launch_us": up_ms * 1e3 / max(up_n, 1),
-                "traffic": None if trec is None else trec.get("bytes_per_step")}
+    if tensor_bound:
+        achieved = flops_up * args.steps / (up_ms * 1e-3) / 1e12
+        roofline = {"kernel": "tc_up (tcgen05 grouped GEMM, W1 and W3 + SiLU*gate)",
+                    "bound": "tensor", "achieved": achieved, "peak": tf, "unit": "TFLOP/s",
+                    "frac": achieved / tf, "peak_source": f"{src} (bf16_tflops burst)",
+                    "frac_of_sustained": achieved / tf_sus if tf_sus else None,
+                    "algorithmic_flops_per_step": flops_up,
+                    "avg_launch_us": up_ms * 1e3 / max(up_n, 1), "traffic": None}
+    else:
+        achieved = bytes_up * args.steps / (up_ms * 1e-3) / 1e9
+        roofline = {"kernel": "expert up-projection (W1 and W3 + SiLU*gate): decode GEMV for "
+                              "T <= 16, tcgen05 for larger T",
+                    "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                    "frac": achieved / hbm, "peak_source": f"{src} (hbm_gbs)",
+                    "algorithmic_bytes_per_step": bytes_up,
+                    "avg_launch_us": up_ms * 1e3 / max(up_n, 1),
+                    "traffic": None if trec is None else trec.get("bytes_per_step")}
 
     # end to end: pinned host buffers, H2D of x and D2H of y inside the timed region
     xh = {T: xs[T].cpu().pin_memory() for T in TOKENS}
@@ -382,7 +439,8 @@ def run_ours(args, world, rank, local):
                 "layer_hbm": {"achieved": layer_gbs, "unit": "GB/s", "frac": layer_gbs / hbm,
                               "algorithmic_bytes_per_step": layer_bytes,
                               "note": "whole step: expert weights + activations / step time"},
-                "phase_ms_per_step": phase_ms, "active_experts": active,
+                "layer_tflops": layer_tf,
+                "phase_ms_per_step": phase_ms, "active_experts": active, "per_T": per_t,
                 "cpu_baseline": cpu,
                 "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
                         "d2h_bytes_per_step": io_bytes},
