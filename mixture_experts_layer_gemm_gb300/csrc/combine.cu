@@ -3,7 +3,8 @@
 // (HARMOEny write-up, part 2 and part 3.3 step 6: finished tokens return to
 // their owner).  The routing weight was applied in the down-projection
 // epilogue; a split-K down projection leaves `splits` partial rows, added
-// here first (in split order), then the k slots (in ascending j), in fp32,
+// here first (in a fixed order over the splits), then the k slots (in
+// ascending j), in fp32,
 // rounded once to the activation type.  Deterministic: no atomics.
 #include "common.cuh"
 #include "kernels.cuh"
@@ -27,10 +28,24 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
                 flag_error(a.err, kErrGatherIndex);
                 continue;
             }
+            // partial rows of the split reduction, four loads in flight at a
+            // time, added in a fixed order: ((p0 + p1) + (p2 + p3)) per group,
+            // groups in split order
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s = 0; s < a.splits; ++s) {
-                const float4 p = *reinterpret_cast<const float4 *>(
-                    a.ypart + s * a.split_stride + static_cast<size_t>(pos) * a.m + c);
+            const float *base = a.ypart + static_cast<size_t>(pos) * a.m + c;
+            int s = 0;
+            for (; s + 4 <= a.splits; s += 4) {
+                const float4 p0 = __ldcg(reinterpret_cast<const float4 *>(base + (s + 0) * a.split_stride));
+                const float4 p1 = __ldcg(reinterpret_cast<const float4 *>(base + (s + 1) * a.split_stride));
+                const float4 p2 = __ldcg(reinterpret_cast<const float4 *>(base + (s + 2) * a.split_stride));
+                const float4 p3 = __ldcg(reinterpret_cast<const float4 *>(base + (s + 3) * a.split_stride));
+                v.x += (p0.x + p1.x) + (p2.x + p3.x);
+                v.y += (p0.y + p1.y) + (p2.y + p3.y);
+                v.z += (p0.z + p1.z) + (p2.z + p3.z);
+                v.w += (p0.w + p1.w) + (p2.w + p3.w);
+            }
+            for (; s < a.splits; ++s) {
+                const float4 p = __ldcg(reinterpret_cast<const float4 *>(base + s * a.split_stride));
                 v.x += p.x;
                 v.y += p.y;
                 v.z += p.z;

@@ -141,6 +141,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     const long long units = static_cast<long long>(s_nact) * geo.splits * geo.rg8;
+    // each CTA takes a contiguous range of units, so that consecutive units
+    // share the expert and split and reuse the staged token rows
+    const long long u_begin = (units * blockIdx.x) / gridDim.x;
+    const long long u_end = (units * (blockIdx.x + 1)) / gridDim.x;
 
     // A slot is re-armed only after all consumer warps released it, which they
     // do only after seeing its copy land; so at any time each slot has at most
@@ -153,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            for (long long u = blockIdx.x; u < units && !s_abort; u += gridDim.x) {
+            for (long long u = u_begin; u < u_end && !s_abort; ++u) {
                 const Unit U = decode_unit(u, s_act, geo, a, rows_total);
                 if (!U.ok) continue;
                 const uint8_t *w = static_cast<const uint8_t *>(PHASE == kUp ? tab.w1[U.e] : tab.w2[U.e]);
@@ -186,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     int staged_e = -1, staged_ks = -1, staged_tp = -1;
-    for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+    for (long long u = u_begin; u < u_end; ++u) {
         // one decision for all consumer warps: the named barriers need all of them
         if (named_sync_or(kBarConsumers, kConsumers, s_abort)) break;
         const Unit U = decode_unit(u, s_act, geo, a, rows_total);

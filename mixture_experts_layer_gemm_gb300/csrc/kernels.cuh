@@ -13,11 +13,14 @@ constexpr int kExpertTableMax = 64;
 struct RouterArgs {
     const void *x;       // [T x m] act type
     const float *wrt;    // [E x m] router weights, transposed, fp32
+    const void *wra;     // [E x m] the same, in the activation type (exact)
     const float *bias;   // [E] or nullptr
     int T, m, E, k;
     int32_t *ids;        // [T*k]
     float *w;            // [T*k]
     float *logits;       // [T*E] or nullptr
+    unsigned *ticket;    // device counter, 0 between launches (fused permute)
+    uint32_t *err;
 };
 
 struct PermuteArgs {
@@ -26,7 +29,9 @@ struct PermuteArgs {
     int32_t *counts, *offsets, *gather, *scatter;
 };
 
-cudaError_t launch_router_topk(const RouterArgs &a, bool act_bf16, cudaStream_t s);
+// Router + top-k with the permute fused in (the launch's last CTA runs it).
+cudaError_t launch_router_topk(const RouterArgs &a, const PermuteArgs &pa, bool act_bf16,
+                               cudaStream_t s);
 cudaError_t launch_topk_from_logits(const float *logits, int T, int E, int k, int32_t *ids,
                                     float *w, cudaStream_t s);
 cudaError_t launch_topk_copy_validate(const int32_t *ids_in, const float *w_in, int T, int E,

@@ -17,6 +17,7 @@ struct moe_layer {
 
     // weights (resident copy, or unused for paged layers)
     float *wrt = nullptr;      // router [E x m] fp32
+    void *wra = nullptr;       // router [E x m] in the activation type
     float *bias = nullptr;     // [E] fp32
     uint8_t *weights = nullptr;
     size_t expert_stride = 0;  // bytes between experts inside `weights`
@@ -35,6 +36,7 @@ struct moe_layer {
     int split_up_max = 1, split_down_max = 1;
     size_t workspace_bytes = 0;
     uint32_t *err_word = nullptr;
+    unsigned *ticket = nullptr;  // fused-permute completion counter (0 between launches)
 
     // paged weights
     moe_pool_t *pool = nullptr;

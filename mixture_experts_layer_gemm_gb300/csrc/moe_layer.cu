@@ -222,6 +222,12 @@ static moe_status_t ingest_weights(moe_layer_t *L, const void *w_router, const f
     CUDA_TRY(cudaMemcpyAsync(stage_r, w_router, static_cast<size_t>(c.m) * c.E * ab,
                              cudaMemcpyHostToDevice, s));
     CUDA_TRY(launch_router_prep(stage_r, bf16_act, c.m, c.E, L->wrt, s));
+    // activation-typed copy [E_pad x m], zero rows past E (E_pad = 8, 16, 32 or 64)
+    const int e_pad = c.E <= 8 ? 8 : c.E <= 16 ? 16 : c.E <= 32 ? 32 : 64;
+    L->wra = L->dalloc(static_cast<size_t>(c.m) * e_pad * ab, &err);
+    if (err) return cuda_fail(err, "cudaMalloc(router)");
+    CUDA_TRY(cudaMemsetAsync(L->wra, 0, static_cast<size_t>(c.m) * e_pad * ab, s));
+    CUDA_TRY(launch_transpose(stage_r, L->wra, c.m, c.E, static_cast<int>(ab), s));
     if (c.has_router_bias) {
         L->bias = static_cast<float *>(L->dalloc(static_cast<size_t>(c.E) * 4, &err));
         if (err) return cuda_fail(err, "cudaMalloc(bias)");
@@ -350,9 +356,10 @@ static moe_status_t alloc_workspace(moe_layer_t *L) {
     }
     L->ypart = static_cast<float *>(L->dalloc(ypart_rows * c.m * 4, &err));
     if (err) return cuda_fail(err, "cudaMalloc(ypart)");
-    L->err_word = static_cast<uint32_t *>(L->dalloc(4, &err));
+    L->err_word = static_cast<uint32_t *>(L->dalloc(8, &err));
     if (err) return cuda_fail(err, "cudaMalloc(error word)");
-    CUDA_TRY(cudaMemset(L->err_word, 0, 4));
+    CUDA_TRY(cudaMemset(L->err_word, 0, 8));
+    L->ticket = reinterpret_cast<unsigned *>(L->err_word + 1);
     L->workspace_bytes += rows * c.p * ab + ypart_rows * c.m * 4;
     return MOE_OK;
 }
@@ -438,14 +445,17 @@ extern "C" moe_status_t moe_route(moe_layer_t *L, const void *x, int T, moe_rout
     if (st != MOE_OK) return st;
     if (T > 0 && (!x || !aligned16(x))) return fail(MOE_ERR_INVALID_ARG, "x is NULL or not 16-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    RouterArgs ra{x, L->wrt, L->bias, T, L->cfg.m, L->cfg.E, L->cfg.k, r->topk_ids, r->topk_w,
-                  r->logits};
-    if (T > 0) {
-        st = launch_phase(L, MOE_PHASE_ROUTER, s, "router_topk",
-                          [&] { return launch_router_topk(ra, L->cfg.act_dtype == MOE_BF16, s); });
-        if (st != MOE_OK) return st;
-    }
-    return run_permute(L, T, r, s);
+    if (T == 0) return run_permute(L, T, r, s);
+    RouterArgs ra{x, L->wrt, L->wra, L->bias, T, L->cfg.m, L->cfg.E, L->cfg.k, r->topk_ids,
+                  r->topk_w, r->logits, L->ticket, L->err_word};
+    PermuteArgs pa{r->topk_ids, T, L->cfg.k, L->cfg.E, r->counts, r->offsets, r->gather_index,
+                   r->scatter_index};
+    st = launch_phase(L, MOE_PHASE_ROUTER, s, "router_topk_permute",
+                      [&] { return launch_router_topk(ra, pa, L->cfg.act_dtype == MOE_BF16, s); });
+    if (st != MOE_OK) return st;
+    CUDA_TRY(cudaEventRecord(L->done, s));
+    r->T = T;
+    return MOE_OK;
 }
 
 extern "C" moe_status_t moe_route_from_logits(moe_layer_t *L, const float *logits, int T,

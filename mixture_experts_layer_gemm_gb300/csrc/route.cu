@@ -5,10 +5,10 @@
 // Router and gating: HARMOEny write-up, part 1 "What is MoE" (a router picks
 // experts per token) and part 3.3 step 1; the gating network runs on the GPU
 // in the expert-cache article, section 3.1.  The fusion of GEMM, softmax and
-// selection into one kernel follows the Deep-Fusion rule of the
-// DeepSpeed-Inference article, part 2: tile along the token dimension, which
-// carries no cross-tile dependency, and keep the reduction (over m, then over
-// E) inside the tile.
+// selection (and the permute) into one kernel follows the Deep-Fusion rule of
+// the DeepSpeed-Inference article, part 2: tile along the token dimension,
+// which carries no cross-tile dependency, and keep the reduction (over m, then
+// over E) inside the tile.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -52,85 +52,213 @@ __device__ __forceinline__ void select_topk(const float (&l)[EMAX], int E, int k
         if (j < k) w[j] = w[j] / denom;
 }
 
-// One CTA per group of 8 tokens.  The 256 threads split the hidden dimension
-// into 16-byte chunks (chunk c goes to thread c mod 256), so even a single
-// token spreads its m x E router products over the whole CTA.  For each token
-// every thread adds its products in sequence, a warp-shuffle tree adds the 32
-// lane sums, and one thread per (token, expert) adds the 8 warp sums in warp
-// order: a fixed, deterministic order.  Then warp w selects the top-k of
-// token w.  x: [T x m] (fp32 or bf16); wrt: router weights transposed to
-// [E x m] fp32 (an exact copy of the given values).
-constexpr int kRouterTokens = 8;
+// Histogram, exclusive scan and stable scatter of the n = T*k flat indices by
+// expert, done by one CTA (any multiple of 32 threads up to 1024):
+//   pass 1: counts[e] by shared-memory integer atomics (order-free);
+//   scan:   offsets by one warp;
+//   pass 2: chunks of blockDim flat indices in index order; inside a warp the
+//           rank of an index among equal ids is the popcount of the match
+//           mask below its lane; per-warp counts are scanned across warps per
+//           expert, so positions follow flat-index order exactly.
+// The ids are read through L2 (they may have been written by other CTAs of the
+// same launch).
+struct PermuteSmem {
+    int count[kMaxExperts];
+    int base[kMaxExperts];
+    int warp_cnt[32][kMaxExperts];
+};
 
-template <typename ActT, int EMAX>
-__global__ void __launch_bounds__(256) router_topk_kernel(RouterArgs a) {
-    __shared__ float s_part[kRouterTokens][8][EMAX];
-    __shared__ float s_logit[kRouterTokens][EMAX];
+__device__ void permute_block(const PermuteArgs &a, PermuteSmem &sm) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t0 = blockIdx.x * kRouterTokens;
-    const int ntok = min(kRouterTokens, a.T - t0);
+    const int nthreads = blockDim.x;
+    const int n = a.T * a.k;
+    if (tid < kMaxExperts) sm.count[tid] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += nthreads) {
+        int id = __ldcg(a.ids + i);
+        if (id < 0 || id >= a.E) id = 0;  // flagged by whoever produced ids
+        atomicAdd(&sm.count[id], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // exclusive scan over E <= 64 counts, two per lane
+        const int c0 = (2 * lane < a.E) ? sm.count[2 * lane] : 0;
+        const int c1 = (2 * lane + 1 < a.E) ? sm.count[2 * lane + 1] : 0;
+        int incl = c0 + c1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const int excl = incl - c0 - c1;
+        if (2 * lane < a.E) {
+            sm.base[2 * lane] = excl;
+            a.counts[2 * lane] = c0;
+            a.offsets[2 * lane] = excl;
+        }
+        if (2 * lane + 1 < a.E) {
+            sm.base[2 * lane + 1] = excl + c0;
+            a.counts[2 * lane + 1] = c1;
+            a.offsets[2 * lane + 1] = excl + c0;
+        }
+        if (lane == 31) a.offsets[a.E] = incl;
+    }
+    __syncthreads();
+    const unsigned lt_mask = (1u << lane) - 1u;
+    const int nwarps = nthreads >> 5;
+    for (int c0 = 0; c0 < n; c0 += nthreads) {
+        const int i = c0 + tid;
+        const bool valid = i < n;
+        int id = valid ? __ldcg(a.ids + i) : -1;
+        if (valid && (id < 0 || id >= a.E)) id = 0;
+        for (int e = lane; e < a.E; e += 32) sm.warp_cnt[warp][e] = 0;
+        __syncwarp();
+        const unsigned peers = __match_any_sync(0xffffffffu, id);
+        const int rank = __popc(peers & lt_mask);
+        if (valid && lane == __ffs(peers) - 1) sm.warp_cnt[warp][id] = __popc(peers);
+        __syncthreads();
+        if (tid < a.E) {
+            int run = sm.base[tid];
+            for (int w = 0; w < nwarps; ++w) {
+                const int c = sm.warp_cnt[w][tid];
+                sm.warp_cnt[w][tid] = run;
+                run += c;
+            }
+            sm.base[tid] = run;
+        }
+        __syncthreads();
+        if (valid) {
+            const int pos = sm.warp_cnt[warp][id] + rank;
+            a.gather[pos] = i;
+            a.scatter[i] = pos;
+        }
+        __syncthreads();
+    }
+}
+
+// Router GEMM + softmax + top-k, with the permute fused in.
+// One CTA per group of TOK tokens (TOK * EMAX <= 64).  The 256 threads split
+// the hidden dimension into 16-byte chunks (chunk c goes to thread c mod 256);
+// a thread loads the router weights of its chunk once and applies them to all
+// TOK tokens, keeping TOK x E partial sums.  Every thread adds its products in
+// sequence, a warp-shuffle tree adds the 32 lane sums and one thread per
+// (token, expert) adds the 8 warp sums in warp order: a fixed, deterministic
+// order.  Warp w then selects the top-k of token w.  The last CTA to finish
+// (a fenced ticket on a counter it resets) runs the permute for the whole batch.
+// With SMEM_W the whole transposed router matrix (E x m, activation type) is
+// first brought into shared memory by bulk copies, so that each thread's
+// products wait on shared-memory reads instead of a chain of L2 round trips.
+template <typename ActT, int EMAX, bool SMEM_W>
+__global__ void __launch_bounds__(256) router_topk_kernel(RouterArgs a, PermuteArgs pa) {
+    constexpr int TOK = (64 / EMAX) < 1 ? 1 : (64 / EMAX);
+    extern __shared__ __align__(16) uint8_t s_w[];
+    __shared__ float s_part[8][TOK][EMAX];
+    __shared__ float s_logit[TOK][EMAX];
+    __shared__ PermuteSmem psm;
+    __shared__ int s_last;
+    __shared__ uint64_t s_wbar;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t0 = blockIdx.x * TOK;
+    const int ntok = min(TOK, a.T - t0);
     constexpr int kVec = 16 / sizeof(ActT);  // elements per 16-byte chunk
     const int nchunks = a.m / kVec;
-
-    for (int tk = 0; tk < ntok; ++tk) {
-        const ActT *xr = static_cast<const ActT *>(a.x) + static_cast<size_t>(t0 + tk) * a.m;
-        float acc[EMAX];
-#pragma unroll
-        for (int e = 0; e < EMAX; ++e) acc[e] = 0.0f;
-        for (int ch = tid; ch < nchunks; ch += 256) {
-            const int c = ch * kVec;
-            const uint4 raw = ld_nc_v4(xr + c);
-            float xv[kVec];
-            if constexpr (sizeof(ActT) == 2) {
-                const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    xv[2 * i] = bf16lo(u[i]);
-                    xv[2 * i + 1] = bf16hi(u[i]);
-                }
-            } else {
-                xv[0] = __uint_as_float(raw.x);
-                xv[1] = __uint_as_float(raw.y);
-                xv[2] = __uint_as_float(raw.z);
-                xv[3] = __uint_as_float(raw.w);
+    if constexpr (SMEM_W) {
+        const uint32_t bytes = static_cast<uint32_t>(a.E) * a.m * sizeof(ActT);
+        if (tid == 0) {
+            mbar_init(&s_wbar, 1);
+            fence_barrier_init();
+            mbar_arrive_expect_tx(&s_wbar, bytes);
+            for (uint32_t off = 0; off < bytes; off += 32768u) {
+                const uint32_t n = bytes - off < 32768u ? bytes - off : 32768u;
+                bulk_g2s(s_w + off, static_cast<const uint8_t *>(a.wra) + off, n, &s_wbar);
             }
+        }
+        __syncthreads();
+        if (!mbar_wait(&s_wbar, 0) && tid == 0) flag_error(a.err, kErrWaitTimeout);
+    }
+
+    float acc[TOK][EMAX];
 #pragma unroll
-            for (int e = 0; e < EMAX; ++e) {
-                if (e < a.E) {
+    for (int tk = 0; tk < TOK; ++tk)
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) acc[tk][e] = 0.0f;
+    for (int ch = tid; ch < nchunks; ch += 256) {
+        const int c = ch * kVec;
+        uint4 xraw[TOK];  // this chunk of every token of the group, packed
+#pragma unroll
+        for (int tk = 0; tk < TOK; ++tk)
+            xraw[tk] = (tk < ntok) ? ld_nc_v4(static_cast<const ActT *>(a.x) +
+                                              static_cast<size_t>(t0 + tk) * a.m + c)
+                                   : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) {
+            if (e < a.E) {
+                float wv[kVec];
+                if constexpr (SMEM_W) {
+                    const uint4 wr = *reinterpret_cast<const uint4 *>(
+                        s_w + (static_cast<size_t>(e) * a.m + c) * sizeof(ActT));
+                    const uint32_t wu[4] = {wr.x, wr.y, wr.z, wr.w};
+                    if constexpr (sizeof(ActT) == 2) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            wv[2 * i] = bf16lo(wu[i]);
+                            wv[2 * i + 1] = bf16hi(wu[i]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) wv[i] = __uint_as_float(wu[i]);
+                    }
+                } else {
                     const float *wr = a.wrt + static_cast<size_t>(e) * a.m + c;
 #pragma unroll
                     for (int i = 0; i < kVec; i += 4) {
-                        const float4 wv = __ldg(reinterpret_cast<const float4 *>(wr + i));
-                        acc[e] = fmaf(xv[i], wv.x, acc[e]);
-                        acc[e] = fmaf(xv[i + 1], wv.y, acc[e]);
-                        acc[e] = fmaf(xv[i + 2], wv.z, acc[e]);
-                        acc[e] = fmaf(xv[i + 3], wv.w, acc[e]);
+                        const float4 w4 = __ldg(reinterpret_cast<const float4 *>(wr + i));
+                        wv[i] = w4.x;
+                        wv[i + 1] = w4.y;
+                        wv[i + 2] = w4.z;
+                        wv[i + 3] = w4.w;
+                    }
+                }
+#pragma unroll
+                for (int tk = 0; tk < TOK; ++tk) {
+                    const uint32_t u[4] = {xraw[tk].x, xraw[tk].y, xraw[tk].z, xraw[tk].w};
+                    if constexpr (sizeof(ActT) == 2) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            acc[tk][e] = fmaf(bf16lo(u[i]), wv[2 * i], acc[tk][e]);
+                            acc[tk][e] = fmaf(bf16hi(u[i]), wv[2 * i + 1], acc[tk][e]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc[tk][e] = fmaf(__uint_as_float(u[i]), wv[i], acc[tk][e]);
                     }
                 }
             }
         }
+    }
+#pragma unroll
+    for (int tk = 0; tk < TOK; ++tk)
 #pragma unroll
         for (int e = 0; e < EMAX; ++e) {
-            const float v = warp_sum(acc[e]);
-            if (lane == 0 && e < a.E) s_part[tk][warp][e] = v;
+            const float v = warp_sum(acc[tk][e]);
+            if (lane == 0) s_part[warp][tk][e] = v;
         }
-    }
     __syncthreads();
     for (int i = tid; i < ntok * a.E; i += 256) {
         const int tk = i / a.E, e = i % a.E;
         float v = 0.0f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) v += s_part[tk][w][e];
+        for (int w = 0; w < 8; ++w) v += s_part[w][tk][e];
         if (a.bias) v += a.bias[e];
         s_logit[tk][e] = v;
         if (a.logits) a.logits[static_cast<size_t>(t0 + tk) * a.E + e] = v;
     }
     __syncthreads();
-    if (warp < ntok) {
-        const int t = t0 + warp;
+    for (int tk = warp; tk < ntok; tk += 8) {
+        const int t = t0 + tk;
         float l[EMAX];
 #pragma unroll
-        for (int e = 0; e < EMAX; ++e) l[e] = (e < a.E) ? s_logit[warp][e] : 0.0f;
+        for (int e = 0; e < EMAX; ++e) l[e] = (e < a.E) ? s_logit[tk][e] : 0.0f;
         int ids[kMaxTopK];
         float w[kMaxTopK];
         select_topk<EMAX>(l, a.E, a.k, ids, w);
@@ -140,6 +268,120 @@ __global__ void __launch_bounds__(256) router_topk_kernel(RouterArgs a) {
                 a.ids[static_cast<size_t>(t) * a.k + j] = ids[j];
                 a.w[static_cast<size_t>(t) * a.k + j] = w[j];
             }
+    }
+    // ---- the last CTA to finish permutes the whole batch
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned ticket = atomicAdd(a.ticket, 1u);
+        s_last = (ticket == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        permute_block(pa, psm);
+        if (tid == 0) *a.ticket = 0;  // ready for the next launch
+    }
+}
+
+// bf16 router on the warp-level tensor cores: logits[16 tokens x E] per CTA
+// as an m16n8k16 GEMM with the tokens on M and the experts on N (8 per MMA).
+// The warps of the CTA (32 for E <= 16) split the hidden dimension in
+// 32-element steps (4 per warp for m = 4096, loads issued together: the kernel
+// is a latency chain at decode sizes, so many warps with few steps each); lane (g, t) reads the
+// 16-byte run t of token rows g and g + 8 and of expert row g of the router
+// matrix (stored [EMAX x m], zero rows past E), which feed two MMAs under one
+// shared permutation of the reduction index.  The warp partials are added
+// in warp order (a fixed order), then each warp selects the top-k of its
+// tokens, and the launch's last CTA runs the permute.
+// Warps per CTA: 32 while the per-thread expert state is small; fewer for
+// wide routers (E > 16) so that 64 K registers cover the top-k state.
+template <int EMAX>
+constexpr int router_warps() { return EMAX <= 16 ? 32 : (EMAX == 32 ? 16 : 8); }
+
+template <int EMAX>
+__global__ void __launch_bounds__(router_warps<EMAX>() * 32) router_mma_kernel(RouterArgs a, PermuteArgs pa) {
+    constexpr int kRouterWarps = router_warps<EMAX>();
+    constexpr int NT = EMAX / 8;
+    constexpr int TOK = 16;
+    extern __shared__ __align__(16) float s_red[];  // [kRouterWarps][TOK][EMAX]
+    __shared__ float s_logit[TOK][EMAX];
+    __shared__ PermuteSmem psm;
+    __shared__ int s_last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int t0 = blockIdx.x * TOK;
+    const int ntok = min(TOK, a.T - t0);
+    const int nsteps = a.m / 32;
+    const int s0 = (nsteps * warp) / kRouterWarps, s1 = (nsteps * (warp + 1)) / kRouterWarps;
+    const uint16_t *x = static_cast<const uint16_t *>(a.x);
+    const uint16_t *w = static_cast<const uint16_t *>(a.wra);
+    const bool ra = g < ntok, rb = g + 8 < ntok;
+    const uint16_t *xa = x + static_cast<size_t>(t0 + (ra ? g : 0)) * a.m + 8 * t;
+    const uint16_t *xb = x + static_cast<size_t>(t0 + (rb ? g + 8 : 0)) * a.m + 8 * t;
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+#pragma unroll 4
+    for (int st = s0; st < s1; ++st) {
+        const int kb = st * 32;
+        const uint4 va = ra ? ld_nc_v4(xa + kb) : make_uint4(0, 0, 0, 0);
+        const uint4 vb = rb ? ld_nc_v4(xb + kb) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const uint4 wv = ld_nc_v4(w + static_cast<size_t>(nt * 8 + g) * a.m + kb + 8 * t);
+            mma_bf16_16816(acc[nt], va.x, vb.x, va.y, vb.y, wv.x, wv.y);
+            mma_bf16_16816(acc[nt], va.z, vb.z, va.w, vb.w, wv.z, wv.w);
+        }
+    }
+    // D fragment: acc[nt][0..1] = (token g, experts nt*8+2t, +1), [2..3] = token g + 8
+    float *red = s_red + static_cast<size_t>(warp) * TOK * EMAX;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int e = nt * 8 + 2 * t;
+        red[g * EMAX + e] = acc[nt][0];
+        red[g * EMAX + e + 1] = acc[nt][1];
+        red[(g + 8) * EMAX + e] = acc[nt][2];
+        red[(g + 8) * EMAX + e + 1] = acc[nt][3];
+    }
+    __syncthreads();
+    for (int i = tid; i < ntok * a.E; i += kRouterWarps * 32) {
+        const int tk = i / a.E, e = i % a.E;
+        float v = 0.0f;
+        for (int ww = 0; ww < kRouterWarps; ++ww) v += s_red[(ww * TOK + tk) * EMAX + e];
+        if (a.bias) v += a.bias[e];
+        s_logit[tk][e] = v;
+        if (a.logits) a.logits[static_cast<size_t>(t0 + tk) * a.E + e] = v;
+    }
+    __syncthreads();
+    for (int tk = warp; tk < ntok; tk += kRouterWarps) {
+        const int tok = t0 + tk;
+        float l[EMAX];
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) l[e] = (e < a.E) ? s_logit[tk][e] : 0.0f;
+        int ids[kMaxTopK];
+        float wts[kMaxTopK];
+        select_topk<EMAX>(l, a.E, a.k, ids, wts);
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+            if (j < a.k && lane == j) {
+                a.ids[static_cast<size_t>(tok) * a.k + j] = ids[j];
+                a.w[static_cast<size_t>(tok) * a.k + j] = wts[j];
+            }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned ticket = atomicAdd(a.ticket, 1u);
+        s_last = (ticket == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        permute_block(pa, psm);
+        if (tid == 0) *a.ticket = 0;  // ready for the next launch
     }
 }
 
@@ -187,100 +429,70 @@ __global__ void topk_copy_validate_kernel(const int32_t *ids_in, const float *w_
     if (bits) flag_error(err, bits);
 }
 
-// Histogram, exclusive scan and stable scatter in one CTA of 1024 threads.
-//   pass 1: counts[e] by shared-memory integer atomics (order-free);
-//   scan:   offsets by one warp;
-//   pass 2: chunks of 1024 flat indices in index order; inside a warp the
-//           rank of an index among equal ids is the popcount of the match
-//           mask below its lane; per-warp counts are scanned across warps per
-//           expert, so positions follow flat-index order exactly.
+// Standalone permute (after top-k from logits or from a given choice).
 __global__ void __launch_bounds__(1024) permute_kernel(PermuteArgs a) {
-    __shared__ int s_count[kMaxExperts];
-    __shared__ int s_base[kMaxExperts];
-    __shared__ int s_warp[32][kMaxExperts];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n = a.T * a.k;
-    if (tid < kMaxExperts) s_count[tid] = 0;
-    __syncthreads();
-    for (int i = tid; i < n; i += blockDim.x) {
-        int id = a.ids[i];
-        if (id < 0 || id >= a.E) id = 0;  // flagged by whoever produced ids
-        atomicAdd(&s_count[id], 1);
-    }
-    __syncthreads();
-    if (warp == 0) {
-        // exclusive scan over E <= 64 counts, two per lane
-        const int c0 = (2 * lane < a.E) ? s_count[2 * lane] : 0;
-        const int c1 = (2 * lane + 1 < a.E) ? s_count[2 * lane + 1] : 0;
-        int incl = c0 + c1;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        const int excl = incl - c0 - c1;
-        if (2 * lane < a.E) {
-            s_base[2 * lane] = excl;
-            a.counts[2 * lane] = c0;
-            a.offsets[2 * lane] = excl;
-        }
-        if (2 * lane + 1 < a.E) {
-            s_base[2 * lane + 1] = excl + c0;
-            a.counts[2 * lane + 1] = c1;
-            a.offsets[2 * lane + 1] = excl + c0;
-        }
-        if (lane == 31) a.offsets[a.E] = incl;
-    }
-    __syncthreads();
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int c0 = 0; c0 < n; c0 += blockDim.x) {
-        const int i = c0 + tid;
-        const bool valid = i < n;
-        int id = valid ? a.ids[i] : -1;
-        if (valid && (id < 0 || id >= a.E)) id = 0;
-        for (int e = lane; e < a.E; e += 32) s_warp[warp][e] = 0;
-        __syncwarp();
-        const unsigned peers = __match_any_sync(0xffffffffu, id);
-        const int rank = __popc(peers & lt_mask);
-        if (valid && lane == __ffs(peers) - 1) s_warp[warp][id] = __popc(peers);
-        __syncthreads();
-        if (tid < a.E) {
-            int run = s_base[tid];
-            for (int w = 0; w < 32; ++w) {
-                const int c = s_warp[w][tid];
-                s_warp[w][tid] = run;
-                run += c;
-            }
-            s_base[tid] = run;
-        }
-        __syncthreads();
-        if (valid) {
-            const int pos = s_warp[warp][id] + rank;
-            a.gather[pos] = i;
-            a.scatter[i] = pos;
-        }
-        __syncthreads();
-    }
+    __shared__ PermuteSmem psm;
+    permute_block(a, psm);
 }
 
 // ---- launchers ----------------------------------------------------------------
-template <typename ActT>
-static cudaError_t launch_router_t(const RouterArgs &a, cudaStream_t s) {
-    dim3 grid((a.T + kRouterTokens - 1) / kRouterTokens), block(256);
-    if (a.E <= 8)
-        router_topk_kernel<ActT, 8><<<grid, block, 0, s>>>(a);
-    else if (a.E <= 16)
-        router_topk_kernel<ActT, 16><<<grid, block, 0, s>>>(a);
-    else if (a.E <= 32)
-        router_topk_kernel<ActT, 32><<<grid, block, 0, s>>>(a);
-    else
-        router_topk_kernel<ActT, 64><<<grid, block, 0, s>>>(a);
+constexpr size_t kRouterSmemMax = 96 * 1024;
+
+template <typename ActT, int EMAX>
+static cudaError_t launch_router_e(const RouterArgs &a, const PermuteArgs &pa, cudaStream_t s) {
+    constexpr int TOK = (64 / EMAX) < 1 ? 1 : (64 / EMAX);
+    const unsigned grid = (a.T + TOK - 1) / TOK;
+    const size_t wbytes = static_cast<size_t>(a.E) * a.m * sizeof(ActT);
+    if (a.wra && wbytes <= kRouterSmemMax) {
+        auto kern = router_topk_kernel<ActT, EMAX, true>;
+        static size_t configured = 0;
+        if (wbytes > configured) {
+            const cudaError_t e = cudaFuncSetAttribute(
+                kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kRouterSmemMax));
+            if (e != cudaSuccess) return e;
+            configured = kRouterSmemMax;
+        }
+        kern<<<grid, 256, wbytes, s>>>(a, pa);
+    } else {
+        router_topk_kernel<ActT, EMAX, false><<<grid, 256, 0, s>>>(a, pa);
+    }
     return cudaGetLastError();
 }
 
-cudaError_t launch_router_topk(const RouterArgs &a, bool act_bf16, cudaStream_t s) {
+template <int EMAX>
+static cudaError_t launch_router_mma(const RouterArgs &a, const PermuteArgs &pa, cudaStream_t s) {
+    constexpr int kRouterWarps = router_warps<EMAX>();
+    const size_t smem = static_cast<size_t>(kRouterWarps) * 16 * EMAX * sizeof(float);
+    auto kern = router_mma_kernel<EMAX>;
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    kern<<<(a.T + 15) / 16, kRouterWarps * 32, smem, s>>>(a, pa);
+    return cudaGetLastError();
+}
+
+template <typename ActT>
+static cudaError_t launch_router_t(const RouterArgs &a, const PermuteArgs &pa, cudaStream_t s) {
+    if (sizeof(ActT) == 2 && a.wra && a.m % 32 == 0) {
+        if (a.E <= 8) return launch_router_mma<8>(a, pa, s);
+        if (a.E <= 16) return launch_router_mma<16>(a, pa, s);
+        if (a.E <= 32) return launch_router_mma<32>(a, pa, s);
+        return launch_router_mma<64>(a, pa, s);
+    }
+    if (a.E <= 8) return launch_router_e<ActT, 8>(a, pa, s);
+    if (a.E <= 16) return launch_router_e<ActT, 16>(a, pa, s);
+    if (a.E <= 32) return launch_router_e<ActT, 32>(a, pa, s);
+    return launch_router_e<ActT, 64>(a, pa, s);
+}
+
+cudaError_t launch_router_topk(const RouterArgs &a, const PermuteArgs &pa, bool act_bf16,
+                               cudaStream_t s) {
     if (a.T <= 0) return cudaSuccess;
-    return act_bf16 ? launch_router_t<__nv_bfloat16>(a, s) : launch_router_t<float>(a, s);
+    return act_bf16 ? launch_router_t<__nv_bfloat16>(a, pa, s) : launch_router_t<float>(a, pa, s);
 }
 
 cudaError_t launch_topk_from_logits(const float *logits, int T, int E, int k, int32_t *ids,
