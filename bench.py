@@ -232,16 +232,17 @@ def run_reference(args, world, rank):
 
 
 # ---- our arm ----------------------------------------------------------------------------
-def traffic_record(kernel_src):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current source of the kernel; else None."""
+def traffic_record():
+    """DRAM bytes of the up-projection per step from the committed ncu summary,
+    if every kernel source it was taken on is unchanged; else None."""
     path = os.path.join(ROOT, "profiles", "decode_up_traffic.json")
     if not os.path.exists(path):
         return None
     rec = json.load(open(path))
-    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
-    if rec.get("source_sha256") != sha:
-        return None
+    for rel, sha in rec.get("source_sha256", {}).items():
+        src = os.path.join(ROOT, rel)
+        if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != sha:
+            return None
     return rec
 
 
@@ -365,8 +366,8 @@ def run_ours(args, world, rank, local):
     # weight-streaming, tensor-bound once most of the work runs on the tensor-core path
     tensor_bound = sum(w["up_flops"] for w in work.values() if w["path"] == "tensor-core") > \
         0.5 * flops_up and max(TOKENS) >= 256
-    trec = traffic_record(os.path.join(ROOT, "mixture_experts_layer_gemm_gb300", "csrc",
-                                       "expert_decode.cu"))
+    trec = traffic_record() if (args.shape == "mixtral" and args.weights == "bf16"
+                                and TOKENS == (1, 4, 16, 64)) else None
     if tensor_bound:
         achieved = flops_up * args.steps / (up_ms * 1e-3) / 1e12
         roofline = {"kernel": "tc_up (tcgen05 grouped GEMM, W1 and W3 + SiLU*gate)",
