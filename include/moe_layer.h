@@ -270,11 +270,27 @@ moe_status_t moe_pool_geometry(size_t budget_bytes, size_t expert_bytes, int way
                                int *n_index, int *usable_slots);
 
 /* Create a pool for layers whose experts occupy expert_bytes each (see
- * moe_layer_info) on the current device.  page_bytes: copy granularity
- * (0 = 16 MiB). */
+ * moe_layer_info) on the current device: N * M slots of expert_bytes rounded
+ * up to 256 plus 768 bytes of alignment room, and a copy stream.
+ * page_bytes: granularity of the host-to-device copies (0 = 16 MiB; a
+ * multiple of 256).  Paged layers created with this pool keep their experts
+ * in pinned host memory; moe_forward on such a layer copies the routing
+ * counts to the host (synchronising the caller's stream once), brings the
+ * missing experts in on the copy stream, and runs each expert's kernels as
+ * soon as its copy has landed, so copies overlap compute.  A slot is never
+ * overwritten while a kernel may still read it.  Results are bit-identical
+ * to a resident layer's.  A pool may serve many layers (set = layer_id mod N)
+ * but one host thread at a time; destroy the layers before the pool. */
 moe_status_t moe_pool_create(size_t budget_bytes, size_t expert_bytes, int ways,
                              size_t page_bytes, moe_pool_t **out);
 moe_status_t moe_pool_destroy(moe_pool_t *pool);
+
+/* The pool's lookups since creation, oldest first (at most 2^20 kept): for
+ * query i, the layer id, the expert, whether it hit (1) or missed (0) and the
+ * slot (set * M + way) that served it.  Any output pointer may be NULL.
+ * *n_out receives the number written (<= max).  Host-only. */
+moe_status_t moe_pool_query_log(moe_pool_t *pool, int32_t *layer, int32_t *expert, int32_t *hit,
+                                int32_t *slot, int max, int *n_out);
 
 /* Status text, and the message of the last failure on this host thread. */
 const char *moe_status_string(moe_status_t s);

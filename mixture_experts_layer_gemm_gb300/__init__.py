@@ -97,6 +97,7 @@ _SIGNATURES = {
     "moe_pool_geometry": [_sz, _sz, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)],
     "moe_pool_create": [_sz, _sz, _i, _sz, ctypes.POINTER(_vp)],
     "moe_pool_destroy": [_vp],
+    "moe_pool_query_log": [_vp, _vp, _vp, _vp, _vp, _i, ctypes.POINTER(_i)],
     "moe_status_string": [_i],
     "moe_last_error": [],
     "moe_version": [],
@@ -256,6 +257,15 @@ def moe_pool_create(budget_bytes, expert_bytes, ways, page_bytes=0):
 
 def moe_pool_destroy(pool):
     _check(lib().moe_pool_destroy(pool))
+
+
+def moe_pool_query_log(pool, max_entries=1 << 20):
+    """(layer, expert, hit, slot) arrays of the pool's lookups so far."""
+    arrs = [np.empty(max_entries, np.int32) for _ in range(4)]
+    n = ctypes.c_int()
+    _check(lib().moe_pool_query_log(pool, *[a.ctypes.data for a in arrs], max_entries,
+                                    ctypes.byref(n)))
+    return tuple(a[:n.value].copy() for a in arrs)
 
 
 def moe_status_string(s) -> str:

@@ -41,6 +41,9 @@ struct moe_layer {
     // paged weights
     moe_pool_t *pool = nullptr;
     uint8_t *pinned_weights = nullptr;  // E experts x expert_stride, pinned host
+    int32_t *counts_host = nullptr;     // pinned copy of the routing counts
+    cudaEvent_t fwd_t0 = nullptr, fwd_t1 = nullptr;  // bracket a paged forward
+    bool fwd_pending = false;
 
     moe_stats_t stats{};
     // per-launch event timing (MOE_OPT_TIMING)

@@ -159,6 +159,9 @@ moe_layer::~moe_layer() {
     if (device >= 0) cudaSetDevice(device);
     for (void *p : allocations) cudaFree(p);
     if (pinned_weights) cudaFreeHost(pinned_weights);
+    if (counts_host) cudaFreeHost(counts_host);
+    if (fwd_t0) cudaEventDestroy(fwd_t0);
+    if (fwd_t1) cudaEventDestroy(fwd_t1);
     for (cudaEvent_t ev : event_pool) cudaEventDestroy(ev);
     for (auto &pe : pending) {
         cudaEventDestroy(pe.a);
@@ -754,6 +757,7 @@ extern "C" moe_status_t moe_layer_timings(moe_layer_t *L, moe_timings_t *out, in
         CUDA_TRY(cudaEventElapsedTime(&ms, pe.a, pe.b));
         L->phase_ms[pe.phase] += ms;
         L->phase_launches[pe.phase] += 1;
+        if (pe.phase == MOE_PHASE_COPY) L->stats.h2d_ms += ms;
         L->event_pool.push_back(pe.a);
         L->event_pool.push_back(pe.b);
     }
@@ -783,6 +787,14 @@ extern "C" moe_status_t moe_layer_info(const moe_layer_t *L, moe_layer_info_t *o
 
 extern "C" moe_status_t moe_layer_stats(moe_layer_t *L, moe_stats_t *out) {
     if (!L || !out) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    if (L->fwd_pending) {  // duration of the last paged forward
+        cudaSetDevice(L->device);
+        CUDA_TRY(cudaEventSynchronize(L->fwd_t1));
+        float ms = 0.0f;
+        CUDA_TRY(cudaEventElapsedTime(&ms, L->fwd_t0, L->fwd_t1));
+        L->stats.forward_ms += ms;
+        L->fwd_pending = false;
+    }
     *out = L->stats;
     return MOE_OK;
 }

@@ -1,14 +1,70 @@
-// paged.cu -- paged expert weights: a fixed GPU budget of expert slots,
-// arranged as N sets (indices) x M ways, shared by every layer of a model
+// paged.cu -- paged expert weights: a fixed GPU budget of expert slots shared
+// by every paged layer of a model, arranged as N sets (indices) x M ways
 // (expert-cache article, section 2.2: S = floor(available / expert size)
-// slots, N = floor(S / M) sets, layer l uses set l mod N, LRU inside a set).
+// slots, N = floor(S / M) sets, layer l uses set l mod N, least recently used
+// expert replaced inside a set).  Each paged layer keeps its experts (in the
+// stored, packed layout) in pinned host memory; a forward pass
+//   1. copies the per-expert token counts to the host (the one host
+//      synchronisation of the call),
+//   2. for each expert with tokens, in ascending id: looks it up in the set;
+//      on a miss, picks a free or the least recently used way, makes the copy
+//      stream wait until the compute that last read that slot has finished,
+//      and copies the expert there page by page (page_bytes per copy) on the
+//      copy stream (expert-cache article, section 3.2: weights move on a
+//      stream of their own);
+//   3. makes the compute stream wait for the expert's copy and runs the
+//      expert's kernels, then records that the slot is in use until they end.
+// So the copy of expert i+1 overlaps the compute of expert i (the expert
+// prefetch of the HARMOEny write-up, part 3.2).  The launch plan (token tiles,
+// reduction splits) is the one a resident layer uses for the same T, so a paged
+// layer's output is bit-identical to the resident layer's.
+#include <algorithm>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "../../include/moe_layer.h"
+#include "common.cuh"
 #include "kernels.cuh"
 #include "layer_impl.h"
 
 using namespace moe;
+
+namespace {
+constexpr size_t kLogCap = size_t(1) << 20;
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+}  // namespace
+
+struct moe_pool {
+    int device = -1;
+    size_t expert_bytes = 0, slot_bytes = 0, page_bytes = 0;
+    int n_index = 0, ways = 0, n_slots = 0;
+    uint8_t *slots = nullptr;
+    cudaStream_t copy_stream = nullptr;
+    struct Slot {
+        int layer = -1, expert = -1;
+        long long last_use = -1;
+        cudaEvent_t ready = nullptr;  // copy into the slot finished
+        cudaEvent_t busy = nullptr;   // last compute reading the slot finished
+        bool busy_recorded = false;
+    };
+    std::vector<Slot> slot;
+    long long clock = 0;
+    std::vector<int32_t> log;  // (layer, expert, hit, slot) per query
+    std::mutex mu;
+    ~moe_pool();
+};
+
+moe_pool::~moe_pool() {
+    if (device >= 0) cudaSetDevice(device);
+    if (copy_stream) cudaStreamSynchronize(copy_stream);
+    for (Slot &s : slot) {
+        if (s.ready) cudaEventDestroy(s.ready);
+        if (s.busy) cudaEventDestroy(s.busy);
+    }
+    if (slots) cudaFree(slots);
+    if (copy_stream) cudaStreamDestroy(copy_stream);
+}
 
 extern "C" moe_status_t moe_pool_geometry(size_t budget_bytes, size_t expert_bytes, int ways,
                                           int *n_index, int *usable_slots) {
@@ -25,32 +81,236 @@ extern "C" moe_status_t moe_pool_geometry(size_t budget_bytes, size_t expert_byt
 
 extern "C" moe_status_t moe_pool_create(size_t budget_bytes, size_t expert_bytes, int ways,
                                         size_t page_bytes, moe_pool_t **out) {
-    (void)budget_bytes;
-    (void)expert_bytes;
-    (void)ways;
-    (void)page_bytes;
-    if (out) *out = nullptr;
-    return fail(MOE_ERR_UNSUPPORTED, "paged pools are not built yet");
-}
-
-extern "C" moe_status_t moe_pool_destroy(moe_pool_t *pool) {
-    (void)pool;
+    if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    int n_index = 0, usable = 0;
+    moe_status_t st = moe_pool_geometry(budget_bytes, expert_bytes, ways, &n_index, &usable);
+    if (st != MOE_OK) return st;
+    if (page_bytes == 0) page_bytes = size_t(16) << 20;
+    if (page_bytes % 256) return fail(MOE_ERR_INVALID_ARG, "page_bytes must be a multiple of 256");
+    moe_pool *P = new (std::nothrow) moe_pool();
+    if (!P) return fail(MOE_ERR_OOM, "host allocation failed");
+    P->expert_bytes = expert_bytes;
+    // a layer stores an expert as up to three 256-byte aligned parts
+    P->slot_bytes = round256(expert_bytes) + 768;
+    P->page_bytes = page_bytes;
+    P->n_index = n_index;
+    P->ways = ways;
+    P->n_slots = usable;
+    cudaError_t e = cudaGetDevice(&P->device);
+    if (e == cudaSuccess) e = cudaMalloc(&P->slots, P->slot_bytes * static_cast<size_t>(usable));
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&P->copy_stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess) {
+        P->slot.resize(static_cast<size_t>(usable));
+        for (auto &s : P->slot) {
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.ready, cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.busy, cudaEventDisableTiming);
+        }
+    }
+    if (e != cudaSuccess) {
+        delete P;
+        return cuda_fail(e, "moe_pool_create");
+    }
+    *out = P;
     return MOE_OK;
 }
 
-moe_status_t paged_attach(moe_layer *L) {
-    (void)L;
-    return fail(MOE_ERR_UNSUPPORTED, "paged layers are not built yet");
+extern "C" moe_status_t moe_pool_destroy(moe_pool_t *pool) {
+    delete pool;
+    return MOE_OK;
 }
 
-void paged_detach(moe_layer *L) { (void)L; }
+extern "C" moe_status_t moe_pool_query_log(moe_pool_t *pool, int32_t *layer, int32_t *expert,
+                                           int32_t *hit, int32_t *slot, int max, int *n_out) {
+    if (!pool || !n_out || max < 0) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    std::lock_guard<std::mutex> lock(pool->mu);
+    const int n = static_cast<int>(std::min<size_t>(pool->log.size() / 4, static_cast<size_t>(max)));
+    for (int i = 0; i < n; ++i) {
+        if (layer) layer[i] = pool->log[4 * i];
+        if (expert) expert[i] = pool->log[4 * i + 1];
+        if (hit) hit[i] = pool->log[4 * i + 2];
+        if (slot) slot[i] = pool->log[4 * i + 3];
+    }
+    *n_out = n;
+    return MOE_OK;
+}
+
+// ---- layer attach / detach -----------------------------------------------------------
+moe_status_t paged_attach(moe_layer *L) {
+    moe_pool *P = L->pool;
+    if (L->expert_stride > P->slot_bytes)
+        return fail(MOE_ERR_INVALID_ARG,
+                    "pool slots hold %zu bytes but this layer stores %zu bytes per expert "
+                    "(create the pool with moe_layer_info().expert_bytes)",
+                    P->slot_bytes, L->expert_stride);
+    if (P->device != L->device) return fail(MOE_ERR_INVALID_ARG, "pool and layer on different devices");
+    const size_t bytes = L->expert_stride * static_cast<size_t>(L->cfg.E);
+    void *host = nullptr;
+    cudaError_t e = cudaHostAlloc(&host, bytes, cudaHostAllocDefault);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc(paged weights)");
+    L->pinned_weights = static_cast<uint8_t *>(host);
+    e = cudaMemcpy(L->pinned_weights, L->weights, bytes, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(paged weights)");
+    // the device copy made during ingestion is no longer needed
+    for (size_t i = 0; i < L->allocations.size(); ++i)
+        if (L->allocations[i] == L->weights) {
+            cudaFree(L->weights);
+            L->allocations.erase(L->allocations.begin() + static_cast<long>(i));
+            break;
+        }
+    L->weights = nullptr;
+    return MOE_OK;
+}
+
+void paged_detach(moe_layer *L) {
+    moe_pool *P = L->pool;
+    if (!P) return;
+    std::lock_guard<std::mutex> lock(P->mu);
+    cudaStreamSynchronize(P->copy_stream);
+    for (auto &s : P->slot)
+        if (s.layer == L->layer_id) {
+            s.layer = -1;
+            s.expert = -1;
+            s.last_use = -1;
+        }
+}
+
+// ---- forward ---------------------------------------------------------------------------
+namespace {
+
+// Set-associative lookup; on a miss the chosen way is re-tagged.  Returns the
+// slot index; *hit tells whether the expert was resident.
+int pool_acquire(moe_pool *P, int layer, int expert, bool *hit) {
+    const int set = layer % P->n_index;
+    const int base = set * P->ways;
+    int found = -1;
+    for (int w = 0; w < P->ways; ++w)
+        if (P->slot[base + w].layer == layer && P->slot[base + w].expert == expert) found = w;
+    *hit = found >= 0;
+    if (found < 0) {
+        int victim = -1;
+        for (int w = 0; w < P->ways && victim < 0; ++w)
+            if (P->slot[base + w].layer < 0) victim = w;
+        if (victim < 0) {
+            victim = 0;
+            for (int w = 1; w < P->ways; ++w)
+                if (P->slot[base + w].last_use < P->slot[base + victim].last_use) victim = w;
+        }
+        P->slot[base + victim].layer = layer;
+        P->slot[base + victim].expert = expert;
+        found = victim;
+    }
+    P->slot[base + found].last_use = P->clock++;
+    if (P->log.size() + 4 <= 4 * kLogCap) {
+        P->log.push_back(layer);
+        P->log.push_back(expert);
+        P->log.push_back(*hit ? 1 : 0);
+        P->log.push_back(base + found);
+    }
+    return base + found;
+}
+
+}  // namespace
+
+#define PG_TRY(expr)                                        \
+    do {                                                    \
+        cudaError_t e_ = (expr);                            \
+        if (e_ != cudaSuccess) return cuda_fail(e_, #expr); \
+    } while (0)
 
 moe_status_t paged_forward(moe_layer *L, const void *x, const moe_routing_t *r, void *y,
                            cudaStream_t s) {
-    (void)L;
-    (void)x;
-    (void)r;
-    (void)y;
-    (void)s;
-    return fail(MOE_ERR_UNSUPPORTED, "paged layers are not built yet");
+    moe_pool *P = L->pool;
+    const moe_config_t &c = L->cfg;
+    std::lock_guard<std::mutex> lock(P->mu);
+    if (!L->counts_host) {
+        PG_TRY(cudaHostAlloc(reinterpret_cast<void **>(&L->counts_host), sizeof(int32_t) * c.E,
+                             cudaHostAllocDefault));
+        PG_TRY(cudaEventCreate(&L->fwd_t0));
+        PG_TRY(cudaEventCreate(&L->fwd_t1));
+    }
+    // 1. token counts to the host: the one synchronisation of a paged call
+    if (L->fwd_pending) {  // the previous call's duration (its events are done after the sync)
+        PG_TRY(cudaEventSynchronize(L->fwd_t1));
+        float ms = 0.0f;
+        PG_TRY(cudaEventElapsedTime(&ms, L->fwd_t0, L->fwd_t1));
+        L->stats.forward_ms += ms;
+        L->fwd_pending = false;
+    }
+    PG_TRY(cudaEventRecord(L->fwd_t0, s));
+    PG_TRY(cudaMemcpyAsync(L->counts_host, r->counts, sizeof(int32_t) * c.E, cudaMemcpyDeviceToHost, s));
+    PG_TRY(cudaStreamSynchronize(s));
+
+    // the launch plan of a resident layer for the same T (bit-identical results)
+    ExpertArgs a = make_expert_args(L, x, r);
+    int splits = 1, nrows_cap = 0;
+    moe_status_t st = MOE_OK;
+    bool first = true;
+    for (int e = 0; e < c.E; ++e) {
+        if (L->counts_host[e] <= 0) continue;
+        bool hit = false;
+        const int si = pool_acquire(P, L->layer_id, e, &hit);
+        moe_pool::Slot &slot = P->slot[si];
+        uint8_t *dst = P->slots + static_cast<size_t>(si) * P->slot_bytes;
+        if (!hit) {
+            // never overwrite weights a kernel may still be reading
+            if (slot.busy_recorded) PG_TRY(cudaStreamWaitEvent(P->copy_stream, slot.busy, 0));
+            cudaEvent_t c0 = L->timing ? L->get_event() : nullptr;
+            if (c0) PG_TRY(cudaEventRecord(c0, P->copy_stream));
+            const uint8_t *src = L->pinned_weights + L->expert_stride * static_cast<size_t>(e);
+            for (size_t off = 0; off < L->expert_stride; off += P->page_bytes) {
+                const size_t n = std::min(P->page_bytes, L->expert_stride - off);
+                PG_TRY(cudaMemcpyAsync(dst + off, src + off, n, cudaMemcpyHostToDevice, P->copy_stream));
+            }
+            PG_TRY(cudaEventRecord(slot.ready, P->copy_stream));
+            if (c0) {
+                cudaEvent_t c1 = L->get_event();
+                if (c1) {
+                    PG_TRY(cudaEventRecord(c1, P->copy_stream));
+                    L->pending.push_back({MOE_PHASE_COPY, c0, c1});
+                }
+            }
+            L->stats.slot_misses += 1;
+            L->stats.h2d_bytes += L->expert_stride;
+        } else {
+            L->stats.slot_hits += 1;
+        }
+        PG_TRY(cudaStreamWaitEvent(s, slot.ready, 0));
+        // this expert's stored matrices now live in the slot
+        const size_t mp = static_cast<size_t>(c.m) * c.p;
+        const bool gated = c.expert == MOE_EXPERT_SWIGLU;
+        const bool i8 = c.weight_dtype == MOE_I8;
+        const size_t wel = i8 ? 1 : 2;
+        const size_t u_bytes = round256((gated ? 2 : 1) * mp * wel), d_bytes = round256(mp * wel);
+        L->tab.w1[e] = dst;
+        L->tab.w2[e] = dst + u_bytes;
+        if (i8) {
+            float *sc = reinterpret_cast<float *>(dst + u_bytes + d_bytes);
+            L->tab.s1[e] = sc;
+            L->tab.s3[e] = gated ? sc + c.p : nullptr;
+            L->tab.s2[e] = sc + static_cast<size_t>(c.p) * (gated ? 2 : 1);
+        }
+        a.only[0] = e;
+        a.n_only = 1;
+        a.tab = &L->tab;
+        int sp = 1;
+        st = run_experts(L, a, L->regime, &sp, s);
+        if (st != MOE_OK) return st;
+        if (first) {
+            splits = sp;
+            nrows_cap = a.n_rows_cap;
+            first = false;
+        }
+        PG_TRY(cudaEventRecord(slot.busy, s));
+        slot.busy_recorded = true;
+    }
+    if (!first) {
+        st = run_combine(L, r, splits, nrows_cap, y, s);
+        if (st != MOE_OK) return st;
+    }
+    PG_TRY(cudaEventRecord(L->fwd_t1, s));
+    PG_TRY(cudaEventRecord(L->done, s));
+    L->fwd_pending = true;
+    L->stats.forwards += 1;
+    return MOE_OK;
 }

@@ -1,0 +1,117 @@
+"""Paged expert weights (expert-cache article, sections 2.2 and 3.2): experts in
+pinned host memory, brought into an N-index x M-way set-associative GPU slot
+pool on a copy stream.  Checked against (a) resident layers with the same
+weights -- outputs must be bit-identical -- and (b) the oracle's replay of the
+same lookups through an LRU set-associative cache -- hits and slots must match
+exactly."""
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_layer_gemm_gb300 as moe
+import oracle
+import workloads as wl
+from gpu_util import Run, to_device
+
+pytestmark = pytest.mark.gpu
+
+SHAPE = wl.LayerShape("paged-swiglu", m=512, p=1024, E=8, k=2, expert=wl.SWIGLU, act="bf16",
+                      weight="bf16")
+
+
+def _expert_bytes(shape):
+    probe = moe.MoELayer(wl.make_layer(shape, seed=99), 4)
+    nbytes = probe.info().expert_bytes
+    probe.close()
+    return nbytes
+
+
+def _run_pair(shape, n_layers, sets, ways, schedule, page_bytes=0, regime=moe.REGIME_AUTO,
+              topk_trace=None):
+    eb = _expert_bytes(shape)
+    pool = moe.moe_pool_create(eb * sets * ways, eb, ways, page_bytes)
+    layers = [wl.make_layer(shape, seed=200 + i) for i in range(n_layers)]
+    max_t = max(T for _, T in schedule)
+    paged = [moe.MoELayer(layers[i], max_t, pool=pool, layer_id=i) for i in range(n_layers)]
+    resident = [moe.MoELayer(layers[i], max_t) for i in range(n_layers)]
+    for ml in paged + resident:
+        ml.set_regime(regime)
+    queries = []
+    for step, (li, T) in enumerate(schedule):
+        x = wl.make_tokens(shape, T, seed=300 + step)
+        if topk_trace is None:
+            rp, rr = Run(paged[li], x), Run(resident[li], x)
+        else:
+            ids, w = topk_trace[step]
+            rp = Run(paged[li], x, routing="topk", ids=ids, w=w)
+            rr = Run(resident[li], x, routing="topk", ids=ids, w=w)
+        np.testing.assert_array_equal(rp.y_np, rr.y_np)
+        assert paged[li].sync_check()[0] == moe.MOE_OK
+        queries += [(li, e) for e in range(shape.E) if rp.counts[e] > 0]
+    log = moe.moe_pool_query_log(pool)
+    stats = [ml.stats() for ml in paged]
+    for ml in paged + resident:
+        ml.close()
+    moe.moe_pool_destroy(pool)
+    return eb, queries, log, stats
+
+
+def _check_log(queries, log, sets, ways):
+    layers = np.array([q[0] for q in queries], np.int32)
+    experts = np.array([q[1] for q in queries], np.int32)
+    hit, slot = oracle.cache_replay(sets, ways, layers, experts)
+    np.testing.assert_array_equal(log[0], layers)
+    np.testing.assert_array_equal(log[1], experts)
+    np.testing.assert_array_equal(log[2], hit)
+    np.testing.assert_array_equal(log[3], slot)
+    return hit
+
+
+def test_paged_equals_resident_and_lru_replay():
+    sets, ways = 2, 2
+    schedule = [(0, 16), (1, 3), (2, 16), (0, 5), (1, 16), (2, 1), (0, 16), (1, 2)]
+    eb, queries, log, stats = _run_pair(SHAPE, 3, sets, ways, schedule)
+    hit = _check_log(queries, log, sets, ways)
+    misses = sum(int(s.slot_misses) for s in stats)
+    assert misses == int((hit == 0).sum())
+    assert sum(int(s.slot_hits) for s in stats) == int(hit.sum())
+    h2d = sum(int(s.h2d_bytes) for s in stats)
+    assert misses * eb <= h2d <= misses * (eb + 768)
+
+
+def test_paged_with_small_pages_and_reuse():
+    """One set, 4 ways, a layer revisited with few experts: hits happen and
+    16 KB pages split every expert into many copies."""
+    sets, ways = 1, 4
+    T = 2
+    trace = []
+    for step in range(6):
+        ids = np.array([[0, 1], [1, 2]], np.int32) if step % 2 == 0 else np.array([[2, 0], [0, 1]], np.int32)
+        trace.append((ids, np.full((T, 2), 0.5, np.float32)))
+    schedule = [(0, T)] * 6
+    eb, queries, log, stats = _run_pair(SHAPE, 1, sets, ways, schedule, page_bytes=16384,
+                                        topk_trace=trace)
+    hit = _check_log(queries, log, sets, ways)
+    assert hit.sum() > 0 and int(stats[0].slot_hits) == int(hit.sum())
+
+
+def test_paged_int8():
+    shape = SHAPE.with_weight("i8")
+    schedule = [(0, 16), (1, 16), (0, 4), (1, 1)]
+    _, queries, log, _ = _run_pair(shape, 2, 1, 2, schedule)
+    _check_log(queries, log, 1, 2)
+
+
+def test_paged_tensor_core_path():
+    schedule = [(0, 200), (1, 64), (0, 100)]
+    _, queries, log, _ = _run_pair(SHAPE, 2, 2, 2, schedule, regime=moe.REGIME_BATCH)
+    _check_log(queries, log, 2, 2)
+
+
+def test_pool_too_small_for_layer_is_rejected():
+    eb = _expert_bytes(SHAPE)
+    pool = moe.moe_pool_create(eb, eb // 2, 1, 0)  # slots of half an expert
+    with pytest.raises(moe.MoeError) as ei:
+        moe.MoELayer(wl.make_layer(SHAPE, seed=5), 4, pool=pool, layer_id=0)
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+    moe.moe_pool_destroy(pool)
