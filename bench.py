@@ -47,6 +47,14 @@ def parse():
     ap.add_argument("--tokens", default="1,4,16,64",
                     help="decode batches per step (profiling runs use one)")
     ap.add_argument("--copies", type=int, default=2, help="weight copies that alternate")
+    ap.add_argument("--paged", action="store_true",
+                    help="paged-weights run: many Mixtral-shaped layers in pinned host memory, "
+                         "a capped GPU slot pool, a seeded decode routing trace")
+    ap.add_argument("--paged-layers", type=int, default=32)
+    ap.add_argument("--paged-steps", type=int, default=32)
+    ap.add_argument("--paged-tokens", type=int, default=16, help="decode batch per layer")
+    ap.add_argument("--paged-budget-gib", type=float, default=16.0)
+    ap.add_argument("--paged-ways", type=int, default=4)
     ap.add_argument("--zipf", type=float, default=None,
                     help="router bias making expert popularity Zipf(s) (batch workloads)")
     ap.add_argument("--shape", default="mixtral", choices=["mixtral", "phi", "small"],
@@ -451,11 +459,133 @@ def run_ours(args, world, rank, local):
         c.close()
 
 
+
+# ---- paged weights (expert-cache configuration) -----------------------------------------
+def host_mem_available():
+    for line in open("/proc/meminfo"):
+        if line.startswith("MemAvailable:"):
+            return int(line.split()[1]) * 1024
+    return 0
+
+
+def link_h2d_gbs(torch, nbytes=1 << 30):
+    """Pinned host-to-device copy bandwidth of this machine (cudaMemcpyAsync)."""
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            d.copy_(h, non_blocking=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(5):
+            d.copy_(h, non_blocking=True)
+        e1.record(s)
+    torch.cuda.synchronize()
+    gbs = 5 * nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del h, d
+    return gbs
+
+
+def run_paged(args, world, rank, local):
+    """Decode T=16 through many paged Mixtral-shaped layers sharing a slot pool
+    (N-index x M-way, set = layer mod N), fed a seeded routing trace in which a
+    layer repeats the previous layer's experts with p = 0.44 and the previous
+    token's with p = 0.5 (expert-cache article, section 2.1)."""
+    import numpy as np
+    import torch
+
+    import mixture_experts_layer_gemm_gb300 as moe
+    import workloads as wl
+    from mixture_experts_layer_gemm_gb300 import build as lib_build
+
+    lib_build.build()
+    shape = wl.MIXTRAL if args.weights == "bf16" else wl.MIXTRAL.with_weight("i8")
+    T, L, S = args.paged_tokens, args.paged_layers, args.paged_steps
+    layer = wl.make_layer(shape, seed=args.seed + rank, device=f"cuda:{local}")
+    probe = moe.MoELayer(layer, T)
+    eb = probe.info().expert_bytes
+    probe.close()
+    need = int(1.15 * L * shape.E * (eb + 1024)) + (8 << 30)
+    avail = host_mem_available()
+    if avail < need:
+        raise SystemExit(f"paged run needs ~{need / 1e9:.0f} GB of host memory, "
+                         f"{avail / 1e9:.0f} GB available")
+    link = link_h2d_gbs(torch)
+    budget = int(args.paged_budget_gib * (1 << 30))
+    n_index, n_slots = moe.moe_pool_geometry(budget, eb, args.paged_ways)
+    pool = moe.moe_pool_create(budget, eb, args.paged_ways, 0)
+    layers = [moe.MoELayer(layer, T, pool=pool, layer_id=l) for l in range(L)]
+    ids, w = wl.make_topk_trace(shape.E, shape.k, S + 1, L, T, seed=args.seed)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(args.seed + 17)
+    ids_d = torch.from_numpy(ids.reshape(S + 1, L, T * shape.k)).to(dev)
+    w_d = torch.from_numpy(w.reshape(S + 1, L, T * shape.k)).to(dev)
+    y = torch.empty((T, shape.m), dtype=torch.bfloat16, device=dev)
+    # fresh N(0,1) token rows per (step, layer), drawn before the timed region
+    xs = torch.randn((S + 1, L, T, shape.m), generator=gen, device=dev).to(torch.bfloat16)
+
+    def step(s):
+        for l, ml in enumerate(layers):
+            ml.route_from_topk(ids_d[s, l], w_d[s, l], T=T, stream=stream)
+            ml.forward(xs[s, l], y, stream=stream)
+
+    step(0)  # warm-up: kernels, tensor maps, first slot fills
+    torch.cuda.synchronize()
+    for ml in layers:
+        ml.set_timing(True)
+        ml.timings(reset=True)
+    st0 = [ml.stats() for ml in layers]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s_ in range(1, S + 1):
+        step(s_)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall_ms = e0.elapsed_time(e1)
+    st1 = [ml.stats() for ml in layers]
+    tim = [ml.timings(reset=True) for ml in layers]
+    hits = sum(b.slot_hits - a.slot_hits for a, b in zip(st0, st1))
+    misses = sum(b.slot_misses - a.slot_misses for a, b in zip(st0, st1))
+    h2d = sum(b.h2d_bytes - a.h2d_bytes for a, b in zip(st0, st1))
+    copy_ms = sum(t["copy"][0] for t in tim)
+    compute_ms = sum(sum(v[0] for k, v in t.items() if k != "copy") for t in tim)
+    overlap = (copy_ms + compute_ms - wall_ms) / max(min(copy_ms, compute_ms), 1e-9)
+    for ml in layers:
+        ml.close()
+    moe.moe_pool_destroy(pool)
+    value = S * T / (wall_ms * 1e-3)
+    line = {"metric": f"MoE-layer tokens/s, paged expert weights (decode, T={T} per layer)",
+            "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": S, "warmup": 1,
+            "ms_per_step": wall_ms / S, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": args.weights, "data": "synthetic",
+            "config": {"workload": f"{L} paged mixtral-8x7b moe layers, decode T={T}, "
+                                   f"{args.paged_budget_gib:g} GiB slot pool, "
+                                   f"{n_index} sets x {args.paged_ways} ways",
+                       "layers": L, "T": T, "trace": "p_layer=0.44, p_token=0.5, seeded",
+                       "tokens_per_step": T},
+            "paged": {"sets": n_index, "ways": args.paged_ways, "slots": n_slots,
+                      "expert_bytes": eb, "hit_rate": hits / max(hits + misses, 1),
+                      "hits": hits, "misses": misses, "h2d_bytes": h2d,
+                      "h2d_gbs_copy_stream": h2d / max(copy_ms * 1e-3, 1e-12) / 1e9,
+                      "h2d_gbs_wall": h2d / (wall_ms * 1e-3) / 1e9,
+                      "link_gbs_measured": link,
+                      "link_frac": (h2d / max(copy_ms * 1e-3, 1e-12) / 1e9) / link,
+                      "copy_ms": copy_ms, "compute_ms": compute_ms, "wall_ms": wall_ms,
+                      "overlap_frac": max(0.0, min(1.0, overlap)),
+                      "bounds_ms": [max(copy_ms, compute_ms), copy_ms + compute_ms]}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.paged:
+        run_paged(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

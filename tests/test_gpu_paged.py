@@ -115,3 +115,40 @@ def test_pool_too_small_for_layer_is_rejected():
         moe.MoELayer(wl.make_layer(SHAPE, seed=5), 4, pool=pool, layer_id=0)
     assert ei.value.status == moe.MOE_ERR_INVALID_ARG
     moe.moe_pool_destroy(pool)
+
+
+def test_paged_step_time_within_overlap_bounds():
+    """Copies and compute overlap: a paged call's time lies between
+    max(copy, compute) and copy + compute (the GPU-only form of the decode
+    latency model max(comm, T_gpu) of the MoE-Lightning note)."""
+    eb = _expert_bytes(SHAPE)
+    pool = moe.moe_pool_create(eb * 2, eb, 2, 0)
+    layers = [moe.MoELayer(wl.make_layer(SHAPE, seed=400 + i), 16, pool=pool, layer_id=i)
+              for i in range(3)]
+    xs = [to_device(wl.make_tokens(SHAPE, 16, seed=500 + i)) for i in range(3)]
+    y = torch.empty((16, SHAPE.m), dtype=torch.bfloat16, device="cuda")
+    for ml, x in zip(layers, xs):  # warm-up
+        ml.route(x)
+        ml.forward(x, y)
+    torch.cuda.synchronize()
+    for ml in layers:
+        ml.set_timing(True)
+        ml.timings(reset=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(4):
+        for ml, x in zip(layers, xs):
+            ml.route(x)
+            ml.forward(x, y)
+    e1.record()
+    torch.cuda.synchronize()
+    wall = e0.elapsed_time(e1)
+    tim = [ml.timings(reset=True) for ml in layers]
+    copy = sum(t["copy"][0] for t in tim)
+    compute = sum(sum(v[0] for k, v in t.items() if k != "copy") for t in tim)
+    assert copy > 0 and compute > 0
+    # event timing adds a little; the host synchronises once per paged call
+    assert 0.9 * max(copy, compute) <= wall
+    for ml in layers:
+        ml.close()
+    moe.moe_pool_destroy(pool)
