@@ -198,6 +198,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(buf * geo.N);
+                // the last token tile of an expert may be partly empty: issue the
+                // MMAs with N rounded up to the 16 tokens that hold data
+                const int n_valid = min(geo.N, (t.q - t.tt * geo.N + 15) / 16 * 16);
+                const uint32_t idesc = idesc_bf16_f32(128, n_valid);
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
                     if (!mbar_wait(&full_bar[stage], phase)) {
                         flag_error(a.err, kErrWaitTimeout);
@@ -212,7 +216,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const uint64_t ad = smem_desc(abase + (kk >> 1) * 512 + (kk & 1) * 32, 16, 1024,
                                                       kLayoutSw64);
                         const uint64_t bd = smem_desc(bbase + kk * 32, 16, 1024, kLayoutSw128);
-                        tc_mma(d, ad, bd, geo.idesc, (kb > t.kb0 || kk > 0) ? 1u : 0u);
+                        tc_mma(d, ad, bd, idesc, (kb > t.kb0 || kk > 0) ? 1u : 0u);
                     }
                     tc_commit(&empty_bar[stage]);  // slot free once these MMAs have read it
                     if (++stage == geo.stages) {
@@ -244,7 +248,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_after();
             const int R = t.rb * 128 + row_in_tile;  // stored weight row of this thread
             const int tok0 = t.tt * geo.N;
-            for (int c0 = 0; c0 < geo.N; c0 += 16) {
+            const int n_valid = min(geo.N, (t.q - tok0 + 15) / 16 * 16);
+            for (int c0 = 0; c0 < n_valid; c0 += 16) {
                 uint32_t v[16];
                 tmem_ld16(tmem_base + (static_cast<uint32_t>(lq * 32) << 16) +
                               static_cast<uint32_t>(buf * geo.N + c0),
