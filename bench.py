@@ -128,15 +128,21 @@ def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    gpu = args.impl == "ours" and torch.cuda.is_available()
     if world > 1:
         import torch.distributed as dist
-        backend = "nccl" if args.impl == "ours" else "gloo"
-        if args.impl == "ours":
+        if gpu:
             torch.cuda.set_device(local)
-        dist.init_process_group(backend=backend)
-    elif args.impl == "ours":
+        dist.init_process_group(backend="nccl" if gpu else "gloo")
+    elif gpu:
         torch.cuda.set_device(0)
     return world, rank, local
+
+
+def job_value(world, tokens_per_step, steps, ms_max):
+    """Whole-job tokens/s of `world` replicas that each ran `steps` steps of
+    `tokens_per_step` tokens, timed by the slowest rank (ms_max)."""
+    return world * tokens_per_step * steps / (ms_max * 1e-3)
 
 
 def barrier(world):
@@ -424,8 +430,8 @@ def run_ours(args, world, rank, local):
     io_bytes = sum(T * shape.m * 2 for T in TOKENS)
 
     tokens_step = sum(TOKENS)
-    value = world * tokens_step * args.steps / (ms_max * 1e-3)
-    e2e_value = world * tokens_step * k_e2e / (e2e_ms * 1e-3) if e2e_ms else None
+    value = job_value(world, tokens_step, args.steps, ms_max)
+    e2e_value = job_value(world, tokens_step, k_e2e, e2e_ms) if e2e_ms else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
