@@ -15,6 +15,8 @@ namespace {
 
 template <bool BF16>
 __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
+    pdl_wait();
+    pdl_trigger();
     const int vec = a.m / 4;  // 4 fp32 per thread
     const long long n = static_cast<long long>(a.T) * vec;
     const int rows = a.T * a.k;
@@ -77,10 +79,9 @@ cudaError_t launch_combine(const CombineArgs &a, bool act_bf16, cudaStream_t s) 
     long long blocks = (n + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (act_bf16)
-        combine_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+        return launch_pdl(combine_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, a);
     else
-        combine_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, a);
 }
 
 }  // namespace moe

@@ -157,6 +157,18 @@ __device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gsrc, uint3
         : "memory");
 }
 
+// ---- programmatic dependent launch -----------------------------------------------
+// Kernels on the forward path are launched so that each may start while its
+// predecessor in the stream finishes.  Protocol: a kernel calls pdl_wait()
+// before it reads anything its predecessor writes or writes anything its
+// predecessor reads, and calls pdl_trigger() only after that wait.  Then a
+// kernel can overlap only its immediate predecessor, and everything issued
+// two kernels back has completed when it starts.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Named barrier over a subset of the CTA's warps.
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

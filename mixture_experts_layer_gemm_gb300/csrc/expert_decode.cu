@@ -122,6 +122,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rows_total = a.T * a.k;
+    // The up projection reads the routing its predecessor (the router) wrote.
+    // The down projection's predecessor is the up projection: the routing is
+    // two launches back and complete, so the weight stream starts at once and
+    // only the consumers wait, before they read the hidden rows.
+    if (PHASE == kUp) {
+        pdl_wait();
+        pdl_trigger();
+    }
 
     if (tid == 0) {
         int n = 0;
@@ -186,6 +194,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
     // ================= consumers: warp w owns row-group 8*g8 + w of each unit ======
+    if (PHASE == kDown) {
+        pdl_wait();
+        pdl_trigger();
+    }
     const int g = lane >> 2, t = lane & 3;
     int stage = 0;
     uint32_t phase = 0;
@@ -366,6 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // h = act(sum_s gate_part[s]) [* sum_s up_part[s]] for split-K up projections.
 template <bool GATED>
 __global__ void up_finish_kernel(const ExpertArgs a, int splits) {
+    pdl_wait();
+    pdl_trigger();
     const size_t rows = static_cast<size_t>(a.T) * a.k;
     const size_t n = rows * a.p;
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
@@ -410,8 +424,7 @@ cudaError_t launch_one(const ExpertArgs &a, int K, int rows, int splits, int num
         if (err != cudaSuccess) return err;
         configured_smem = static_cast<int>(smem);
     }
-    kern<<<num_sms, kThreads, smem, s>>>(*a.tab, a, geo);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(num_sms), dim3(kThreads), smem, s, *a.tab, a, geo);
 }
 
 template <WeightType WT, int PHASE, bool GATED>
@@ -459,10 +472,9 @@ cudaError_t launch_decode_up_finish(const ExpertArgs &a, bool gated, int splits,
     if (n == 0) return cudaSuccess;
     const int blocks = static_cast<int>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
     if (gated)
-        up_finish_kernel<true><<<blocks, 256, 0, s>>>(a, splits);
+        return launch_pdl(up_finish_kernel<true>, dim3(blocks), dim3(256), 0, s, a, splits);
     else
-        up_finish_kernel<false><<<blocks, 256, 0, s>>>(a, splits);
-    return cudaGetLastError();
+        return launch_pdl(up_finish_kernel<false>, dim3(blocks), dim3(256), 0, s, a, splits);
 }
 
 }  // namespace moe

@@ -19,6 +19,8 @@ __device__ __forceinline__ int expert_of(const int32_t *offsets, int E, int pos)
 
 template <bool GATED>
 __global__ void __launch_bounds__(256) simt_up_kernel(const ExpertTables tab, const ExpertArgs a) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const long long wid = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
     const int rows = a.T * a.k;
@@ -49,6 +51,8 @@ __global__ void __launch_bounds__(256) simt_up_kernel(const ExpertTables tab, co
 }
 
 __global__ void __launch_bounds__(256) simt_down_kernel(const ExpertTables tab, const ExpertArgs a) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const long long wid = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
     const int rows = a.T * a.k;
@@ -75,18 +79,16 @@ cudaError_t launch_simt_up(const ExpertArgs &a, bool gated, cudaStream_t s) {
     if (warps == 0) return cudaSuccess;
     const long long blocks = (warps * 32 + 255) / 256;
     if (gated)
-        simt_up_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(*a.tab, a);
+        return launch_pdl(simt_up_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, *a.tab, a);
     else
-        simt_up_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(*a.tab, a);
-    return cudaGetLastError();
+        return launch_pdl(simt_up_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, *a.tab, a);
 }
 
 cudaError_t launch_simt_down(const ExpertArgs &a, cudaStream_t s) {
     const long long warps = static_cast<long long>(a.T) * a.k * a.m;
     if (warps == 0) return cudaSuccess;
     const long long blocks = (warps * 32 + 255) / 256;
-    simt_down_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(*a.tab, a);
-    return cudaGetLastError();
+    return launch_pdl(simt_down_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, *a.tab, a);
 }
 
 }  // namespace moe

@@ -104,6 +104,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rows_total = a.T * a.k;
+    pdl_wait();
+    pdl_trigger();
 
     if (tid == 0) {
         int n = 0;
@@ -326,6 +328,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // x_perm[pos] = x[gather[pos] / k] for the permuted rows (16-byte vectors).
 __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ gather,
                                    int rows, int k, int m, uint16_t *__restrict__ xp, uint32_t *err) {
+    pdl_wait();
+    pdl_trigger();
     const int vec = m / 8;
     const long long n = static_cast<long long>(rows) * vec;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
@@ -353,8 +357,7 @@ cudaError_t launch_tc_t(const ExpertArgs &a, const TcGeom &g, const CUtensorMap 
         if (err != cudaSuccess) return err;
         configured = static_cast<int>(smem);
     }
-    kern<<<num_sms, kTcThreads, smem, s>>>(*a.tab, a, g, bmap);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(num_sms), dim3(kTcThreads), smem, s, *a.tab, a, g, bmap);
 }
 
 TcGeom make_tc_geom(int K, int rows, int splits, int N) {
@@ -383,9 +386,9 @@ cudaError_t launch_gather_rows(const void *x, const int32_t *gather, int rows, i
     if (n == 0) return cudaSuccess;
     long long blocks = (n + 255) / 256;
     if (blocks > 152 * 8) blocks = 152 * 8;
-    gather_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        static_cast<const uint16_t *>(x), gather, rows, k, m, static_cast<uint16_t *>(x_perm), err);
-    return cudaGetLastError();
+    return launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                      static_cast<const uint16_t *>(x), gather, rows, k, m,
+                      static_cast<uint16_t *>(x_perm), err);
 }
 
 cudaError_t launch_tc_up(const ExpertArgs &a, bool gated, int splits, int N, const CUtensorMap &xmap,

@@ -150,6 +150,8 @@ __device__ void permute_block(const PermuteArgs &a, PermuteSmem &sm) {
 // products wait on shared-memory reads instead of a chain of L2 round trips.
 template <typename ActT, int EMAX, bool SMEM_W>
 __global__ void __launch_bounds__(256) router_topk_kernel(RouterArgs a, PermuteArgs pa) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int TOK = (64 / EMAX) < 1 ? 1 : (64 / EMAX);
     extern __shared__ __align__(16) uint8_t s_w[];
     __shared__ float s_part[8][TOK][EMAX];
@@ -301,6 +303,8 @@ constexpr int router_warps() { return EMAX <= 16 ? 32 : (EMAX == 32 ? 16 : 8); }
 
 template <int EMAX>
 __global__ void __launch_bounds__(router_warps<EMAX>() * 32) router_mma_kernel(RouterArgs a, PermuteArgs pa) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int kRouterWarps = router_warps<EMAX>();
     constexpr int NT = EMAX / 8;
     constexpr int TOK = 16;
@@ -390,6 +394,8 @@ template <int EMAX>
 __global__ void __launch_bounds__(128) topk_from_logits_kernel(const float *logits, int T, int E,
                                                                int k, int32_t *ids_out,
                                                                float *w_out) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= T) return;
     float l[EMAX];
@@ -410,6 +416,8 @@ __global__ void __launch_bounds__(128) topk_from_logits_kernel(const float *logi
 // [0, E) to expert 0 and flagging them, and flagging repeated ids.
 __global__ void topk_copy_validate_kernel(const int32_t *ids_in, const float *w_in, int T, int E,
                                           int k, int32_t *ids_out, float *w_out, uint32_t *err) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= T) return;
     uint32_t bits = 0;
@@ -431,6 +439,8 @@ __global__ void topk_copy_validate_kernel(const int32_t *ids_in, const float *w_
 
 // Standalone permute (after top-k from logits or from a given choice).
 __global__ void __launch_bounds__(1024) permute_kernel(PermuteArgs a) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ PermuteSmem psm;
     permute_block(a, psm);
 }
@@ -452,11 +462,10 @@ static cudaError_t launch_router_e(const RouterArgs &a, const PermuteArgs &pa, c
             if (e != cudaSuccess) return e;
             configured = kRouterSmemMax;
         }
-        kern<<<grid, 256, wbytes, s>>>(a, pa);
+        return launch_pdl(kern, dim3(grid), dim3(256), wbytes, s, a, pa);
     } else {
-        router_topk_kernel<ActT, EMAX, false><<<grid, 256, 0, s>>>(a, pa);
+        return launch_pdl(router_topk_kernel<ActT, EMAX, false>, dim3(grid), dim3(256), 0, s, a, pa);
     }
-    return cudaGetLastError();
 }
 
 template <int EMAX>
@@ -471,8 +480,7 @@ static cudaError_t launch_router_mma(const RouterArgs &a, const PermuteArgs &pa,
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    kern<<<(a.T + 15) / 16, kRouterWarps * 32, smem, s>>>(a, pa);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((a.T + 15) / 16), dim3(kRouterWarps * 32), smem, s, a, pa);
 }
 
 template <typename ActT>
@@ -500,28 +508,25 @@ cudaError_t launch_topk_from_logits(const float *logits, int T, int E, int k, in
     if (T <= 0) return cudaSuccess;
     dim3 grid((T + 127) / 128), block(128);
     if (E <= 8)
-        topk_from_logits_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
+        return launch_pdl(topk_from_logits_kernel<8>, grid, block, 0, s, logits, T, E, k, ids, w);
     else if (E <= 16)
-        topk_from_logits_kernel<16><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
+        return launch_pdl(topk_from_logits_kernel<16>, grid, block, 0, s, logits, T, E, k, ids, w);
     else if (E <= 32)
-        topk_from_logits_kernel<32><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
+        return launch_pdl(topk_from_logits_kernel<32>, grid, block, 0, s, logits, T, E, k, ids, w);
     else
-        topk_from_logits_kernel<64><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
-    return cudaGetLastError();
+        return launch_pdl(topk_from_logits_kernel<64>, grid, block, 0, s, logits, T, E, k, ids, w);
 }
 
 cudaError_t launch_topk_copy_validate(const int32_t *ids_in, const float *w_in, int T, int E,
                                       int k, int32_t *ids_out, float *w_out, uint32_t *err,
                                       cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    topk_copy_validate_kernel<<<(T + 127) / 128, 128, 0, s>>>(ids_in, w_in, T, E, k, ids_out, w_out,
-                                                              err);
-    return cudaGetLastError();
+    return launch_pdl(topk_copy_validate_kernel, dim3((T + 127) / 128), dim3(128), 0, s, ids_in,
+                      w_in, T, E, k, ids_out, w_out, err);
 }
 
 cudaError_t launch_permute(const PermuteArgs &a, cudaStream_t s) {
-    permute_kernel<<<1, 1024, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(permute_kernel, dim3(1), dim3(1024), 0, s, a);
 }
 
 }  // namespace moe
