@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--tokens", default="1,4,16,64",
                     help="decode batches per step (profiling runs use one)")
     ap.add_argument("--copies", type=int, default=2, help="weight copies that alternate")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one step (all route + forward calls) in a CUDA graph and "
+                         "time its replays")
     ap.add_argument("--paged", action="store_true",
                     help="paged-weights run: many Mixtral-shaped layers in pinned host memory, "
                          "a capped GPU slot pool, a seeded decode routing trace")
@@ -260,6 +263,17 @@ def traffic_record():
     return rec
 
 
+def capture(torch, fn, layers):
+    """A CUDA graph of fn() (route + forward calls on the current stream) and
+    the number of library kernel launches it holds."""
+    n0 = sum(c.stats().kernel_launches for c in layers)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g, sum(c.stats().kernel_launches for c in layers) - n0
+
+
 def run_ours(args, world, rank, local):
     import numpy as np
     import torch
@@ -279,15 +293,23 @@ def run_ours(args, world, rank, local):
     ys = {T: torch.empty((T, shape.m), dtype=torch.bfloat16, device=dev) for T in TOKENS}
     stream = torch.cuda.current_stream()
 
-    def step():
+    def step():  # on the current stream (the capture stream while a graph is captured)
         for i, T in enumerate(TOKENS):
             c = copies[i % len(copies)]
-            c.route(xs[T], stream=stream)
-            c.forward(xs[T], ys[T], stream=stream)
+            c.route(xs[T])
+            c.forward(xs[T], ys[T])
 
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
+    launches_per_step = None
+    run_step = step
+    if args.graph:
+        graph, launches_per_step = capture(torch, step, copies)
+        run_step = graph.replay
+        for _ in range(max(args.warmup, 3)):
+            run_step()
+        torch.cuda.synchronize()
     for c in copies:
         st, flags = c.sync_check()
         if st != moe.MOE_OK:
@@ -302,14 +324,15 @@ def run_ours(args, world, rank, local):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(args.steps):
-        step()
+        run_step()
     ev1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     barrier(world)
     ms = ev0.elapsed_time(ev1)
     ms_max = max_over_ranks(world, ms)
-    launches = sum(c.stats().kernel_launches for c in copies) - launches0
+    launches = (launches_per_step * args.steps if args.graph
+                else sum(c.stats().kernel_launches for c in copies) - launches0)
 
     # Per-launch kernel durations.  Kernels of one call are launched with
     # programmatic dependent launch, so each may start while its predecessor
@@ -423,13 +446,18 @@ def run_ours(args, world, rank, local):
         for i, T in enumerate(TOKENS):
             c = copies[i % len(copies)]
             xd[T].copy_(xh[T], non_blocking=True)
-            c.route(xd[T], stream=stream)
-            c.forward(xd[T], ys[T], stream=stream)
+            c.route(xd[T])
+            c.forward(xd[T], ys[T])
             yh[T].copy_(ys[T], non_blocking=True)
 
     k_e2e = max(args.steps // 2, 1)
     e2e_ms = None
     if not args.no_e2e:
+        for _ in range(3):
+            step_e2e()
+        torch.cuda.synchronize()
+        if args.graph:
+            step_e2e = capture(torch, step_e2e, copies)[0].replay
         for _ in range(3):
             step_e2e()
         torch.cuda.synchronize()
@@ -462,8 +490,10 @@ def run_ours(args, world, rank, local):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic",
-                "config": workload_config(shape, args.weights,
-                                          "inputs larger than L2: two weight copies alternate"),
+                "config": dict(workload_config(shape, args.weights,
+                                               "inputs larger than L2: two weight copies alternate"),
+                               launch="one CUDA graph per step, replayed" if args.graph
+                               else "stream launches with programmatic dependent launch"),
                 "roofline": roofline,
                 "layer_hbm": {"achieved": layer_gbs, "unit": "GB/s", "frac": layer_gbs / hbm,
                               "algorithmic_bytes_per_step": layer_bytes,

@@ -242,7 +242,10 @@ typedef struct {
 moe_status_t moe_layer_stats(moe_layer_t *layer, moe_stats_t *out);
 
 /* Wait (up to timeout_ms, polling) for the layer's last launched work, then
- * read and clear the device error word.  Returns MOE_ERR_TIMEOUT if the work
+ * read and clear the device error word.  The wait covers everything queued on
+ * the stream of the layer's last route or forward call up to this call (that
+ * stream must still exist; a stream being captured into a graph is refused
+ * with MOE_ERR_INVALID_ARG).  Returns MOE_ERR_TIMEOUT if the work
  * did not finish in time, MOE_ERR_INVALID_ARG if a kernel flagged bad
  * routing data (the flag bits are written to *flags if flags is not NULL),
  * MOE_OK otherwise. */

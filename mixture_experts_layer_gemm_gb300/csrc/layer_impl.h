@@ -59,6 +59,12 @@ struct moe_layer {
     cudaEvent_t get_event();
 
     cudaEvent_t done = nullptr;
+    // Stream of the last route or forward call.  No event is recorded per call:
+    // an event between two launches would end the programmatic-launch overlap
+    // of the last kernel of one call with the first of the next.
+    // moe_layer_sync_check records `done` on this stream when it is called.
+    cudaStream_t last_stream = nullptr;
+    bool launched = false;
     cudaStream_t ingest_stream = nullptr;
     std::vector<void *> allocations;
 

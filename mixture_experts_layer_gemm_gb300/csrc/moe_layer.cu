@@ -429,7 +429,8 @@ static moe_status_t run_permute(moe_layer_t *L, int T, moe_routing_t *r, cudaStr
                    r->scatter_index};
     moe_status_t st = launch_phase(L, MOE_PHASE_PERMUTE, s, "permute", [&] { return launch_permute(pa, s); });
     if (st != MOE_OK) return st;
-    CUDA_TRY(cudaEventRecord(L->done, s));
+    L->last_stream = s;
+    L->launched = true;
     r->T = T;
     return MOE_OK;
 }
@@ -456,7 +457,8 @@ extern "C" moe_status_t moe_route(moe_layer_t *L, const void *x, int T, moe_rout
     st = launch_phase(L, MOE_PHASE_ROUTER, s, "router_topk_permute",
                       [&] { return launch_router_topk(ra, pa, L->cfg.act_dtype == MOE_BF16, s); });
     if (st != MOE_OK) return st;
-    CUDA_TRY(cudaEventRecord(L->done, s));
+    L->last_stream = s;
+    L->launched = true;
     r->T = T;
     return MOE_OK;
 }
@@ -728,7 +730,8 @@ extern "C" moe_status_t moe_forward(moe_layer_t *L, const void *x, const moe_rou
     if (st != MOE_OK) return st;
     st = run_combine(L, r, splits, a.n_rows_cap, y, s);
     if (st != MOE_OK) return st;
-    CUDA_TRY(cudaEventRecord(L->done, s));
+    L->last_stream = s;
+    L->launched = true;
     return MOE_OK;
 }
 
@@ -803,6 +806,13 @@ extern "C" moe_status_t moe_layer_sync_check(moe_layer_t *L, int timeout_ms, uin
     if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
     if (flags) *flags = 0;
     cudaSetDevice(L->device);
+    if (L->launched) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        CUDA_TRY(cudaStreamIsCapturing(L->last_stream, &cs));
+        if (cs != cudaStreamCaptureStatusNone)
+            return fail(MOE_ERR_INVALID_ARG, "the layer's last stream is being captured into a graph");
+        CUDA_TRY(cudaEventRecord(L->done, L->last_stream));
+    }
     const auto t0 = std::chrono::steady_clock::now();
     for (;;) {
         cudaError_t q = cudaEventQuery(L->done);

@@ -124,7 +124,7 @@ extern "C" moe_status_t moe_forward_static_scratch(moe_layer_t *L, const void *x
     st = launch_phase(L, MOE_PHASE_COMBINE, s, "combine",
                       [&] { return launch_combine(ca, true, s); });
     if (st != MOE_OK) return st;
-    const cudaError_t e = cudaEventRecord(L->done, s);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    L->last_stream = s;
+    L->launched = true;
     return MOE_OK;
 }

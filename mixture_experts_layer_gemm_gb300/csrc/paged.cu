@@ -309,7 +309,8 @@ moe_status_t paged_forward(moe_layer *L, const void *x, const moe_routing_t *r, 
         if (st != MOE_OK) return st;
     }
     PG_TRY(cudaEventRecord(L->fwd_t1, s));
-    PG_TRY(cudaEventRecord(L->done, s));
+    L->last_stream = s;
+    L->launched = true;
     L->fwd_pending = true;
     L->stats.forwards += 1;
     return MOE_OK;
