@@ -375,8 +375,7 @@ def run_ours(args, world, rank, local):
             "down_bytes": n_act * (shape.m * shape.p * wbytes + scale_dn) + rows * shape.p * 2,
             "up_flops": 2.0 * n_up * shape.m * shape.p * rows,
             "down_flops": 2.0 * shape.m * shape.p * rows,
-            "path": "tensor-core" if (rows + shape.E - 1) // shape.E > 6 and args.weights == "bf16"
-            else "gemv"}
+            "path": "tensor-core" if (rows + shape.E - 1) // shape.E > 6 else "gemv"}
     bytes_up = sum(w["up_bytes"] for w in work.values())
     bytes_down = sum(w["down_bytes"] for w in work.values())
     flops_up = sum(w["up_flops"] for w in work.values())

@@ -83,15 +83,23 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 }
 
 // Four signed int8 values (one 32-bit word, byte 0 first) -> two bf16x2 words
-// holding bytes (0,1) and (2,3).  Every int8 is exactly representable in bf16.
+// holding bytes (0,1) and (2,3), exactly, with byte permutes and one packed
+// bf16 FMA per pair (no int-to-float or float-to-bf16 conversions).
+// A two's-complement byte b with low seven bits l and sign bit s is
+// l - 128 s.  The bf16 bit pattern 0x4300 | l is 128 + l (exponent 2^7, l in
+// the seven mantissa bits), and 0x4300 | (s << 7) is 128 + 128 s (0x4380 is
+// 2^8).  Their difference, l - 128 s, lies in [-128, 127], so the packed
+// subtraction (an FMA by -1) is exact.
 __device__ __forceinline__ void i8x4_to_bf16x2x2(uint32_t v, uint32_t &lo, uint32_t &hi) {
-    const int32_t s = static_cast<int32_t>(v);
-    const float f0 = static_cast<float>((s << 24) >> 24);
-    const float f1 = static_cast<float>((s << 16) >> 24);
-    const float f2 = static_cast<float>((s << 8) >> 24);
-    const float f3 = static_cast<float>(s >> 24);
-    lo = pack_bf16x2(f0, f1);
-    hi = pack_bf16x2(f2, f3);
+    const uint32_t mag = v & 0x7F7F7F7Fu;
+    const uint32_t sgn = v & 0x80808080u;
+    const uint32_t x_lo = __byte_perm(mag, 0x43434343u, 0x4140);  // {b0, 0x43, b1, 0x43}
+    const uint32_t x_hi = __byte_perm(mag, 0x43434343u, 0x4342);  // {b2, 0x43, b3, 0x43}
+    const uint32_t y_lo = __byte_perm(sgn, 0x43434343u, 0x4140);
+    const uint32_t y_hi = __byte_perm(sgn, 0x43434343u, 0x4342);
+    const uint32_t minus_one = 0xBF80BF80u;  // bf16x2 (-1, -1)
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(lo) : "r"(y_lo), "r"(minus_one), "r"(x_lo));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(hi) : "r"(y_hi), "r"(minus_one), "r"(x_hi));
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

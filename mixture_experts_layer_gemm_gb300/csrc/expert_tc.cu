@@ -34,6 +34,7 @@
 #include "kernels.cuh"
 #include "packing.h"
 #include "tc.cuh"
+#include "tc_tiles.cuh"
 
 namespace moe {
 
@@ -46,42 +47,6 @@ constexpr int kMaxTcStages = 8;
 constexpr int kTcSmemBudget = 200 * 1024;
 
 enum Phase { kUp = 0, kDown = 1 };
-
-struct TcGeom {
-    int K;          // reduction length
-    int rg;         // row-groups of 16 stored rows
-    int n_rb;       // 128-row blocks
-    int nkb;        // K / 64
-    int splits;     // reduction splits
-    int N;          // token tile
-    int stages;
-    int b_bytes;    // N * 128
-    int tmem_cols;  // power of two >= 2N
-    uint32_t idesc;
-};
-
-struct TcTile {
-    int e, ks, rb, tt, off, q, kb0, kb1;
-};
-
-__device__ __forceinline__ TcTile tc_tile(long long u, const long long *prefix, const int *act,
-                                          const int *offs, const int *qs, int nact, const TcGeom &g) {
-    int i = 0;
-    while (i + 1 < nact && u >= prefix[i + 1]) ++i;
-    const long long local = u - prefix[i];
-    const int ntt = (qs[i] + g.N - 1) / g.N;
-    TcTile t;
-    t.e = act[i];
-    t.off = offs[i];
-    t.q = qs[i];
-    t.tt = static_cast<int>(local % ntt);
-    const long long rest = local / ntt;
-    t.rb = static_cast<int>(rest % g.n_rb);
-    t.ks = static_cast<int>(rest / g.n_rb);
-    t.kb0 = static_cast<int>((static_cast<long long>(g.nkb) * t.ks) / g.splits);
-    t.kb1 = static_cast<int>((static_cast<long long>(g.nkb) * (t.ks + 1)) / g.splits);
-    return t;
-}
 
 template <int PHASE, bool GATED>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -108,29 +73,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pdl_trigger();
 
     if (tid == 0) {
-        int n = 0;
-        long long acc = 0;
-        s_prefix[0] = 0;
-        for (int e = 0; e < a.E; ++e) {
-            const int off = a.offsets[e], end = a.offsets[e + 1];
-            if (off < 0 || end > rows_total || end < off) {
-                flag_error(a.err, kErrOffsets);
-                continue;
-            }
-            const int q = end - off;
-            bool take = q > 0;
-            if (a.n_only > 0) {
-                take = false;
-                for (int i = 0; i < a.n_only; ++i) take |= (a.only[i] == e && q > 0);
-            }
-            if (!take) continue;
-            s_act[n] = e;
-            s_off[n] = off;
-            s_q[n] = q;
-            acc += static_cast<long long>(geo.splits) * geo.n_rb * ((q + geo.N - 1) / geo.N);
-            s_prefix[++n] = acc;
-        }
-        s_nact = n;
+        s_nact = tc_list_tiles(a, geo, s_act, s_off, s_q, s_prefix);
         s_abort = 0;
         for (int i = 0; i < geo.stages; ++i) {
             mbar_init(&full_bar[i], 1);

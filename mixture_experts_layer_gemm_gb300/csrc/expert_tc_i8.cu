@@ -1,0 +1,393 @@
+// expert_tc_i8.cu -- grouped expert GEMM on the tensor cores with int8 weights
+// (per-output-channel symmetric codes; DeepSpeed-Inference article, part 4:
+// INT8 weights dequantised inside the kernel).
+//
+// Numerics: the codes q (|q| <= 127) are exact in bf16, so the tensor cores
+// compute sum_k q[row, k] x[token, k] in fp32 from bf16 operands, and the
+// epilogue multiplies by the row's scale -- the same "scale after the dot
+// product" as the int8 weight-streaming GEMV.
+//
+// Shared-memory traffic, not the tensor pipe, bounds the bf16 grouped GEMM
+// (TMA fill + operand reads).  Widening int8 to bf16 in shared memory would
+// add a write and a read of twice the bytes, so the widened tile goes to
+// tensor memory instead and the MMA takes its A operand from there:
+//   stage (128 reduction elements): A8 = 128 weight rows x 128 int8 (one
+//     contiguous 16 KB run of the packed layout, one bulk copy) and
+//     B = N tokens x 128 bf16 (two tensor-map copies of 64 columns, 128-byte
+//     swizzle);
+//   converter warps (two per TMEM lane quarter; a thread takes one weight row
+//     and one half of the stage's reduction range) widen 64 codes to 32
+//     bf16x2 words and store them to an A buffer in tensor memory (two
+//     buffers of 64 columns);
+//   the MMA thread issues 8 MMAs of K = 16 per stage, A from tensor memory,
+//     B from shared memory, D = 128 lanes x N fp32 columns (two buffers).
+// Tensor memory: D buffers at columns [0, 2N) (N <= 128), A buffers at
+// [256, 384); 512 columns allocated (one CTA per SM).
+// Warp roles (448 threads): 0 producer, 1 tensor-memory owner + MMA issuer,
+// 2-5 epilogue, 6-13 converters.  Every wait is bounded; a wait that gives up
+// sets kErrWaitTimeout and the CTA drains and returns.
+#include "common.cuh"
+#include "kernels.cuh"
+#include "packing.h"
+#include "tc.cuh"
+#include "tc_tiles.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kThreads = 448;
+constexpr int kEpiWarps = 4;
+constexpr int kCvtWarps = 8;  // two per TMEM lane quarter, one K half each
+constexpr int kA8Bytes = 16384;  // 128 rows x 128 int8
+constexpr int kMaxStages = 8;
+constexpr int kSmemBudget = 200 * 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kACol = 256;  // first column of the A buffers
+constexpr int kABufs = 2;        // A buffers of 64 columns at [256, 384)
+
+enum Phase { kUp = 0, kDown = 1 };
+
+template <int PHASE, bool GATED>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_i8_kernel(const ExpertTables tab, const ExpertArgs a, const TcGeom geo,
+                 const __grid_constant__ CUtensorMap bmap) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
+    __shared__ uint64_t afull_bar[kABufs], aempty_bar[kABufs];
+    __shared__ uint64_t tfull_bar[2], tempty_bar[2], done_bar;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_act[kMaxExperts], s_off[kMaxExperts], s_q[kMaxExperts];
+    __shared__ long long s_prefix[kMaxExperts + 1];
+    __shared__ int s_nact;
+    __shared__ volatile int s_abort;
+
+    const uint32_t raw_s = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const int stage_bytes = kA8Bytes + 2 * geo.b_bytes;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rows_total = a.T * a.k;
+    pdl_wait();
+    pdl_trigger();
+
+    if (tid == 0) {
+        s_nact = tc_list_tiles(a, geo, s_act, s_off, s_q, s_prefix);
+        s_abort = 0;
+        for (int i = 0; i < geo.stages; ++i) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&empty_bar[i], 1 + kCvtWarps);  // MMA commit + converter warps
+        }
+        for (int i = 0; i < kABufs; ++i) {
+            mbar_init(&afull_bar[i], kCvtWarps);
+            mbar_init(&aempty_bar[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull_bar[i], 1);
+            mbar_init(&tempty_bar[i], kEpiWarps);
+        }
+        mbar_init(&done_bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(&s_tmem, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = s_tmem;
+    const int nact = s_nact;
+    const long long total = nact ? s_prefix[nact] : 0;
+
+    uint32_t last_parity[kMaxStages];
+    bool used[kMaxStages];
+    for (int i = 0; i < kMaxStages; ++i) used[i] = false;
+    if (warp == 0) {
+        // ======================= producer =======================================
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (long long u = blockIdx.x; u < total && !s_abort; u += gridDim.x) {
+                const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
+                const uint8_t *w = static_cast<const uint8_t *>(PHASE == kUp ? tab.w1[t.e] : tab.w2[t.e]);
+                const int brow = t.off + t.tt * geo.N;
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                    if (!mbar_wait(&empty_bar[stage], phase ^ 1u)) {
+                        flag_error(a.err, kErrWaitTimeout);
+                        s_abort = 1;
+                        break;
+                    }
+                    uint8_t *st = smem + stage * stage_bytes;
+                    mbar_arrive_expect_tx(&full_bar[stage], kA8Bytes + 2 * geo.b_bytes);
+                    const size_t blk = static_cast<size_t>(kb) * geo.rg + 8 * t.rb;
+                    bulk_g2s(st, w + blk * kBlockBytes, kA8Bytes, &full_bar[stage]);
+                    tma_load_2d(st + kA8Bytes, &bmap, kb * 128, brow, &full_bar[stage]);
+                    tma_load_2d(st + kA8Bytes + geo.b_bytes, &bmap, kb * 128 + 64, brow, &full_bar[stage]);
+                    used[stage] = true;
+                    last_parity[stage] = phase;
+                    if (++stage == geo.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ======================= MMA issuer =====================================
+        if (lane == 0) {
+            int stage = 0, abuf = 0;
+            uint32_t phase = 0, aphase = 0;
+            int ntile = 0;
+            for (long long u = blockIdx.x; u < total && !s_abort; u += gridDim.x, ++ntile) {
+                const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
+                const int buf = ntile & 1;
+                const uint32_t use_parity = (ntile >> 1) & 1;
+                if (!mbar_wait(&tempty_bar[buf], use_parity ^ 1u)) {
+                    flag_error(a.err, kErrWaitTimeout);
+                    s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(buf * geo.N);
+                const int n_valid = min(geo.N, (t.q - t.tt * geo.N + 15) / 16 * 16);
+                const uint32_t idesc = idesc_bf16_f32(128, n_valid);
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                    if (!mbar_wait(&full_bar[stage], phase) || !mbar_wait(&afull_bar[abuf], aphase)) {
+                        flag_error(a.err, kErrWaitTimeout);
+                        s_abort = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t bbase = smem_u32(smem + stage * stage_bytes + kA8Bytes);
+                    const uint32_t acol = tmem_base + kACol + static_cast<uint32_t>(abuf * 64);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t bd = smem_desc(bbase + (kk >> 2) * geo.b_bytes + (kk & 3) * 32, 16,
+                                                      1024, kLayoutSw128);
+                        tc_mma_tmem_a(d, acol + kk * 8, bd, idesc, (kb > t.kb0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&empty_bar[stage]);   // B slot read
+                    tc_commit(&aempty_bar[abuf]);   // A buffer read
+                    if (++stage == geo.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    if (++abuf == kABufs) {
+                        abuf = 0;
+                        aphase ^= 1u;
+                    }
+                }
+                tc_commit(&tfull_bar[buf]);
+            }
+            tc_commit(&done_bar);
+            if (!mbar_wait(&done_bar, 0)) flag_error(a.err, kErrWaitTimeout);
+        }
+    } else if (warp < 2 + kEpiWarps) {
+        // ======================= epilogue =======================================
+        const int lq = warp & 3;
+        const int row_in_tile = lq * 32 + lane;
+        int ntile = 0;
+        for (long long u = blockIdx.x; u < total; u += gridDim.x, ++ntile) {
+            if (__any_sync(0xffffffffu, s_abort)) break;
+            const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
+            const int buf = ntile & 1;
+            const uint32_t use_parity = (ntile >> 1) & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&tfull_bar[buf], use_parity))) {
+                if (lane == 0) flag_error(a.err, kErrWaitTimeout);
+                s_abort = 1;
+                break;
+            }
+            tc_fence_after();
+            const int R = t.rb * 128 + row_in_tile;  // stored weight row of this thread
+            // per-row scale: SwiGLU gate rows use s1, up rows s3 (feature f);
+            // ReLU rows s1[R]; down-projection rows s2[R]
+            const int r16 = R & 15;
+            const int f = (R >> 4) * 8 + (r16 & 7);
+            float scale;
+            if (PHASE == kUp && GATED)
+                scale = (r16 < 8) ? tab.s1[t.e][f] : tab.s3[t.e][f];
+            else if (PHASE == kUp)
+                scale = tab.s1[t.e][R];
+            else
+                scale = tab.s2[t.e][R];
+            const int tok0 = t.tt * geo.N;
+            const int n_valid = min(geo.N, (t.q - tok0 + 15) / 16 * 16);
+            for (int c0 = 0; c0 < n_valid; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(tmem_base + (static_cast<uint32_t>(lq * 32) << 16) +
+                              static_cast<uint32_t>(buf * geo.N + c0),
+                          v);
+                tmem_ld_wait();
+                if (PHASE == kUp && GATED) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float gv = __uint_as_float(v[j]) * scale;
+                        const float uv = __shfl_down_sync(0xffffffffu, gv, 8);
+                        const int tok = tok0 + c0 + j;
+                        if (r16 < 8 && tok < t.q) {
+                            const int pos = t.off + tok;
+                            if (geo.splits == 1) {
+                                static_cast<__nv_bfloat16 *>(a.h)[static_cast<size_t>(pos) * a.p + f] =
+                                    __float2bfloat16_rn(silu(gv) * uv);
+                            } else {
+                                const size_t o = (static_cast<size_t>(t.ks) * a.n_rows_cap + pos) * a.p + f;
+                                a.gate_part[o] = gv;
+                                a.up_part[o] = uv;
+                            }
+                        }
+                    }
+                } else if (PHASE == kUp) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int tok = tok0 + c0 + j;
+                        if (tok < t.q) {
+                            const int pos = t.off + tok;
+                            const float hv = __uint_as_float(v[j]) * scale;
+                            if (geo.splits == 1)
+                                static_cast<__nv_bfloat16 *>(a.h)[static_cast<size_t>(pos) * a.p + R] =
+                                    __float2bfloat16_rn(fmaxf(hv, 0.0f));
+                            else
+                                a.gate_part[(static_cast<size_t>(t.ks) * a.n_rows_cap + pos) * a.p + R] = hv;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int tok = tok0 + c0 + j;
+                        if (tok < t.q) {
+                            const int pos = t.off + tok;
+                            const int fi = a.gather[pos];
+                            const float wgt = (fi >= 0 && fi < rows_total) ? a.topk_w[fi] : 0.0f;
+                            a.ypart[(static_cast<size_t>(t.ks) * a.n_rows_cap + pos) * a.m + R] =
+                                wgt * (__uint_as_float(v[j]) * scale);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+        }
+    } else {
+        // ======================= converters =====================================
+        // thread = one weight row r of the 128-row block and one K half hk of
+        // the stage: row group r / 16, atom half G = (r % 16) / 8, row g = r % 8
+        // inside the 512-byte atoms; codes 64 hk .. 64 hk + 63 are atom hk
+        const int lq = warp & 3;
+        const int hk = (warp - 2 - kEpiWarps) >> 2;
+        const int r = lq * 32 + lane;
+        const int rgl = r >> 4, G = (r >> 3) & 1, g = r & 7;
+        const uint32_t row_off = static_cast<uint32_t>(rgl * kBlockBytes + G * 1024 + hk * 512);
+        int stage = 0, abuf = 0;
+        uint32_t phase = 0, aphase = 0;
+        for (long long u = blockIdx.x; u < total; u += gridDim.x) {
+            if (__any_sync(0xffffffffu, s_abort)) break;
+            const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
+            bool ok = true;
+            for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                // warp-uniform waits: tcgen05.st below needs the whole warp
+                if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[stage], phase)) ||
+                    !__all_sync(0xffffffffu, mbar_wait(&aempty_bar[abuf], aphase ^ 1u))) {
+                    if (lane == 0) flag_error(a.err, kErrWaitTimeout);
+                    s_abort = 1;
+                    ok = false;
+                    break;
+                }
+                const uint32_t a8_s = smem_u32(smem + stage * stage_bytes) + row_off;
+                uint32_t wv[32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint4 q = lds_v4(a8_s + atom_chunk_offset(g, c));
+                    // codes 16c .. 16c + 15 of this half -> columns 8c .. 8c + 7
+                    i8x4_to_bf16x2x2(q.x, wv[c * 8 + 0], wv[c * 8 + 1]);
+                    i8x4_to_bf16x2x2(q.y, wv[c * 8 + 2], wv[c * 8 + 3]);
+                    i8x4_to_bf16x2x2(q.z, wv[c * 8 + 4], wv[c * 8 + 5]);
+                    i8x4_to_bf16x2x2(q.w, wv[c * 8 + 6], wv[c * 8 + 7]);
+                }
+                tc_fence_after();
+                tmem_st32(tmem_base + (static_cast<uint32_t>(lq * 32) << 16) + kACol +
+                              static_cast<uint32_t>(abuf * 64 + hk * 32),
+                          wv);
+                tmem_st_wait();
+                tc_fence_before();
+                fence_proxy_async_smem();  // our reads of the A8 slot precede its next copy
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&afull_bar[abuf]);
+                    mbar_arrive(&empty_bar[stage]);
+                }
+                if (++stage == geo.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                if (++abuf == kABufs) {
+                    abuf = 0;
+                    aphase ^= 1u;
+                }
+            }
+            if (!ok) break;
+        }
+    }
+    // one barrier for every role; then no copy may still be in flight and the
+    // tensor memory is released
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0 && lane == 0)
+        for (int i = 0; i < geo.stages; ++i)
+            if (used[i]) mbar_wait(&full_bar[i], last_parity[i]);
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+template <int PHASE, bool GATED>
+cudaError_t launch_t(const ExpertArgs &a, const TcGeom &g, const CUtensorMap &bmap, int num_sms,
+                     cudaStream_t s) {
+    const size_t smem = 1024 + static_cast<size_t>(g.stages) * (kA8Bytes + 2 * g.b_bytes);
+    auto kern = tc_i8_kernel<PHASE, GATED>;
+    static int configured = 0;
+    if (static_cast<int>(smem) > configured) {
+        const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     static_cast<int>(smem));
+        if (err != cudaSuccess) return err;
+        configured = static_cast<int>(smem);
+    }
+    return launch_pdl(kern, dim3(num_sms), dim3(kThreads), smem, s, *a.tab, a, g, bmap);
+}
+
+// K: reduction length (multiple of 128); rows: stored rows (multiple of 128);
+// N: token tile, 16 .. 128 in steps of 16.
+TcGeom make_geom(int K, int rows, int splits, int N) {
+    TcGeom g;
+    g.K = K;
+    g.rg = rows / 16;
+    g.n_rb = rows / 128;
+    g.nkb = K / 128;
+    g.splits = splits;
+    g.N = N;
+    g.b_bytes = N * 128;
+    const int st = kSmemBudget / (kA8Bytes + 2 * g.b_bytes);
+    g.stages = st > kMaxStages ? kMaxStages : st;
+    g.tmem_cols = static_cast<int>(kTmemCols);
+    g.idesc = idesc_bf16_f32(128, N);
+    return g;
+}
+
+}  // namespace
+
+cudaError_t launch_tc_i8_up(const ExpertArgs &a, bool gated, int splits, int N, const CUtensorMap &xmap,
+                            int num_sms, cudaStream_t s) {
+    if (N < 16 || N > kTcI8MaxN || N % 16) return cudaErrorInvalidValue;
+    const TcGeom g = make_geom(a.m, gated ? 2 * a.p : a.p, splits, N);
+    return gated ? launch_t<kUp, true>(a, g, xmap, num_sms, s) : launch_t<kUp, false>(a, g, xmap, num_sms, s);
+}
+
+cudaError_t launch_tc_i8_down(const ExpertArgs &a, int splits, int N, const CUtensorMap &hmap,
+                              int num_sms, cudaStream_t s) {
+    if (N < 16 || N > kTcI8MaxN || N % 16) return cudaErrorInvalidValue;
+    const TcGeom g = make_geom(a.p, a.m, splits, N);
+    return launch_t<kDown, false>(a, g, hmap, num_sms, s);
+}
+
+}  // namespace moe

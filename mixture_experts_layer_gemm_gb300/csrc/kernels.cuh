@@ -112,6 +112,13 @@ cudaError_t launch_tc_up(const ExpertArgs &a, bool gated, int splits, int N, con
                          int num_sms, cudaStream_t s);
 cudaError_t launch_tc_down(const ExpertArgs &a, int splits, int N, const CUtensorMap &hmap,
                            int num_sms, cudaStream_t s);
+// The same with int8 weights (K a multiple of 128): codes widened to bf16 in
+// tensor memory, per-row scale in the epilogue; N tokens per tile, 16..128.
+constexpr int kTcI8MaxN = 128;
+cudaError_t launch_tc_i8_up(const ExpertArgs &a, bool gated, int splits, int N, const CUtensorMap &xmap,
+                            int num_sms, cudaStream_t s);
+cudaError_t launch_tc_i8_down(const ExpertArgs &a, int splits, int N, const CUtensorMap &hmap,
+                              int num_sms, cudaStream_t s);
 
 // fp32 path (SIMT, warp-shuffle reductions)
 cudaError_t launch_simt_up(const ExpertArgs &a, bool gated, cudaStream_t s);

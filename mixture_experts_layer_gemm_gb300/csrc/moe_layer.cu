@@ -71,7 +71,11 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
 constexpr int kSplitUpMax = 4, kSplitDownMax = 16;
-constexpr int kTcMinMeanTokens = 6;  // mean tokens per expert above which the tensor-core path runs
+// Mean tokens per expert above which the tensor-core path runs.  The int8
+// weight-streaming kernel widens each code once per pass and reuses it for
+// every token tile, so it stays ahead of the tensor cores for longer.
+constexpr int kTcMinMeanTokens = 6;
+constexpr int kTcMinMeanTokensI8 = 12;
 
 // Smallest split of a K-long reduction whose staged token rows (8 * nt rows of
 // K / splits bf16) fit the shared-memory budget.
@@ -352,7 +356,7 @@ static moe_status_t alloc_workspace(moe_layer_t *L) {
             L->workspace_bytes += 2 * n * 4;
         }
     }
-    if (c.act_dtype == MOE_BF16 && c.weight_dtype == MOE_BF16) {
+    if (c.act_dtype == MOE_BF16) {  // token rows in expert order for the tensor-core path
         L->x_perm = L->dalloc(rows * c.m * 2, &err);
         if (err) return cuda_fail(err, "cudaMalloc(x_perm)");
         L->workspace_bytes += rows * c.m * 2;
@@ -603,14 +607,17 @@ static moe_status_t run_experts_tc(moe_layer_t *L, ExpertArgs &a, int *splits_ou
     const moe_config_t &c = L->cfg;
     const bool gated = c.expert == MOE_EXPERT_SWIGLU;
     const int rows = a.T * a.k;
+    const bool i8 = c.weight_dtype == MOE_I8;
     const int mean_q = (rows + c.E - 1) / c.E;
-    const int N = tc_tile_n(mean_q);
+    int N = tc_tile_n(mean_q);
+    if (i8 && N > kTcI8MaxN) N = kTcI8MaxN;
+    const int bk = i8 ? 128 : 64;  // reduction elements per pipeline stage
     const int rows_up = gated ? 2 * c.p : c.p;
     int s_up = 1, s_down = 1;
     if (rows <= static_cast<int>(L->decode_rows_cap)) {
         const int n_act = expected_active(a.T, a.k, a.E);
-        s_up = tc_splits(c.m / 64, rows_up, N, mean_q, n_act, L->num_sms, L->split_up_max);
-        s_down = tc_splits(c.p / 64, c.m, N, mean_q, n_act, L->num_sms, L->split_down_max);
+        s_up = tc_splits(c.m / bk, rows_up, N, mean_q, n_act, L->num_sms, L->split_up_max);
+        s_down = tc_splits(c.p / bk, c.m, N, mean_q, n_act, L->num_sms, L->split_down_max);
         a.n_rows_cap = static_cast<int>(L->decode_rows_cap);
     } else {
         a.n_rows_cap = rows;
@@ -622,14 +629,18 @@ static moe_status_t run_experts_tc(moe_layer_t *L, ExpertArgs &a, int *splits_ou
         return launch_gather_rows(a.x, a.gather, rows, a.k, c.m, L->x_perm, L->err_word, s);
     });
     if (st == MOE_OK)
-        st = launch_phase(L, MOE_PHASE_UP, s, "tc_up",
-                          [&] { return launch_tc_up(a, gated, s_up, N, *xm, L->num_sms, s); });
+        st = launch_phase(L, MOE_PHASE_UP, s, "tc_up", [&] {
+            return i8 ? launch_tc_i8_up(a, gated, s_up, N, *xm, L->num_sms, s)
+                      : launch_tc_up(a, gated, s_up, N, *xm, L->num_sms, s);
+        });
     if (st == MOE_OK && s_up > 1)
         st = launch_phase(L, MOE_PHASE_UP_FINISH, s, "up_finish",
                           [&] { return launch_decode_up_finish(a, gated, s_up, s); });
     if (st == MOE_OK)
-        st = launch_phase(L, MOE_PHASE_DOWN, s, "tc_down",
-                          [&] { return launch_tc_down(a, s_down, N, *hm, L->num_sms, s); });
+        st = launch_phase(L, MOE_PHASE_DOWN, s, "tc_down", [&] {
+            return i8 ? launch_tc_i8_down(a, s_down, N, *hm, L->num_sms, s)
+                      : launch_tc_down(a, s_down, N, *hm, L->num_sms, s);
+        });
     *splits_out = s_down;
     return st;
 }
@@ -650,17 +661,19 @@ moe_status_t run_experts(moe_layer_t *L, ExpertArgs &a, int regime, int *splits_
         return st;
     }
     // regime: the weight-streaming GEMV while experts see few tokens, the
-    // tensor-core grouped GEMM beyond (bf16 weights; rows in 128-row blocks)
+    // tensor-core grouped GEMM beyond (rows in 128-row blocks; int8 weights
+    // also need K in 128-element blocks, which int8 layers have)
     const int mean_q = (rows + c.E - 1) / c.E;
-    const bool tc_shape = c.weight_dtype == MOE_BF16 && L->x_perm &&
-                          (gated ? (2 * c.p) % 128 : c.p % 128) == 0 && c.m % 128 == 0;
+    const bool tc_shape = L->x_perm && (gated ? (2 * c.p) % 128 : c.p % 128) == 0 &&
+                          c.m % 128 == 0 && (c.weight_dtype != MOE_I8 || c.p % 128 == 0);
     const bool fits_decode = rows <= static_cast<int>(L->decode_rows_cap);
     bool use_tc = false;
     if (regime == 2) {
-        if (!tc_shape) return fail(MOE_ERR_UNSUPPORTED, "batch kernels need bf16 weights and 128-row blocks");
+        if (!tc_shape) return fail(MOE_ERR_UNSUPPORTED, "batch kernels need 128-row blocks");
         use_tc = true;
     } else if (regime == 0) {
-        use_tc = tc_shape && (mean_q > kTcMinMeanTokens || !fits_decode);
+        const int min_q = c.weight_dtype == MOE_I8 ? kTcMinMeanTokensI8 : kTcMinMeanTokens;
+        use_tc = tc_shape && (mean_q > min_q || !fits_decode);
     }
     if (use_tc) return run_experts_tc(L, a, splits_out, s);
     const WeightType wt = (c.weight_dtype == MOE_I8) ? WeightType::kI8 : WeightType::kBF16;

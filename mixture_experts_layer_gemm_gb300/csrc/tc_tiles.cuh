@@ -1,0 +1,83 @@
+// tc_tiles.cuh -- the tile space of the grouped expert GEMMs on the tensor
+// cores: (expert, reduction split, 128-row block, token tile), token tile
+// fastest, so that CTAs working at the same time share a weight block
+// through L2.  Each CTA of a persistent launch takes tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ...; the active experts and the prefix sums of their
+// tile counts sit in shared memory.
+#pragma once
+
+#include <stdint.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+struct TcGeom {
+    int K;          // reduction length
+    int rg;         // row-groups of 16 stored rows
+    int n_rb;       // 128-row blocks
+    int nkb;        // K / (reduction elements per pipeline stage)
+    int splits;     // reduction splits
+    int N;          // token tile
+    int stages;
+    int b_bytes;    // N * 128
+    int tmem_cols;  // columns allocated
+    uint32_t idesc;
+};
+
+struct TcTile {
+    int e, ks, rb, tt, off, q, kb0, kb1;
+};
+
+__device__ __forceinline__ TcTile tc_tile(long long u, const long long *prefix, const int *act,
+                                          const int *offs, const int *qs, int nact, const TcGeom &g) {
+    int i = 0;
+    while (i + 1 < nact && u >= prefix[i + 1]) ++i;
+    const long long local = u - prefix[i];
+    const int ntt = (qs[i] + g.N - 1) / g.N;
+    TcTile t;
+    t.e = act[i];
+    t.off = offs[i];
+    t.q = qs[i];
+    t.tt = static_cast<int>(local % ntt);
+    const long long rest = local / ntt;
+    t.rb = static_cast<int>(rest % g.n_rb);
+    t.ks = static_cast<int>(rest / g.n_rb);
+    t.kb0 = static_cast<int>((static_cast<long long>(g.nkb) * t.ks) / g.splits);
+    t.kb1 = static_cast<int>((static_cast<long long>(g.nkb) * (t.ks + 1)) / g.splits);
+    return t;
+}
+
+// One thread: list the experts this launch covers (all with tokens, or those
+// in a.only), their segments, and the prefix sums of their tile counts.
+// Returns the number of experts listed.
+__device__ __forceinline__ int tc_list_tiles(const ExpertArgs &a, const TcGeom &geo, int *act,
+                                             int *offs, int *qs, long long *prefix) {
+    const int rows_total = a.T * a.k;
+    int n = 0;
+    long long acc = 0;
+    prefix[0] = 0;
+    for (int e = 0; e < a.E; ++e) {
+        const int off = a.offsets[e], end = a.offsets[e + 1];
+        if (off < 0 || end > rows_total || end < off) {
+            flag_error(a.err, kErrOffsets);
+            continue;
+        }
+        const int q = end - off;
+        bool take = q > 0;
+        if (a.n_only > 0) {
+            take = false;
+            for (int i = 0; i < a.n_only; ++i) take |= (a.only[i] == e && q > 0);
+        }
+        if (!take) continue;
+        act[n] = e;
+        offs[n] = off;
+        qs[n] = q;
+        acc += static_cast<long long>(geo.splits) * geo.n_rb * ((q + geo.N - 1) / geo.N);
+        prefix[++n] = acc;
+    }
+    return n;
+}
+
+}  // namespace moe

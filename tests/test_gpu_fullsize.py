@@ -30,6 +30,12 @@ def mixtral_lib(mixtral):
 
 
 @pytest.fixture(scope="module")
+def mixtral_q(mixtral):
+    """The oracle's own int8 codes and scales of the Mixtral-shaped experts."""
+    return oracle_quantized(mixtral)
+
+
+@pytest.fixture(scope="module")
 def phi():
     return wl.make_layer(wl.PHI35, seed=0, device="cuda")
 
@@ -64,11 +70,11 @@ def test_mixtral_decode_bf16(mixtral, mixtral_lib, T):
     assert run.counts.sum() == 2 * T
 
 
-def test_mixtral_decode_int8(mixtral):
+def test_mixtral_decode_int8(mixtral, mixtral_q):
     shape = wl.MIXTRAL.with_weight("i8")
     layer = wl.Layer(shape, mixtral.w_router, None, mixtral.w1, mixtral.w2, mixtral.w3)
     ml = moe.MoELayer(layer, 64, with_logits=True)
-    q = oracle_quantized(layer)
+    q = mixtral_q
     codes, scales = moe.moe_layer_read_expert(ml.handle, 5, 2, (shape.p, shape.m), np.int8)
     np.testing.assert_array_equal(codes, q["w2"][5])
     np.testing.assert_array_equal(scales, q["s2"][5])
@@ -98,6 +104,19 @@ def test_mixtral_batch_zipf(mixtral, T):
     ml = moe.MoELayer(layer, T, with_logits=True)
     run = _check(ml, layer, T, seed=400 + T, n_sample=8, tol=1e-2)
     assert run.counts[0] == run.counts.max()
+    ml.close()
+
+
+@pytest.mark.parametrize("T", [512, 2048])
+def test_mixtral_batch_zipf_int8(mixtral, mixtral_q, T):
+    """The batch regime with int8 weights (tensor cores, codes widened in
+    tensor memory): against the original weights at 3e-2 and the oracle's own
+    dequantised weights at 1e-2."""
+    shape = wl.MIXTRAL.with_zipf(1.2).with_weight("i8")
+    layer = wl.Layer(shape, mixtral.w_router, wl.zipf_bias(shape.E, 1.2), mixtral.w1, mixtral.w2,
+                     mixtral.w3)
+    ml = moe.MoELayer(layer, T, with_logits=True)
+    _check(ml, layer, T, seed=450 + T, n_sample=6, tol=3e-2, quantized=mixtral_q)
     ml.close()
 
 

@@ -229,7 +229,38 @@ def test_int8_codes_and_scales_bit_exact():
 
 @pytest.mark.parametrize("T", [1, 16, 64])
 def test_int8_decode(T):
-    run_and_check(I8, T, seed=14)
+    run_and_check(I8, T, seed=14, regime=moe.REGIME_DECODE)
+
+
+@pytest.mark.parametrize("T", [1, 37, 200, 700])
+def test_int8_tensor_core(T):
+    """int8 codes widened to bf16 in tensor memory, row scale in the epilogue."""
+    run_and_check(I8, T, seed=16, regime=moe.REGIME_BATCH)
+
+
+@pytest.mark.parametrize("T", [5, 300])
+def test_int8_relu_tensor_core(T):
+    run_and_check(RELU_BF16.with_weight("i8"), T, seed=17, regime=moe.REGIME_BATCH)
+
+
+def test_int8_zipf_batch_auto_regime():
+    run, _ = run_and_check(I8.with_zipf(1.2), 900, seed=18)
+    assert run.counts[0] > 4 * run.counts[-1]
+
+
+def test_int8_tensor_core_and_decode_paths_agree():
+    """Both int8 paths take the same codes and scales: their outputs differ
+    only by fp32 summation order and the rounding of h."""
+    layer = get_layer(I8, seed=19)
+    x = wl.make_tokens(I8, 48, seed=20)
+    ys = []
+    for regime in (moe.REGIME_DECODE, moe.REGIME_BATCH):
+        ml = moe.MoELayer(layer, 48)
+        ml.set_regime(regime)
+        ys.append(f64(Run(ml, x).y_np))
+        ml.close()
+    rel = np.linalg.norm(ys[0] - ys[1], axis=1) / np.linalg.norm(ys[1], axis=1)
+    assert rel.max() <= 1e-2
 
 
 # ---- edge cases ------------------------------------------------------------------------
