@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--paged-tokens", type=int, default=16, help="decode batch per layer")
     ap.add_argument("--paged-budget-gib", type=float, default=16.0)
     ap.add_argument("--paged-ways", type=int, default=4)
+    ap.add_argument("--paged-prefetch", type=int, default=0,
+                    help="experts each paged layer prefetches for the next layer (0: off)")
     ap.add_argument("--zipf", type=float, default=None,
                     help="router bias making expert popularity Zipf(s) (batch workloads)")
     ap.add_argument("--shape", default="mixtral", choices=["mixtral", "phi", "small"],
@@ -566,6 +568,7 @@ def run_paged(args, world, rank, local):
     budget = int(args.paged_budget_gib * (1 << 30))
     n_index, n_slots = moe.moe_pool_geometry(budget, eb, args.paged_ways)
     pool = moe.moe_pool_create(budget, eb, args.paged_ways, 0)
+    moe.moe_pool_set_prefetch(pool, args.paged_prefetch)
     layers = [moe.MoELayer(layer, T, pool=pool, layer_id=l) for l in range(L)]
     ids, w = wl.make_topk_trace(shape.E, shape.k, S + 1, L, T, seed=args.seed)
     dev = torch.device("cuda", local)
@@ -601,6 +604,8 @@ def run_paged(args, world, rank, local):
     hits = sum(b.slot_hits - a.slot_hits for a, b in zip(st0, st1))
     misses = sum(b.slot_misses - a.slot_misses for a, b in zip(st0, st1))
     h2d = sum(b.h2d_bytes - a.h2d_bytes for a, b in zip(st0, st1))
+    pf_copies = sum(b.prefetch_copies - a.prefetch_copies for a, b in zip(st0, st1))
+    pf_hits = sum(b.prefetch_hits - a.prefetch_hits for a, b in zip(st0, st1))
     copy_ms = sum(t["copy"][0] for t in tim)
     compute_ms = sum(sum(v[0] for k, v in t.items() if k != "copy") for t in tim)
     overlap = (copy_ms + compute_ms - wall_ms) / max(min(copy_ms, compute_ms), 1e-9)
@@ -614,12 +619,16 @@ def run_paged(args, world, rank, local):
             "vs_baseline": None, "dtype": args.weights, "data": "synthetic",
             "config": {"workload": f"{L} paged mixtral-8x7b moe layers, decode T={T}, "
                                    f"{args.paged_budget_gib:g} GiB slot pool, "
-                                   f"{n_index} sets x {args.paged_ways} ways",
+                                   f"{n_index} sets x {args.paged_ways} ways, "
+                                   f"prefetch {args.paged_prefetch}",
                        "layers": L, "T": T, "trace": "p_layer=0.44, p_token=0.5, seeded",
                        "tokens_per_step": T},
             "paged": {"sets": n_index, "ways": args.paged_ways, "slots": n_slots,
                       "expert_bytes": eb, "hit_rate": hits / max(hits + misses, 1),
                       "hits": hits, "misses": misses, "h2d_bytes": h2d,
+                      "prefetch": args.paged_prefetch, "prefetch_copies": pf_copies,
+                      "prefetch_hits": pf_hits,
+                      "prefetch_used_frac": pf_hits / max(pf_copies, 1),
                       "h2d_gbs_copy_stream": h2d / max(copy_ms * 1e-3, 1e-12) / 1e9,
                       "h2d_gbs_wall": h2d / (wall_ms * 1e-3) / 1e9,
                       "link_gbs_measured": link,

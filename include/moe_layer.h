@@ -238,6 +238,8 @@ typedef struct {
     uint64_t h2d_bytes;
     double h2d_ms;       /* summed duration of the copy-stream transfers   */
     double forward_ms;   /* summed duration of paged forward calls         */
+    uint64_t prefetch_copies; /* experts this layer's calls prefetched for the next layer */
+    uint64_t prefetch_hits;   /* lookups of this layer served by a prefetched expert      */
 } moe_stats_t;
 moe_status_t moe_layer_stats(moe_layer_t *layer, moe_stats_t *out);
 
@@ -288,10 +290,21 @@ moe_status_t moe_pool_create(size_t budget_bytes, size_t expert_bytes, int ways,
                              size_t page_bytes, moe_pool_t **out);
 moe_status_t moe_pool_destroy(moe_pool_t *pool);
 
-/* The pool's lookups since creation, oldest first (at most 2^20 kept): for
- * query i, the layer id, the expert, whether it hit (1) or missed (0) and the
- * slot (set * M + way) that served it.  Any output pointer may be NULL.
- * *n_out receives the number written (<= max).  Host-only. */
+/* Cross-layer prefetch (HARMOEny write-up, part 3.2; expert-cache article,
+ * section 2.1: consecutive layers often pick the same experts).  With
+ * max_experts > 0, every paged forward of layer l, after its own lookups,
+ * copies in for layer l + 1 (when attached to this pool and mapped to a
+ * different set) the max_experts experts that had the most tokens in this
+ * call (ties to the lower id) and are not resident for l + 1.  Each takes an
+ * empty or the least recently used way of l + 1's set.  0 (the default)
+ * turns it off.  Host-only; takes effect from the next forward call. */
+moe_status_t moe_pool_set_prefetch(moe_pool_t *pool, int max_experts);
+
+/* The pool's lookups and prefetch inserts since creation, oldest first (at
+ * most 2^20 kept): for entry i, the layer id, the expert, the kind -- 0 miss,
+ * 1 hit, 2 prefetch insert, 3 hit on a prefetched expert not used before --
+ * and the slot (set * M + way).  Any output pointer may be NULL.  *n_out
+ * receives the number written (<= max).  Host-only. */
 moe_status_t moe_pool_query_log(moe_pool_t *pool, int32_t *layer, int32_t *expert, int32_t *hit,
                                 int32_t *slot, int max, int *n_out);
 

@@ -66,7 +66,8 @@ class moe_timings_t(ctypes.Structure):
 class moe_stats_t(ctypes.Structure):
     _fields_ = [("kernel_launches", ctypes.c_uint64), ("forwards", ctypes.c_uint64), ("slot_hits", ctypes.c_uint64),
                 ("slot_misses", ctypes.c_uint64), ("h2d_bytes", ctypes.c_uint64),
-                ("h2d_ms", ctypes.c_double), ("forward_ms", ctypes.c_double)]
+                ("h2d_ms", ctypes.c_double), ("forward_ms", ctypes.c_double),
+                ("prefetch_copies", ctypes.c_uint64), ("prefetch_hits", ctypes.c_uint64)]
 
 
 class MoeError(RuntimeError):
@@ -98,6 +99,7 @@ _SIGNATURES = {
     "moe_pool_create": [_sz, _sz, _i, _sz, ctypes.POINTER(_vp)],
     "moe_pool_destroy": [_vp],
     "moe_pool_query_log": [_vp, _vp, _vp, _vp, _vp, _i, ctypes.POINTER(_i)],
+    "moe_pool_set_prefetch": [_vp, _i],
     "moe_status_string": [_i],
     "moe_last_error": [],
     "moe_version": [],
@@ -259,8 +261,16 @@ def moe_pool_destroy(pool):
     _check(lib().moe_pool_destroy(pool))
 
 
+def moe_pool_set_prefetch(pool, max_experts):
+    _check(lib().moe_pool_set_prefetch(pool, max_experts))
+
+
+LOG_MISS, LOG_HIT, LOG_PREFETCH, LOG_PREFETCH_HIT = 0, 1, 2, 3
+
+
 def moe_pool_query_log(pool, max_entries=1 << 20):
-    """(layer, expert, hit, slot) arrays of the pool's lookups so far."""
+    """(layer, expert, kind, slot) arrays of the pool's lookups and prefetch
+    inserts so far; kind is LOG_MISS, LOG_HIT, LOG_PREFETCH or LOG_PREFETCH_HIT."""
     arrs = [np.empty(max_entries, np.int32) for _ in range(4)]
     n = ctypes.c_int()
     _check(lib().moe_pool_query_log(pool, *[a.ctypes.data for a in arrs], max_entries,

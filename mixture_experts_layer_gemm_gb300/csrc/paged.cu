@@ -15,7 +15,11 @@
 //   3. makes the compute stream wait for the expert's copy and runs the
 //      expert's kernels, then records that the slot is in use until they end.
 // So the copy of expert i+1 overlaps the compute of expert i (the expert
-// prefetch of the HARMOEny write-up, part 3.2).  The launch plan (token tiles,
+// prefetch of the HARMOEny write-up, part 3.2).  With cross-layer prefetch on
+// (moe_pool_set_prefetch), a call then also copies, for layer_id + 1, the
+// experts this call used most (up to the prefetch count), guessing that the
+// next layer picks the same ones (expert-cache article, section 2.1); the
+// copies queue on the copy stream behind this call's own.  The launch plan (token tiles,
 // reduction splits) is the one a resident layer uses for the same T, so a paged
 // layer's output is bit-identical to the resident layer's.
 #include <algorithm>
@@ -44,11 +48,14 @@ struct moe_pool {
     struct Slot {
         int layer = -1, expert = -1;
         long long last_use = -1;
+        bool fetched = false;         // filled by a prefetch and not used since
         cudaEvent_t ready = nullptr;  // copy into the slot finished
         cudaEvent_t busy = nullptr;   // last compute reading the slot finished
         bool busy_recorded = false;
     };
     std::vector<Slot> slot;
+    std::vector<moe_layer *> layer_of;  // attached paged layers by layer id
+    int prefetch = 0;                   // experts prefetched for the next layer per call
     long long clock = 0;
     std::vector<int32_t> log;  // (layer, expert, hit, slot) per query
     std::mutex mu;
@@ -120,6 +127,13 @@ extern "C" moe_status_t moe_pool_destroy(moe_pool_t *pool) {
     return MOE_OK;
 }
 
+extern "C" moe_status_t moe_pool_set_prefetch(moe_pool_t *pool, int max_experts) {
+    if (!pool || max_experts < 0) return fail(MOE_ERR_INVALID_ARG, "pool is NULL or count negative");
+    std::lock_guard<std::mutex> lock(pool->mu);
+    pool->prefetch = max_experts;
+    return MOE_OK;
+}
+
 extern "C" moe_status_t moe_pool_query_log(moe_pool_t *pool, int32_t *layer, int32_t *expert,
                                            int32_t *hit, int32_t *slot, int max, int *n_out) {
     if (!pool || !n_out || max < 0) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
@@ -144,6 +158,14 @@ moe_status_t paged_attach(moe_layer *L) {
                     "(create the pool with moe_layer_info().expert_bytes)",
                     P->slot_bytes, L->expert_stride);
     if (P->device != L->device) return fail(MOE_ERR_INVALID_ARG, "pool and layer on different devices");
+    {
+        std::lock_guard<std::mutex> lock(P->mu);
+        const size_t id = static_cast<size_t>(L->layer_id);
+        if (id < P->layer_of.size() && P->layer_of[id])
+            return fail(MOE_ERR_INVALID_ARG, "layer id %d is already attached to this pool", L->layer_id);
+        if (id >= P->layer_of.size()) P->layer_of.resize(id + 1, nullptr);
+        P->layer_of[id] = L;
+    }
     const size_t bytes = L->expert_stride * static_cast<size_t>(L->cfg.E);
     void *host = nullptr;
     cudaError_t e = cudaHostAlloc(&host, bytes, cudaHostAllocDefault);
@@ -172,42 +194,121 @@ void paged_detach(moe_layer *L) {
             s.layer = -1;
             s.expert = -1;
             s.last_use = -1;
+            s.fetched = false;
         }
+    const size_t id = static_cast<size_t>(L->layer_id);
+    if (id < P->layer_of.size() && P->layer_of[id] == L) P->layer_of[id] = nullptr;
 }
 
 // ---- forward ---------------------------------------------------------------------------
 namespace {
 
-// Set-associative lookup; on a miss the chosen way is re-tagged.  Returns the
-// slot index; *hit tells whether the expert was resident.
-int pool_acquire(moe_pool *P, int layer, int expert, bool *hit) {
-    const int set = layer % P->n_index;
-    const int base = set * P->ways;
-    int found = -1;
-    for (int w = 0; w < P->ways; ++w)
-        if (P->slot[base + w].layer == layer && P->slot[base + w].expert == expert) found = w;
-    *hit = found >= 0;
-    if (found < 0) {
-        int victim = -1;
-        for (int w = 0; w < P->ways && victim < 0; ++w)
-            if (P->slot[base + w].layer < 0) victim = w;
-        if (victim < 0) {
-            victim = 0;
-            for (int w = 1; w < P->ways; ++w)
-                if (P->slot[base + w].last_use < P->slot[base + victim].last_use) victim = w;
-        }
-        P->slot[base + victim].layer = layer;
-        P->slot[base + victim].expert = expert;
-        found = victim;
-    }
-    P->slot[base + found].last_use = P->clock++;
+enum LogKind { kMiss = 0, kHit = 1, kPrefetch = 2, kPrefetchHit = 3 };
+
+void pool_log(moe_pool *P, int layer, int expert, int kind, int slot) {
     if (P->log.size() + 4 <= 4 * kLogCap) {
         P->log.push_back(layer);
         P->log.push_back(expert);
-        P->log.push_back(*hit ? 1 : 0);
-        P->log.push_back(base + found);
+        P->log.push_back(kind);
+        P->log.push_back(slot);
     }
-    return base + found;
+}
+
+// Way of (layer, expert) in its set, or -1.
+int pool_find(const moe_pool *P, int layer, int expert) {
+    const int base = (layer % P->n_index) * P->ways;
+    for (int w = 0; w < P->ways; ++w)
+        if (P->slot[base + w].layer == layer && P->slot[base + w].expert == expert) return base + w;
+    return -1;
+}
+
+// The way a new entry takes in the set of `layer`: the first empty way, else
+// the least recently used.
+int pool_victim(const moe_pool *P, int layer) {
+    const int base = (layer % P->n_index) * P->ways;
+    for (int w = 0; w < P->ways; ++w)
+        if (P->slot[base + w].layer < 0) return base + w;
+    int victim = base;
+    for (int w = 1; w < P->ways; ++w)
+        if (P->slot[base + w].last_use < P->slot[victim].last_use) victim = base + w;
+    return victim;
+}
+
+// Demand lookup; on a miss the chosen way is re-tagged.  Returns the slot
+// index and the log kind (miss, hit, or first use of a prefetched entry).
+int pool_acquire(moe_pool *P, int layer, int expert, int *kind) {
+    int si = pool_find(P, layer, expert);
+    if (si < 0) {
+        si = pool_victim(P, layer);
+        P->slot[si].layer = layer;
+        P->slot[si].expert = expert;
+        P->slot[si].fetched = false;
+        *kind = kMiss;
+    } else {
+        *kind = P->slot[si].fetched ? kPrefetchHit : kHit;
+        P->slot[si].fetched = false;
+    }
+    P->slot[si].last_use = P->clock++;
+    pool_log(P, layer, expert, *kind, si);
+    return si;
+}
+
+// Copy expert `e` of layer N into slot si on the copy stream, page by page,
+// after the last compute that read the slot; records the slot's ready event.
+// Copy time is attributed to layer L (the caller).
+moe_status_t pool_copy_in(moe_pool *P, moe_layer *L, moe_layer *N, int e, int si) {
+    moe_pool::Slot &slot = P->slot[si];
+    uint8_t *dst = P->slots + static_cast<size_t>(si) * P->slot_bytes;
+    cudaError_t err = cudaSuccess;
+    if (slot.busy_recorded) err = cudaStreamWaitEvent(P->copy_stream, slot.busy, 0);
+    cudaEvent_t c0 = (err == cudaSuccess && L->timing) ? L->get_event() : nullptr;
+    if (c0) err = cudaEventRecord(c0, P->copy_stream);
+    const uint8_t *src = N->pinned_weights + N->expert_stride * static_cast<size_t>(e);
+    for (size_t off = 0; err == cudaSuccess && off < N->expert_stride; off += P->page_bytes) {
+        const size_t n = std::min(P->page_bytes, N->expert_stride - off);
+        err = cudaMemcpyAsync(dst + off, src + off, n, cudaMemcpyHostToDevice, P->copy_stream);
+    }
+    if (err == cudaSuccess) err = cudaEventRecord(slot.ready, P->copy_stream);
+    if (err == cudaSuccess && c0) {
+        cudaEvent_t c1 = L->get_event();
+        if (c1) {
+            err = cudaEventRecord(c1, P->copy_stream);
+            L->pending.push_back({MOE_PHASE_COPY, c0, c1});
+        }
+    }
+    if (err != cudaSuccess) return cuda_fail(err, "expert page copy");
+    L->stats.h2d_bytes += N->expert_stride;
+    return MOE_OK;
+}
+
+// Cross-layer prefetch after layer L's demand lookups: up to P->prefetch of
+// the experts with tokens (most tokens first, ties to the lower id) are
+// brought in for layer L + 1 if it is attached and maps to another set.
+moe_status_t pool_prefetch_next(moe_pool *P, moe_layer *L, const int32_t *counts, int E) {
+    const int nl = L->layer_id + 1;
+    if (P->prefetch <= 0 || nl >= static_cast<int>(P->layer_of.size()) || !P->layer_of[nl]) return MOE_OK;
+    if (nl % P->n_index == L->layer_id % P->n_index) return MOE_OK;  // would evict this layer's experts
+    moe_layer *N = P->layer_of[nl];
+    if (N->cfg.E != E || N->expert_stride > P->slot_bytes) return MOE_OK;
+    std::vector<int> order;
+    for (int e = 0; e < E; ++e)
+        if (counts[e] > 0) order.push_back(e);
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return counts[a] > counts[b]; });
+    if (static_cast<int>(order.size()) > P->prefetch) order.resize(static_cast<size_t>(P->prefetch));
+    for (int e : order) {
+        if (pool_find(P, nl, e) >= 0) continue;
+        const int si = pool_victim(P, nl);
+        moe_pool::Slot &slot = P->slot[si];
+        slot.layer = nl;
+        slot.expert = e;
+        slot.fetched = true;
+        slot.last_use = P->clock++;
+        pool_log(P, nl, e, kPrefetch, si);
+        moe_status_t st = pool_copy_in(P, L, N, e, si);
+        if (st != MOE_OK) return st;
+        L->stats.prefetch_copies += 1;
+    }
+    return MOE_OK;
 }
 
 }  // namespace
@@ -248,32 +349,18 @@ moe_status_t paged_forward(moe_layer *L, const void *x, const moe_routing_t *r, 
     bool first = true;
     for (int e = 0; e < c.E; ++e) {
         if (L->counts_host[e] <= 0) continue;
-        bool hit = false;
-        const int si = pool_acquire(P, L->layer_id, e, &hit);
+        int kind = kMiss;
+        const int si = pool_acquire(P, L->layer_id, e, &kind);
         moe_pool::Slot &slot = P->slot[si];
         uint8_t *dst = P->slots + static_cast<size_t>(si) * P->slot_bytes;
-        if (!hit) {
+        if (kind == kMiss) {
             // never overwrite weights a kernel may still be reading
-            if (slot.busy_recorded) PG_TRY(cudaStreamWaitEvent(P->copy_stream, slot.busy, 0));
-            cudaEvent_t c0 = L->timing ? L->get_event() : nullptr;
-            if (c0) PG_TRY(cudaEventRecord(c0, P->copy_stream));
-            const uint8_t *src = L->pinned_weights + L->expert_stride * static_cast<size_t>(e);
-            for (size_t off = 0; off < L->expert_stride; off += P->page_bytes) {
-                const size_t n = std::min(P->page_bytes, L->expert_stride - off);
-                PG_TRY(cudaMemcpyAsync(dst + off, src + off, n, cudaMemcpyHostToDevice, P->copy_stream));
-            }
-            PG_TRY(cudaEventRecord(slot.ready, P->copy_stream));
-            if (c0) {
-                cudaEvent_t c1 = L->get_event();
-                if (c1) {
-                    PG_TRY(cudaEventRecord(c1, P->copy_stream));
-                    L->pending.push_back({MOE_PHASE_COPY, c0, c1});
-                }
-            }
+            moe_status_t cs = pool_copy_in(P, L, L, e, si);
+            if (cs != MOE_OK) return cs;
             L->stats.slot_misses += 1;
-            L->stats.h2d_bytes += L->expert_stride;
         } else {
             L->stats.slot_hits += 1;
+            if (kind == kPrefetchHit) L->stats.prefetch_hits += 1;
         }
         PG_TRY(cudaStreamWaitEvent(s, slot.ready, 0));
         // this expert's stored matrices now live in the slot
@@ -308,6 +395,8 @@ moe_status_t paged_forward(moe_layer *L, const void *x, const moe_routing_t *r, 
         st = run_combine(L, r, splits, nrows_cap, y, s);
         if (st != MOE_OK) return st;
     }
+    st = pool_prefetch_next(P, L, L->counts_host, c.E);
+    if (st != MOE_OK) return st;
     PG_TRY(cudaEventRecord(L->fwd_t1, s));
     L->last_stream = s;
     L->launched = true;

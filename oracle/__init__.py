@@ -41,6 +41,8 @@ PINS = {
     "expert": "|O| closed form (op counter); dense-MLP numpy reduction; one-hot entries",
     "layer": "identical experts make y routing-independent; E=1,k=1 dense MLP",
     "cache_replay": "slot-count formulas of the expert-cache article; hand traces",
+    "cache_replay_calls": "equals cache_replay with prefetch off; hand traces with prefetch; "
+                          "closed-form hit counts for repeated expert sets",
 }
 
 _lib = None
@@ -61,9 +63,11 @@ def lib():
         L.moe_oracle_layer.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, i32,
                                        vp, vp, vp, i32, vp, dp, vp, i32, dp, vp, i32]
         L.moe_oracle_cache_replay.argtypes = [i32, i32, i32, vp, vp, vp, vp]
+        L.moe_oracle_cache_replay_calls.argtypes = [i32, i32, i32, vp, i32, vp, i32, i32, vp, vp,
+                                                    vp, vp, i32, vp]
         for f in (L.moe_oracle_router_logits, L.moe_oracle_topk, L.moe_oracle_permute,
                   L.moe_oracle_quantize_cols, L.moe_oracle_expert, L.moe_oracle_layer,
-                  L.moe_oracle_cache_replay):
+                  L.moe_oracle_cache_replay, L.moe_oracle_cache_replay_calls):
             f.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -222,6 +226,30 @@ def cache_replay(n_index, n_way, layers, experts):
     _check(lib().moe_oracle_cache_replay(n_index, n_way, n, _ptr(layers), _ptr(experts),
                                          _ptr(hit), _ptr(slot)), "cache_replay")
     return hit, slot
+
+
+MISS, HIT, PREFETCH, PREFETCH_HIT = 0, 1, 2, 3
+
+
+def cache_replay_calls(n_index, n_way, call_layers, counts, n_layers, n_prefetch):
+    """Replay whole layer calls (layer id, per-expert token counts [E]) through
+    the N-index x M-way LRU cache, prefetching up to n_prefetch of each call's
+    experts for the next layer.
+
+    Returns (layer, expert, kind, slot) int32 arrays, one entry per lookup or
+    prefetch insert; kind is MISS, HIT, PREFETCH or PREFETCH_HIT."""
+    call_layers = _c(np.asarray(call_layers, np.int32))
+    counts = _c(np.asarray(counts, np.int32))
+    n_calls = len(call_layers)
+    E = counts.shape[1] if counts.ndim == 2 and n_calls else 1
+    cap = max(1, int((counts > 0).sum()) + n_calls * max(n_prefetch, 0))
+    out = [np.empty(cap, np.int32) for _ in range(4)]
+    n = ctypes.c_int(0)
+    _check(lib().moe_oracle_cache_replay_calls(n_index, n_way, n_calls, _ptr(call_layers), E,
+                                               _ptr(counts), n_layers, n_prefetch,
+                                               *[_ptr(o) for o in out], cap, ctypes.byref(n)),
+           "cache_replay_calls")
+    return tuple(o[:n.value] for o in out)
 
 
 def forward(x, w_router, w1, w2, w3, k, kind, bias=None, scales=None, tokens=None):

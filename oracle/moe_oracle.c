@@ -431,3 +431,143 @@ int moe_oracle_cache_replay(int n_index, int n_way, int n_queries,
     free(last_use);
     return OR_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* The same cache driven by whole layer calls, with optional cross-layer
+ * prefetch: experts chosen in layer l are fetched for layer l + 1 ahead of
+ * its call (HARMOEny write-up, part 3.2: prefetch the next layer's experts
+ * during the current layer's compute; expert-cache article, section 2.1:
+ * consecutive layers often pick the same experts).
+ *
+ * Call c is layer call_layer[c] with per-expert token counts
+ * counts[c * E .. c * E + E - 1].  For each call:
+ *   1. demand: every expert with tokens, in ascending id, is looked up in set
+ *      layer mod N; a miss takes an empty way (lowest index) or the least
+ *      recently used way; every lookup makes the way most recently used;
+ *   2. prefetch (n_prefetch > 0, layer + 1 < n_layers, and layer + 1 maps to a
+ *      different set): the n_prefetch experts of this call with the most
+ *      tokens (ties to the lower id) are looked up for layer + 1; one that is
+ *      not resident is inserted as in a miss and becomes most recently used;
+ *      one that is resident is left untouched.
+ * Log entry i: layer_out, expert_out, kind_out (0 demand miss, 1 demand hit,
+ * 2 prefetch insert, 3 demand hit on a prefetched entry not used before) and
+ * slot_out (set * M + way).  Writes at most max_out entries; *n_out receives
+ * the number of entries the replay produced. */
+int moe_oracle_cache_replay_calls(int n_index, int n_way, int n_calls, const int32_t *call_layer,
+                                  int E, const int32_t *counts, int n_layers, int n_prefetch,
+                                  int32_t *layer_out, int32_t *expert_out, int32_t *kind_out,
+                                  int32_t *slot_out, int max_out, int *n_out) {
+    if (n_index <= 0 || n_way <= 0 || n_calls < 0 || E <= 0 || n_prefetch < 0 || !n_out ||
+        (n_calls > 0 && (!call_layer || !counts)) || max_out < 0)
+        return OR_BAD_ARG;
+    size_t n_slots = (size_t)n_index * n_way;
+    long long *tag_layer = (long long *)malloc(sizeof(long long) * n_slots);
+    long long *tag_expert = (long long *)malloc(sizeof(long long) * n_slots);
+    long long *last_use = (long long *)malloc(sizeof(long long) * n_slots);
+    int *fetched = (int *)malloc(sizeof(int) * n_slots); /* inserted by prefetch, unused */
+    int *order = (int *)malloc(sizeof(int) * (size_t)E);
+    if (!tag_layer || !tag_expert || !last_use || !fetched || !order) {
+        free(tag_layer);
+        free(tag_expert);
+        free(last_use);
+        free(fetched);
+        free(order);
+        return OR_NOMEM;
+    }
+    for (size_t s = 0; s < n_slots; ++s) {
+        tag_layer[s] = -1;
+        tag_expert[s] = -1;
+        last_use[s] = -1;
+        fetched[s] = 0;
+    }
+    long long clock = 0;
+    int n = 0;
+#define OR_LOG(L_, E_, K_, S_)                              \
+    do {                                                    \
+        if (n < max_out) {                                  \
+            if (layer_out) layer_out[n] = (int32_t)(L_);    \
+            if (expert_out) expert_out[n] = (int32_t)(E_);  \
+            if (kind_out) kind_out[n] = (int32_t)(K_);      \
+            if (slot_out) slot_out[n] = (int32_t)(S_);      \
+        }                                                   \
+        ++n;                                                \
+    } while (0)
+    for (int c = 0; c < n_calls; ++c) {
+        const int l = call_layer[c];
+        const int32_t *cnt = counts + (size_t)c * E;
+        /* 1. demand lookups */
+        for (int e = 0; e < E; ++e) {
+            if (cnt[e] <= 0) continue;
+            size_t base = (size_t)(l % n_index) * n_way;
+            int found = -1;
+            for (int w = 0; w < n_way; ++w)
+                if (tag_layer[base + w] == l && tag_expert[base + w] == e) found = w;
+            int kind;
+            if (found < 0) {
+                int victim = -1;
+                for (int w = 0; w < n_way && victim < 0; ++w)
+                    if (tag_layer[base + w] < 0) victim = w;
+                if (victim < 0) {
+                    victim = 0;
+                    for (int w = 1; w < n_way; ++w)
+                        if (last_use[base + w] < last_use[base + victim]) victim = w;
+                }
+                tag_layer[base + victim] = l;
+                tag_expert[base + victim] = e;
+                fetched[base + victim] = 0;
+                found = victim;
+                kind = 0;
+            } else {
+                kind = fetched[base + found] ? 3 : 1;
+                fetched[base + found] = 0;
+            }
+            last_use[base + found] = clock++;
+            OR_LOG(l, e, kind, base + found);
+        }
+        /* 2. prefetch for the next layer */
+        const int nl = l + 1;
+        if (n_prefetch == 0 || nl >= n_layers || (nl % n_index) == (l % n_index)) continue;
+        int n_cand = 0;
+        for (int e = 0; e < E; ++e)
+            if (cnt[e] > 0) order[n_cand++] = e;
+        /* by count descending, ties to the lower id (insertion sort: stable) */
+        for (int i = 1; i < n_cand; ++i) {
+            int v = order[i], j = i - 1;
+            while (j >= 0 && cnt[order[j]] < cnt[v]) {
+                order[j + 1] = order[j];
+                --j;
+            }
+            order[j + 1] = v;
+        }
+        if (n_cand > n_prefetch) n_cand = n_prefetch;
+        size_t base = (size_t)(nl % n_index) * n_way;
+        for (int i = 0; i < n_cand; ++i) {
+            const int e = order[i];
+            int found = -1;
+            for (int w = 0; w < n_way; ++w)
+                if (tag_layer[base + w] == nl && tag_expert[base + w] == e) found = w;
+            if (found >= 0) continue;
+            int victim = -1;
+            for (int w = 0; w < n_way && victim < 0; ++w)
+                if (tag_layer[base + w] < 0) victim = w;
+            if (victim < 0) {
+                victim = 0;
+                for (int w = 1; w < n_way; ++w)
+                    if (last_use[base + w] < last_use[base + victim]) victim = w;
+            }
+            tag_layer[base + victim] = nl;
+            tag_expert[base + victim] = e;
+            fetched[base + victim] = 1;
+            last_use[base + victim] = clock++;
+            OR_LOG(nl, e, 2, base + victim);
+        }
+    }
+#undef OR_LOG
+    *n_out = n;
+    free(tag_layer);
+    free(tag_expert);
+    free(last_use);
+    free(fetched);
+    free(order);
+    return OR_OK;
+}

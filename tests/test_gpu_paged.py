@@ -27,9 +27,11 @@ def _expert_bytes(shape):
 
 
 def _run_pair(shape, n_layers, sets, ways, schedule, page_bytes=0, regime=moe.REGIME_AUTO,
-              topk_trace=None):
+              topk_trace=None, prefetch=0, counts_out=None):
     eb = _expert_bytes(shape)
     pool = moe.moe_pool_create(eb * sets * ways, eb, ways, page_bytes)
+    if prefetch:
+        moe.moe_pool_set_prefetch(pool, prefetch)
     layers = [wl.make_layer(shape, seed=200 + i) for i in range(n_layers)]
     max_t = max(T for _, T in schedule)
     paged = [moe.MoELayer(layers[i], max_t, pool=pool, layer_id=i) for i in range(n_layers)]
@@ -48,6 +50,8 @@ def _run_pair(shape, n_layers, sets, ways, schedule, page_bytes=0, regime=moe.RE
         np.testing.assert_array_equal(rp.y_np, rr.y_np)
         assert paged[li].sync_check()[0] == moe.MOE_OK
         queries += [(li, e) for e in range(shape.E) if rp.counts[e] > 0]
+        if counts_out is not None:
+            counts_out.append(rp.counts.copy())
     log = moe.moe_pool_query_log(pool)
     stats = [ml.stats() for ml in paged]
     for ml in paged + resident:
@@ -151,4 +155,79 @@ def test_paged_step_time_within_overlap_bounds():
     assert 0.9 * max(copy, compute) <= wall
     for ml in layers:
         ml.close()
+    moe.moe_pool_destroy(pool)
+
+
+def _check_calls(schedule, counts, log, sets, ways, n_layers, prefetch, stats):
+    lay, exp_, kind, slot = oracle.cache_replay_calls(sets, ways, [li for li, _ in schedule],
+                                                      np.array(counts), n_layers, prefetch)
+    np.testing.assert_array_equal(log[0], lay)
+    np.testing.assert_array_equal(log[1], exp_)
+    np.testing.assert_array_equal(log[2], kind)
+    np.testing.assert_array_equal(log[3], slot)
+    for li in range(n_layers):
+        mine = lay == li
+        assert int(stats[li].prefetch_hits) == int(((kind == oracle.PREFETCH_HIT) & mine).sum())
+        assert int(stats[li].slot_misses) == int(((kind == oracle.MISS) & mine).sum())
+    # a prefetch insert for layer l + 1 is issued (and counted) by layer l
+    issued = sum(int(st.prefetch_copies) for st in stats)
+    assert issued == int((kind == oracle.PREFETCH).sum())
+    return kind
+
+
+def test_cross_layer_prefetch_matches_oracle_and_resident():
+    """Layers reuse their predecessor's experts: prefetched experts serve the
+    next layer's lookups (kind 3), outputs stay bit-identical to resident layers
+    and the pool log equals the oracle's call replay."""
+    sets, ways, n_layers, T = 3, 2, 4, 2
+    trace, schedule = [], []
+    base = [np.array([[0, 1], [1, 0]], np.int32), np.array([[2, 3], [3, 2]], np.int32)]
+    for step in range(3):
+        for li in range(n_layers):
+            ids = base[(li // 2 + step) % 2]  # pairs of consecutive layers share experts
+            trace.append((ids, np.full((T, 2), 0.5, np.float32)))
+            schedule.append((li, T))
+    counts = []
+    eb, _, log, stats = _run_pair(SHAPE, n_layers, sets, ways, schedule, topk_trace=trace,
+                                  prefetch=2, counts_out=counts)
+    kind = _check_calls(schedule, counts, log, sets, ways, n_layers, 2, stats)
+    assert (kind == oracle.PREFETCH_HIT).sum() > 0
+
+
+@pytest.mark.parametrize("prefetch", [1, 8])
+def test_cross_layer_prefetch_random_trace(prefetch):
+    """A seeded decode trace (copy the previous layer's choice with p = 0.44,
+    else the previous step's, else fresh) through 6 layers and 4 sets x 2 ways."""
+    sets, ways, n_layers, T, steps = 4, 2, 6, 3, 3
+    tr = wl.make_topk_trace(SHAPE.E, SHAPE.k, steps, n_layers, T, seed=7)
+    trace, schedule = [], []
+    for st_ in range(steps):
+        for li in range(n_layers):
+            trace.append((tr[0][st_, li], tr[1][st_, li]))
+            schedule.append((li, T))
+    counts = []
+    _, _, log, stats = _run_pair(SHAPE, n_layers, sets, ways, schedule, topk_trace=trace,
+                                 prefetch=prefetch, counts_out=counts)
+    _check_calls(schedule, counts, log, sets, ways, n_layers, prefetch, stats)
+
+
+def test_prefetch_count_is_validated():
+    eb = _expert_bytes(SHAPE)
+    pool = moe.moe_pool_create(eb * 2, eb, 1, 0)
+    with pytest.raises(moe.MoeError):
+        moe.moe_pool_set_prefetch(pool, -1)
+    moe.moe_pool_set_prefetch(pool, 0)
+    moe.moe_pool_destroy(pool)
+
+
+def test_duplicate_layer_id_in_a_pool_is_rejected():
+    eb = _expert_bytes(SHAPE)
+    pool = moe.moe_pool_create(eb * 4, eb, 2, 0)
+    a = moe.MoELayer(wl.make_layer(SHAPE, seed=5), 4, pool=pool, layer_id=3)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.MoELayer(wl.make_layer(SHAPE, seed=6), 4, pool=pool, layer_id=3)
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+    a.close()
+    b = moe.MoELayer(wl.make_layer(SHAPE, seed=6), 4, pool=pool, layer_id=3)  # id free again
+    b.close()
     moe.moe_pool_destroy(pool)

@@ -345,3 +345,103 @@ def test_cache_replay_matches_independent_model():
         hit, slot = oracle.cache_replay(n_index, n_way, layers, experts)
         h2, s2 = _lru_model(n_index, n_way, list(layers), list(experts))
         assert list(hit) == h2 and list(slot) == s2
+
+
+# --------------------------------------------------------------------------
+# the cache driven by layer calls, with cross-layer prefetch
+def test_cache_calls_without_prefetch_equal_query_replay():
+    """Prefetch off: the call replay is the query replay of each call's experts
+    in ascending id (the pinned function above)."""
+    r = _rng(23)
+    E, n_calls = 8, 400
+    layers = r.integers(0, 20, size=n_calls)
+    counts = r.integers(0, 3, size=(n_calls, E)) * (r.random((n_calls, E)) < 0.4)
+    ql, qe = [], []
+    for l, c in zip(layers, counts):
+        for e in range(E):
+            if c[e] > 0:
+                ql.append(l)
+                qe.append(e)
+    for n_index, n_way in [(12, 4), (5, 2), (1, 3)]:
+        lay, exp_, kind, slot = oracle.cache_replay_calls(n_index, n_way, layers, counts, 20, 0)
+        hit, slot2 = oracle.cache_replay(n_index, n_way, ql, qe)
+        assert list(lay) == ql and list(exp_) == qe
+        assert list(kind) == list(hit) and list(slot) == list(slot2)
+
+
+def test_cache_calls_hand_trace_prefetch_used():
+    # 2 sets x 2 ways, layers 0 and 1, prefetch 2.  Call 0 (layer 0, experts
+    # 0 and 1) misses twice into set 0, then prefetches (1,0) and (1,1) into
+    # set 1; call 1 (layer 1, same experts) finds both prefetched (kind 3);
+    # call 2 repeats layer 1: plain hits.
+    counts = np.array([[2, 1, 0], [1, 1, 0], [1, 1, 0]])
+    lay, exp_, kind, slot = oracle.cache_replay_calls(2, 2, [0, 1, 1], counts, 2, 2)
+    assert list(lay) == [0, 0, 1, 1, 1, 1, 1, 1]
+    assert list(exp_) == [0, 1, 0, 1, 0, 1, 0, 1]
+    assert list(kind) == [0, 0, 2, 2, 3, 3, 1, 1]
+    assert list(slot) == [0, 1, 2, 3, 2, 3, 2, 3]
+
+
+def test_cache_calls_hand_trace_prefetch_evicted():
+    # 2 sets x 2 ways, 3 layers, prefetch 2.
+    # call 0, layer 0, counts (1,0,2): (0,0) miss w0, (0,2) miss w1; prefetch for
+    #   layer 1 by count: e2 then e0 -> set 1 w0, w1.
+    # call 1, layer 1, counts (0,3,1): (1,1) miss evicts LRU (1,2) -> slot 2;
+    #   (1,2) now misses, evicts LRU (1,0) -> slot 3; prefetch for layer 2:
+    #   e1 (3 tokens) then e2 -> set 0, evicting (0,0) then (0,2).
+    # call 2, layer 0, counts (1,1,0): both miss (evicting (2,1), (2,2));
+    #   prefetch e0, e1 (tie, lower id first) for layer 1: (1,0) evicts (1,1)
+    #   at slot 2, then (1,1) is gone and evicts (1,2) at slot 3.
+    counts = np.array([[1, 0, 2], [0, 3, 1], [1, 1, 0]])
+    lay, exp_, kind, slot = oracle.cache_replay_calls(2, 2, [0, 1, 0], counts, 3, 2)
+    assert list(lay) == [0, 0, 1, 1, 1, 1, 2, 2, 0, 0, 1, 1]
+    assert list(exp_) == [0, 2, 2, 0, 1, 2, 1, 2, 0, 1, 0, 1]
+    assert list(kind) == [0, 0, 2, 2, 0, 0, 2, 2, 0, 0, 2, 2]
+    assert list(slot) == [0, 1, 2, 3, 2, 3, 0, 1, 0, 1, 2, 3]
+
+
+@pytest.mark.parametrize("a,L,S", [(2, 6, 4), (3, 4, 3), (1, 8, 2)])
+def test_cache_calls_closed_form_repeated_expert_set(a, L, S):
+    """Every layer picks the same a experts at every step, each layer owns a
+    set of at least a ways.  Without prefetch: L a misses then hits.  With
+    prefetch >= a: only layer 0 misses at step 0; layers 1..L-1 find their a
+    experts prefetched (kind 3); everything after is a plain hit; (L-1) a
+    prefetch inserts in total."""
+    E = 8
+    counts = np.zeros((S * L, E), np.int32)
+    counts[:, :a] = np.arange(a, 0, -1)
+    layers = np.tile(np.arange(L), S)
+    _, _, k0, _ = oracle.cache_replay_calls(L, a, layers, counts, L, 0)
+    assert (k0 == 0).sum() == L * a and (k0 == 1).sum() == (S - 1) * L * a
+    _, _, k1, _ = oracle.cache_replay_calls(L, a, layers, counts, L, a)
+    assert (k1 == 0).sum() == a
+    assert (k1 == 3).sum() == (L - 1) * a
+    assert (k1 == 2).sum() == (L - 1) * a
+    assert (k1 == 1).sum() == (S - 1) * L * a
+
+
+def test_cache_calls_prefetch_invariants():
+    r = _rng(29)
+    E, n_layers = 8, 32
+    n_calls = 32 * 20
+    layers = np.tile(np.arange(n_layers), 20)
+    counts = (r.random((n_calls, E)) < 0.3) * r.integers(1, 5, size=(n_calls, E))
+    for n_index, n_way, pf in [(12, 4, 2), (12, 4, 8), (7, 2, 1), (1, 4, 4)]:
+        lay, exp_, kind, slot = oracle.cache_replay_calls(n_index, n_way, layers, counts,
+                                                          n_layers, pf)
+        assert np.all(slot // n_way == lay % n_index)  # every entry in its layer's set
+        if n_index == 1:
+            assert not np.any(kind >= 2)  # the next layer shares the set: no prefetch
+        # a first use of a prefetched entry follows a prefetch insert of the same
+        # (layer, expert) into the same slot
+        last = {}
+        for l, e, k, s in zip(lay, exp_, kind, slot):
+            if k == 2:
+                last[(l, e)] = s
+            elif k == 3:
+                assert last.get((l, e)) == s
+                del last[(l, e)]
+        # prefetch inserts per call never exceed the prefetch count
+        demand = kind != 2
+        assert (kind == 2).sum() <= pf * n_calls
+        assert demand.sum() == int((counts > 0).sum())
