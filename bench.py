@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--tokens", default="1,4,16,64",
                     help="decode batches per step (profiling runs use one)")
     ap.add_argument("--copies", type=int, default=2, help="weight copies that alternate")
+    ap.add_argument("--pair-tiles", type=int, default=0, choices=[0, 1],
+                    help="256-token tensor-core tiles on CTA pairs (1) or one CTA each (0, default)")
     ap.add_argument("--graph", action="store_true",
                     help="capture one step (all route + forward calls) in a CUDA graph and "
                          "time its replays")
@@ -289,6 +291,8 @@ def run_ours(args, world, rank, local):
     layer, xs_np = make_inputs(shape, args.seed + rank, f"cuda:{local}")
     max_t = max(TOKENS)
     copies = [moe.MoELayer(layer, max_t) for _ in range(max(args.copies, 1))]
+    for c in copies:
+        c.set_pair_tiles(bool(args.pair_tiles))
     dev = torch.device("cuda", local)
     xs = {T: torch.from_numpy(xs_np[T].view(np.int16).copy()).view(torch.bfloat16).to(dev)
           for T in TOKENS}

@@ -27,7 +27,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_OOM, MOE_ERR_CUDA, \
     MOE_ERR_TIMEOUT, MOE_ERR_INTERNAL = range(7)
 MOE_F32, MOE_BF16, MOE_I8 = 0, 1, 2
 MOE_EXPERT_RELU2, MOE_EXPERT_SWIGLU = 0, 1
-MOE_OPT_REGIME, MOE_OPT_TIMING = 1, 2
+MOE_OPT_REGIME, MOE_OPT_TIMING, MOE_OPT_PAIR_TILES = 1, 2, 3
 REGIME_AUTO, REGIME_DECODE, REGIME_BATCH = 0, 1, 2
 
 DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16, "i8": MOE_I8}
@@ -345,6 +345,9 @@ class MoELayer:
 
     def set_timing(self, on: bool):
         moe_layer_set_option(self.handle, MOE_OPT_TIMING, int(on))
+
+    def set_pair_tiles(self, on: bool):
+        moe_layer_set_option(self.handle, MOE_OPT_PAIR_TILES, int(on))
 
     def timings(self, reset=True):
         return moe_layer_timings(self.handle, reset)

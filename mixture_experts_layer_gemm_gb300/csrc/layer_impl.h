@@ -14,6 +14,7 @@ struct moe_layer {
     int device = -1;
     int num_sms = 0;
     int regime = 0;  // MOE_OPT_REGIME
+    bool pair_tiles = false;  // MOE_OPT_PAIR_TILES
 
     // weights (resident copy, or unused for paged layers)
     float *wrt = nullptr;      // router [E x m] fp32

@@ -622,12 +622,26 @@ static moe_status_t run_experts_tc(moe_layer_t *L, ExpertArgs &a, int *splits_ou
     } else {
         a.n_rows_cap = rows;
     }
+    // 256-token tiles run on CTA pairs (half the shared-memory traffic per
+    // SM) when both matrices come in 256-row pair blocks and nothing is split
+    const bool pair = !i8 && L->pair_tiles && N == 256 && s_up == 1 && s_down == 1 &&
+                      rows_up % 256 == 0 && c.m % 256 == 0;
     const CUtensorMap *xm = nullptr, *hm = nullptr;
-    moe_status_t st = tc_maps(L, N, &xm, &hm);
+    moe_status_t st = tc_maps(L, pair ? N / 2 : N, &xm, &hm);
     if (st != MOE_OK) return st;
     st = launch_phase(L, MOE_PHASE_GATHER, s, "gather_rows", [&] {
         return launch_gather_rows(a.x, a.gather, rows, a.k, c.m, L->x_perm, L->err_word, s);
     });
+    if (pair) {
+        if (st == MOE_OK)
+            st = launch_phase(L, MOE_PHASE_UP, s, "tc2_up",
+                              [&] { return launch_tc2_up(a, gated, *xm, L->num_sms, s); });
+        if (st == MOE_OK)
+            st = launch_phase(L, MOE_PHASE_DOWN, s, "tc2_down",
+                              [&] { return launch_tc2_down(a, *hm, L->num_sms, s); });
+        *splits_out = 1;
+        return st;
+    }
     if (st == MOE_OK)
         st = launch_phase(L, MOE_PHASE_UP, s, "tc_up", [&] {
             return i8 ? launch_tc_i8_up(a, gated, s_up, N, *xm, L->num_sms, s)
@@ -759,6 +773,11 @@ extern "C" moe_status_t moe_layer_set_option(moe_layer_t *L, moe_option_t opt, i
     if (opt == MOE_OPT_TIMING) {
         if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "timing must be 0 or 1");
         L->timing = value != 0;
+        return MOE_OK;
+    }
+    if (opt == MOE_OPT_PAIR_TILES) {
+        if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "pair tiles must be 0 or 1");
+        L->pair_tiles = value != 0;
         return MOE_OK;
     }
     return fail(MOE_ERR_INVALID_ARG, "unknown option %d", int(opt));

@@ -168,6 +168,48 @@ def test_relu_bf16_tensor_core(T):
     run_and_check(RELU_BF16, T, seed=28, regime=moe.REGIME_BATCH)
 
 
+@pytest.mark.parametrize("shape,T", [(SWIGLU_BF16, 700), (SWIGLU_BF16, 1500), (RELU_BF16, 640)])
+def test_pair_tiles_match_single_cta_and_oracle(shape, T):
+    """256-token tiles on CTA pairs (tcgen05 cta_group::2) against one CTA per
+    128 x 256 tile: the same products summed in fp32, so the outputs agree to
+    rounding, and both meet the oracle bar."""
+    layer = get_layer(shape, seed=31)
+    x = wl.make_tokens(shape, T, seed=32)
+    ys = []
+    for pair in (True, False):
+        ml = moe.MoELayer(layer, T, with_logits=True)
+        ml.set_pair_tiles(pair)
+        run = Run(ml, x)
+        assert ml.sync_check()[0] == moe.MOE_OK
+        ids, w = check_routing(run, layer, x)
+        rel, _ = max_token_rel_l2(run.y_np, oracle_y(layer, x, ids, w))
+        assert rel <= TOL["bf16"], (pair, rel)
+        ys.append(f64(run.y_np))
+        ml.close()
+    d = np.linalg.norm(ys[0] - ys[1], axis=1) / np.maximum(np.linalg.norm(ys[1], axis=1), 1e-30)
+    assert d.max() <= 5e-3
+
+
+def test_pair_tiles_ragged_segments():
+    """Expert 0 takes every token (600 = 2 x 256 + 88) and the others ~86 each:
+    full pair tiles, a last tile of 88 tokens (halves of 48 after rounding to
+    32) and single short tiles."""
+    shape = SWIGLU_BF16
+    layer = get_layer(shape, seed=33)
+    T = 600
+    x = wl.make_tokens(shape, T, seed=34)
+    ids = np.stack([np.zeros(T, np.int32), 1 + (np.arange(T) % 7)], axis=1).astype(np.int32)
+    w = np.tile(np.array([[0.625, 0.375]], np.float32), (T, 1))
+    ml = moe.MoELayer(layer, T)
+    ml.set_regime(moe.REGIME_BATCH)
+    run = Run(ml, x, routing="topk", ids=ids, w=w)
+    assert ml.sync_check()[0] == moe.MOE_OK
+    assert run.counts[0] == T
+    rel, _ = max_token_rel_l2(run.y_np, oracle_y(layer, x, ids, w.astype(np.float64)))
+    assert rel <= TOL["bf16"], rel
+    ml.close()
+
+
 def test_zipf_batch_auto_regime():
     """A skewed batch with more than the decode row cap: the automatic choice
     is the tensor-core path, with hot and cold experts of very uneven size."""
