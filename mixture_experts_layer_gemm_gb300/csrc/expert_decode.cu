@@ -20,8 +20,8 @@
 //      covers one 512-byte atom without bank conflicts.
 // GB300-specific design:
 //   - one producer thread streams each unit's 16 KB weight stages from HBM
-//     with bulk asynchronous copies (the TMA engine) into a 6-stage
-//     shared-memory ring guarded by mbarriers, so up to 96 KB per SM are in
+//     with bulk asynchronous copies (the TMA engine) into an 8-stage
+//     shared-memory ring guarded by mbarriers, so up to 128 KB per SM are in
 //     flight whatever the register budget;
 //   - the per-warp dot products run on the warp-level tensor-core MMA
 //     (m16n8k16, bf16 in, fp32 accumulate) with the tokens on the N side:
@@ -47,7 +47,7 @@ namespace {
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;  // + one producer warp
-constexpr int kStages = 6;
+constexpr int kStages = 8;  // 128 KB of weights in flight per SM
 constexpr int kBlocksPerStage = 8;
 constexpr int kStageBytes = kBlocksPerStage * kBlockBytes;  // 16 KB
 constexpr int kRowsPerUnit = 16;
