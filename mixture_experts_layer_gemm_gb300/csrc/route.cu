@@ -68,6 +68,57 @@ struct PermuteSmem {
     int warp_cnt[32][kMaxExperts];
 };
 
+// The same stable counting sort for at most 32 (token, slot) pairs, by one
+// warp and without block barriers (decode batches): lane i holds pair i; the
+// lanes with equal expert ids find each other with a match, a pair's rank
+// among them is the number of lower lanes with its id (stable by i); lanes e
+// and e + 32 count expert e and e + 32 and scan the counts.
+constexpr int kPermuteWarpMax = 32;
+__device__ void permute_warp(const PermuteArgs &a, int lane) {
+    const int n = a.T * a.k;  // <= kPermuteWarpMax
+    int id = -1;
+    if (lane < n) {
+        id = __ldcg(a.ids + lane);
+        if (id < 0 || id >= a.E) id = 0;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, id);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    int c0 = 0, c1 = 0;  // pairs choosing expert lane, lane + 32
+    for (int j = 0; j < n; ++j) {
+        const int idj = __shfl_sync(0xffffffffu, id, j);
+        c0 += idj == lane;
+        c1 += idj == lane + 32;
+    }
+    int s0 = c0, s1 = c1;  // inclusive scans over the lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v0 = __shfl_up_sync(0xffffffffu, s0, o);
+        const int v1 = __shfl_up_sync(0xffffffffu, s1, o);
+        if (lane >= o) {
+            s0 += v0;
+            s1 += v1;
+        }
+    }
+    const int total0 = __shfl_sync(0xffffffffu, s0, 31);
+    const int excl0 = s0 - c0, excl1 = total0 + s1 - c1;
+    if (lane < a.E) {
+        a.counts[lane] = c0;
+        a.offsets[lane] = excl0;
+    }
+    if (lane + 32 < a.E) {
+        a.counts[lane + 32] = c1;
+        a.offsets[lane + 32] = excl1;
+    }
+    if (lane == 0) a.offsets[a.E] = n;
+    const int b0 = __shfl_sync(0xffffffffu, excl0, id & 31);
+    const int b1 = __shfl_sync(0xffffffffu, excl1, id & 31);
+    if (lane < n) {
+        const int pos = (id < 32 ? b0 : b1) + rank;
+        a.gather[pos] = lane;
+        a.scatter[lane] = pos;
+    }
+}
+
 __device__ void permute_block(const PermuteArgs &a, PermuteSmem &sm) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nthreads = blockDim.x;
@@ -375,6 +426,16 @@ __global__ void __launch_bounds__(router_warps<EMAX>() * 32) router_mma_kernel(R
                 a.w[static_cast<size_t>(tok) * a.k + j] = wts[j];
             }
     }
+    if (gridDim.x == 1) {
+        // the whole batch is in this CTA: no ticket; one warp permutes small batches
+        __syncthreads();
+        if (pa.T * pa.k <= kPermuteWarpMax) {
+            if (warp == 0) permute_warp(pa, lane);
+        } else {
+            permute_block(pa, psm);
+        }
+        return;
+    }
     __threadfence();
     __syncthreads();
     if (tid == 0) {
@@ -442,6 +503,10 @@ __global__ void __launch_bounds__(1024) permute_kernel(PermuteArgs a) {
     pdl_wait();
     pdl_trigger();
     __shared__ PermuteSmem psm;
+    if (a.T * a.k <= kPermuteWarpMax) {
+        if (threadIdx.x < 32) permute_warp(a, threadIdx.x);
+        return;
+    }
     permute_block(a, psm);
 }
 
