@@ -47,8 +47,8 @@ def parse():
     ap.add_argument("--tokens", default="1,4,16,64",
                     help="decode batches per step (profiling runs use one)")
     ap.add_argument("--copies", type=int, default=2, help="weight copies that alternate")
-    ap.add_argument("--pair-tiles", type=int, default=0, choices=[0, 1],
-                    help="256-token tensor-core tiles on CTA pairs (1) or one CTA each (0, default)")
+    ap.add_argument("--pair-tiles", type=int, default=1, choices=[0, 1],
+                    help="up-projection 256-token tiles on CTA pairs (1, default) or one CTA each (0)")
     ap.add_argument("--graph", action="store_true",
                     help="capture one step (all route + forward calls) in a CUDA graph and "
                          "time its replays")

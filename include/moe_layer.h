@@ -194,10 +194,12 @@ moe_status_t moe_forward_static_scratch(moe_layer_t *layer, const void *x, const
  *   MOE_OPT_TIMING: 1 = bracket every kernel launch of this layer with a pair
  *     of CUDA events recorded on the launch stream (read with
  *     moe_layer_timings); 0 = off (default).
- *   MOE_OPT_PAIR_TILES: 1 = 256-token tensor-core tiles run on pairs of
- *     CTAs (tcgen05 cta_group::2) where the shapes allow; 0 (default) = one
- *     CTA per 128 x 256 tile, currently the faster.  Both give the same
- *     results up to the order of fp32 additions inside the MMA. */
+ *   MOE_OPT_PAIR_TILES: 1 (default) = the up projection's 256-token
+ *     tensor-core tiles run on pairs of CTAs (tcgen05 cta_group::2, 256 x 256
+ *     tiles over two SMs) where the shapes allow (resident bf16 layers,
+ *     stored rows a multiple of 256); 0 = one CTA per 128 x 256 tile.  Both
+ *     give the same results up to the order of fp32 additions inside the
+ *     MMA. */
 typedef enum { MOE_OPT_REGIME = 1, MOE_OPT_TIMING = 2, MOE_OPT_PAIR_TILES = 3 } moe_option_t;
 moe_status_t moe_layer_set_option(moe_layer_t *layer, moe_option_t opt, int value);
 

@@ -1,5 +1,6 @@
 // expert_tc2.cu -- the grouped expert GEMM on CTA pairs (tcgen05 cta_group::2)
-// for token tiles of 256, the batch regime's compute-bound case.
+// for token tiles of 256, the batch regime's compute-bound case (used for the
+// up projection; the down projection measured faster on one CTA per tile).
 //
 // Why pairs: with one CTA computing a 128 x 256 tile, every 64-deep step
 // brings 16 KB of weights and 32 KB of tokens into shared memory and the MMAs
@@ -10,7 +11,8 @@
 // halves for the tokens and the operand reads drop to 32 KB per step.
 //
 //   A (per CTA) = its 128 weight rows x 64 reduction elements: one contiguous
-//       16 KB run of the packed layout, one bulk copy, 64-byte swizzle;
+//       16 KB run of the packed layout (64-byte swizzle built in), fetched as
+//       128 rows of 128 bytes through a tensor map over the weight buffer;
 //   B (per CTA) = its 128 tokens x 64 elements of x_perm / h, one tensor-map
 //       copy, 128-byte swizzle;
 //   D = 128 lanes x 256 fp32 columns in each CTA's tensor memory (rows of its
@@ -18,21 +20,19 @@
 //   the even CTA's MMA thread issues M = 256, N = 256 MMAs that read both
 //       CTAs' operands at the same shared-memory offsets.
 // Signalling (mbarriers, all waits bounded):
-//   full[s]   each CTA's copies of stage s landed (its own producer, local);
-//   pfull[s]  (even CTA) the odd CTA's stage s landed: the odd CTA's MMA warp,
-//             otherwise idle, relays its full[s] with a cluster-scope arrive;
+//   full[s]   (even CTA) both CTAs' copies of stage s landed: every copy of
+//             the pair completes its bytes on this barrier (the pair form of
+//             the tensor copy), and the even CTA's producer arms it with the
+//             bytes of both;
 //   empty[s]  both CTAs: the pair MMAs that read stage s completed (commit to
 //             each CTA's barrier);
 //   tfull[b]  both CTAs: accumulator buffer b complete (commit to each);
 //   tempty[b] (even CTA) all eight epilogue warps of the pair read buffer b.
 // Tiles: (expert, 256-row pair block, 256-token tile), token tile fastest;
 // both CTAs of a pair walk the same tile sequence.
-// Status: exact, but slower than one CTA per 128 x 256 tile on the batch
-// workload, so it is off unless MOE_OPT_PAIR_TILES asks for it.  The MMAs run
-// at full rate and the memory system is mostly idle; the copies into the pair
-// land late.  Each CTA's copies complete on its own barrier here; letting
-// them complete on the even CTA's barrier directly (the .cta_group::2 form of
-// the tensor copy) is the untried alternative.  Every path reaches the
+// Teardown: the even CTA's producer waits for the last phase of every stage
+// it armed (both CTAs' bytes); the odd CTA's producer waits until its last
+// stages were consumed by the MMAs (which implies they landed).  Every path reaches the
 // final cluster barrier, so neither CTA leaves while the other may still read
 // its shared memory or the MMAs may still write its tensor memory.
 #include "common.cuh"
@@ -59,9 +59,9 @@ enum Phase { kUp = 0, kDown = 1 };
 template <int PHASE, bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
     tc2_kernel(const ExpertTables tab, const ExpertArgs a, const TcGeom geo,
-               const __grid_constant__ CUtensorMap bmap) {
+               const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], pfull_bar[kMaxStages];
+    __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
     __shared__ uint64_t tfull_bar[2], tempty_bar[2], done_bar;
     __shared__ uint32_t s_tmem;
     __shared__ int s_act[kMaxExperts], s_off[kMaxExperts], s_q[kMaxExperts];
@@ -85,7 +85,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < geo.stages; ++i) {
             mbar_init(&full_bar[i], 1);
             mbar_init(&empty_bar[i], 1);
-            mbar_init(&pfull_bar[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull_bar[i], 1);
@@ -111,6 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
+            const uint8_t *wbase = static_cast<const uint8_t *>(a.wbase);
             for (long long u = pair; u < total && !s_abort; u += npairs) {
                 const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
                 const uint8_t *w = static_cast<const uint8_t *>(PHASE == kUp ? tab.w1[t.e] : tab.w2[t.e]);
@@ -124,10 +124,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     uint8_t *st = smem + stage * kStageBytes;
-                    mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
+                    const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);  // the even CTA's
+                    if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * kStageBytes);
                     const size_t blk = static_cast<size_t>(kb) * geo.rg + 8 * rb;
-                    bulk_g2s_local(st, w + blk * kBlockBytes, kHalfA, &full_bar[stage]);
-                    tma_load_2d_local(st + kHalfA, &bmap, kb * 64, brow, &full_bar[stage]);
+                    const int arow = static_cast<int>(((w - wbase) + blk * kBlockBytes) >> 7);  // 128-byte rows
+                    tma_load_2d_pair(st, &amap, 0, arow, fb);
+                    tma_load_2d_pair(st + kHalfA, &bmap, kb * 64, brow, fb);
                     used[stage] = true;
                     last_parity[stage] = phase;
                     if (++stage == geo.stages) {
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nv = min(kN, (t.q - t.tt * kN + 31) / 32 * 32);
                 const uint32_t idesc = idesc_bf16_f32(256, nv);
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
-                    if (!mbar_wait(&full_bar[stage], phase) || !mbar_wait_cluster(&pfull_bar[stage], phase)) {
+                    if (!mbar_wait_cluster(&full_bar[stage], phase)) {
                         flag_error(a.err, kErrWaitTimeout);
                         s_abort = 1;
                         break;
@@ -186,25 +188,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_commit_pair(smem_u32(&done_bar));  // every pair MMA issued has completed
             if (!mbar_wait(&done_bar, 0)) flag_error(a.err, kErrWaitTimeout);
-        } else if (lane == 0) {
-            // =================== relay (odd CTA): my stage landed ===============
-            int stage = 0;
-            uint32_t phase = 0;
-            for (long long u = pair; u < total && !s_abort; u += npairs) {
-                const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
-                for (int kb = t.kb0; kb < t.kb1; ++kb) {
-                    if (!mbar_wait(&full_bar[stage], phase)) {
-                        flag_error(a.err, kErrWaitTimeout);
-                        s_abort = 1;
-                        break;
-                    }
-                    mbar_arrive_cluster(mapa_shared(smem_u32(&pfull_bar[stage]), 0));
-                    if (++stage == geo.stages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
         }
     } else {
         // ======================= epilogue (both CTAs) ===========================
@@ -277,7 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 0 && lane == 0)
         for (int i = 0; i < geo.stages; ++i)
-            if (used[i]) mbar_wait(&full_bar[i], last_parity[i]);
+            if (used[i]) {
+                if (leader)
+                    mbar_wait_cluster(&full_bar[i], last_parity[i]);
+                else
+                    mbar_wait_cluster(&empty_bar[i], last_parity[i]);
+            }
     __syncwarp();
     cluster_sync_all();
     if (warp == 1) {
@@ -287,8 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int PHASE, bool GATED>
-cudaError_t launch_t(const ExpertArgs &a, const TcGeom &g, const CUtensorMap &bmap, int num_sms,
-                     cudaStream_t s) {
+cudaError_t launch_t(const ExpertArgs &a, const TcGeom &g, const CUtensorMap &amap, const CUtensorMap &bmap,
+                     int num_sms, cudaStream_t s) {
     const size_t smem = 1024 + static_cast<size_t>(g.stages) * kStageBytes;
     auto kern = tc2_kernel<PHASE, GATED>;
     static int configured = 0, pairs = 0;
@@ -321,7 +309,7 @@ cudaError_t launch_t(const ExpertArgs &a, const TcGeom &g, const CUtensorMap &bm
     }
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, *a.tab, a, g, bmap);
+    return cudaLaunchKernelEx(&cfg, kern, *a.tab, a, g, amap, bmap);
 }
 
 // K: reduction length (multiple of 64); rows: stored rows (multiple of 256).
@@ -342,15 +330,11 @@ TcGeom make_geom(int K, int rows) {
 
 }  // namespace
 
-cudaError_t launch_tc2_up(const ExpertArgs &a, bool gated, const CUtensorMap &xmap_half, int num_sms,
-                          cudaStream_t s) {
+cudaError_t launch_tc2_up(const ExpertArgs &a, bool gated, const CUtensorMap &wmap, const CUtensorMap &xmap_half,
+                          int num_sms, cudaStream_t s) {
     const TcGeom g = make_geom(a.m, gated ? 2 * a.p : a.p);
-    return gated ? launch_t<kUp, true>(a, g, xmap_half, num_sms, s) : launch_t<kUp, false>(a, g, xmap_half, num_sms, s);
-}
-
-cudaError_t launch_tc2_down(const ExpertArgs &a, const CUtensorMap &hmap_half, int num_sms, cudaStream_t s) {
-    const TcGeom g = make_geom(a.p, a.m);
-    return launch_t<kDown, false>(a, g, hmap_half, num_sms, s);
+    return gated ? launch_t<kUp, true>(a, g, wmap, xmap_half, num_sms, s)
+                 : launch_t<kUp, false>(a, g, wmap, xmap_half, num_sms, s);
 }
 
 }  // namespace moe

@@ -88,6 +88,7 @@ struct ExpertArgs {
     uint32_t *err;
     int only[kExpertTableMax];
     int n_only;
+    const void *wbase;           // start of the resident weight buffer (CTA-pair kernels)
 };
 
 enum class WeightType { kF32, kBF16, kI8 };
@@ -115,9 +116,10 @@ cudaError_t launch_tc_down(const ExpertArgs &a, int splits, int N, const CUtenso
 // The same on CTA pairs (cta_group::2) for 256-token tiles, bf16 weights,
 // stored rows a multiple of 256, no reduction split; the tensor map fetches
 // 128-token halves (the N = 128 map).
-cudaError_t launch_tc2_up(const ExpertArgs &a, bool gated, const CUtensorMap &xmap_half, int num_sms,
-                          cudaStream_t s);
-cudaError_t launch_tc2_down(const ExpertArgs &a, const CUtensorMap &hmap_half, int num_sms, cudaStream_t s);
+// wmap: the packed weights (a.wbase on) as 128-byte rows, 128-row boxes.
+cudaError_t launch_tc2_up(const ExpertArgs &a, bool gated, const CUtensorMap &wmap, const CUtensorMap &xmap_half,
+                          int num_sms, cudaStream_t s);
+
 // The same with int8 weights (K a multiple of 128): codes widened to bf16 in
 // tensor memory, per-row scale in the epilogue; N tokens per tile, 16..128.
 constexpr int kTcI8MaxN = 128;

@@ -14,7 +14,7 @@ struct moe_layer {
     int device = -1;
     int num_sms = 0;
     int regime = 0;  // MOE_OPT_REGIME
-    bool pair_tiles = false;  // MOE_OPT_PAIR_TILES
+    bool pair_tiles = true;  // MOE_OPT_PAIR_TILES
 
     // weights (resident copy, or unused for paged layers)
     float *wrt = nullptr;      // router [E x m] fp32
@@ -31,6 +31,8 @@ struct moe_layer {
     // tensor maps over x_perm and h for token tiles N = 16, 32, 64, 128, 256
     bool tmap_ok[5] = {};
     CUtensorMap tmap_x[5], tmap_h[5];
+    bool tmap_w_ok = false;  // the resident weights as 128-byte rows (CTA-pair kernels)
+    CUtensorMap tmap_w;
     float *ypart = nullptr;
     float *gate_part = nullptr, *up_part = nullptr;
     size_t decode_rows_cap = 0;

@@ -559,6 +559,27 @@ static moe_status_t make_row_map(CUtensorMap *map, void *base, int K, size_t row
     return MOE_OK;
 }
 
+// The resident weight buffer as rows of 128 bytes, 128-row boxes (16 KB): one
+// box is one 128-row block of a packed matrix at one reduction block.
+static moe_status_t weight_map(moe_layer_t *L, const CUtensorMap **out) {
+    if (!L->tmap_w_ok) {
+        PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+        if (!enc) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+        const size_t bytes = L->expert_stride * static_cast<size_t>(L->cfg.E);
+        const cuuint64_t dims[2] = {64u, static_cast<cuuint64_t>(bytes / 128)};
+        const cuuint64_t strides[1] = {128u};
+        const cuuint32_t box[2] = {64u, 128u};
+        const cuuint32_t es[2] = {1u, 1u};
+        const CUresult r = enc(&L->tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, L->weights, dims, strides, box, es,
+                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(weights) failed (%d)", int(r));
+        L->tmap_w_ok = true;
+    }
+    *out = &L->tmap_w;
+    return MOE_OK;
+}
+
 static int tc_tile_n(int mean_q) {
     if (mean_q <= 12) return 16;
     if (mean_q <= 24) return 32;
@@ -622,31 +643,32 @@ static moe_status_t run_experts_tc(moe_layer_t *L, ExpertArgs &a, int *splits_ou
     } else {
         a.n_rows_cap = rows;
     }
-    // 256-token tiles run on CTA pairs (half the shared-memory traffic per
-    // SM) when both matrices come in 256-row pair blocks and nothing is split
-    const bool pair = !i8 && L->pair_tiles && N == 256 && s_up == 1 && s_down == 1 &&
-                      rows_up % 256 == 0 && c.m % 256 == 0;
-    const CUtensorMap *xm = nullptr, *hm = nullptr;
-    moe_status_t st = tc_maps(L, pair ? N / 2 : N, &xm, &hm);
+    // The up projection's 256-token tiles run on CTA pairs (less shared-memory
+    // traffic per SM; measured faster) when its matrix comes in 256-row pair
+    // blocks and nothing is split; the down projection stays on one CTA per
+    // tile, which measured faster for it.
+    const bool pair_up = !i8 && L->pair_tiles && !L->pool && L->weights && N == 256 && s_up == 1 &&
+                         rows_up % 256 == 0;
+    const CUtensorMap *xm = nullptr, *hm = nullptr, *xm_half = nullptr, *hm_half = nullptr;
+    moe_status_t st = tc_maps(L, N, &xm, &hm);
+    if (st == MOE_OK && pair_up) st = tc_maps(L, N / 2, &xm_half, &hm_half);
     if (st != MOE_OK) return st;
     st = launch_phase(L, MOE_PHASE_GATHER, s, "gather_rows", [&] {
         return launch_gather_rows(a.x, a.gather, rows, a.k, c.m, L->x_perm, L->err_word, s);
     });
-    if (pair) {
+    if (pair_up) {
+        const CUtensorMap *wm = nullptr;
+        if (st == MOE_OK) st = weight_map(L, &wm);
+        a.wbase = L->weights;
         if (st == MOE_OK)
             st = launch_phase(L, MOE_PHASE_UP, s, "tc2_up",
-                              [&] { return launch_tc2_up(a, gated, *xm, L->num_sms, s); });
-        if (st == MOE_OK)
-            st = launch_phase(L, MOE_PHASE_DOWN, s, "tc2_down",
-                              [&] { return launch_tc2_down(a, *hm, L->num_sms, s); });
-        *splits_out = 1;
-        return st;
-    }
-    if (st == MOE_OK)
+                              [&] { return launch_tc2_up(a, gated, *wm, *xm_half, L->num_sms, s); });
+    } else if (st == MOE_OK) {
         st = launch_phase(L, MOE_PHASE_UP, s, "tc_up", [&] {
             return i8 ? launch_tc_i8_up(a, gated, s_up, N, *xm, L->num_sms, s)
                       : launch_tc_up(a, gated, s_up, N, *xm, L->num_sms, s);
         });
+    }
     if (st == MOE_OK && s_up > 1)
         st = launch_phase(L, MOE_PHASE_UP_FINISH, s, "up_finish",
                           [&] { return launch_decode_up_finish(a, gated, s_up, s); });
