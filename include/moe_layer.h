@@ -249,14 +249,24 @@ typedef struct {
 } moe_stats_t;
 moe_status_t moe_layer_stats(moe_layer_t *layer, moe_stats_t *out);
 
+/* Bits of a layer's device error word (reported by moe_layer_sync_check). */
+typedef enum {
+    MOE_FLAG_EXPERT_ID = 1u << 0,     /* expert id outside [0, E): routed to expert 0      */
+    MOE_FLAG_DUPLICATE_ID = 1u << 1,  /* the same expert twice in one token's top-k      */
+    MOE_FLAG_GATHER_INDEX = 1u << 2,  /* gather index outside [0, T*k): access skipped   */
+    MOE_FLAG_OFFSETS = 1u << 3,       /* offsets not monotone or out of range: clamped   */
+    MOE_FLAG_WAIT_TIMEOUT = 1u << 4,  /* a bounded device wait gave up (a bug or a hang) */
+    MOE_FLAG_TMEM_ALLOC = 1u << 5     /* tensor-memory allocation did not succeed        */
+} moe_flag_t;
+
 /* Wait (up to timeout_ms, polling) for the layer's last launched work, then
  * read and clear the device error word.  The wait covers everything queued on
  * the stream of the layer's last route or forward call up to this call (that
  * stream must still exist; a stream being captured into a graph is refused
- * with MOE_ERR_INVALID_ARG).  Returns MOE_ERR_TIMEOUT if the work
- * did not finish in time, MOE_ERR_INVALID_ARG if a kernel flagged bad
- * routing data (the flag bits are written to *flags if flags is not NULL),
- * MOE_OK otherwise. */
+ * with MOE_ERR_INVALID_ARG).  Returns MOE_ERR_TIMEOUT if the work did not
+ * finish in time or a kernel's bounded wait gave up (MOE_FLAG_WAIT_TIMEOUT),
+ * MOE_ERR_INVALID_ARG if a kernel flagged bad routing data (the other flags),
+ * MOE_OK otherwise; the flag bits are written to *flags if flags is not NULL. */
 moe_status_t moe_layer_sync_check(moe_layer_t *layer, int timeout_ms, uint32_t *flags);
 
 /* Copy one stored expert matrix back to the host, in the user's orientation
@@ -317,6 +327,18 @@ moe_status_t moe_pool_query_log(moe_pool_t *pool, int32_t *layer, int32_t *exper
 /* Status text, and the message of the last failure on this host thread. */
 const char *moe_status_string(moe_status_t s);
 const char *moe_last_error(void);
+
+/* Self-test of the device-side wait limit.  Every wait in the library's
+ * kernels polls its mbarrier a bounded number of times and, if the phase has
+ * not completed, sets MOE_FLAG_WAIT_TIMEOUT, releases what it holds and
+ * returns, so a lost signal ends as an error status instead of a hung GPU.
+ * This launches one CTA whose threads wait, with that same bounded loop, on
+ * an mbarrier phase that nothing completes, giving up after `polls` polls
+ * (1 <= polls <= 2^24), and copies the resulting error bits to *flags (may be
+ * NULL).  Synchronises `stream`.  Returns MOE_ERR_TIMEOUT when the wait gave
+ * up (the expected outcome) and MOE_ERR_INTERNAL if it did not; the CUDA
+ * context stays usable either way. */
+moe_status_t moe_selftest_bounded_wait(uint32_t polls, uint32_t *flags, void *stream);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int moe_version(void);

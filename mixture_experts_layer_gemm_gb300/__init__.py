@@ -100,6 +100,7 @@ _SIGNATURES = {
     "moe_pool_destroy": [_vp],
     "moe_pool_query_log": [_vp, _vp, _vp, _vp, _vp, _i, ctypes.POINTER(_i)],
     "moe_pool_set_prefetch": [_vp, _i],
+    "moe_selftest_bounded_wait": [ctypes.c_uint32, _vp, _vp],
     "moe_status_string": [_i],
     "moe_last_error": [],
     "moe_version": [],
@@ -276,6 +277,21 @@ def moe_pool_query_log(pool, max_entries=1 << 20):
     _check(lib().moe_pool_query_log(pool, *[a.ctypes.data for a in arrs], max_entries,
                                     ctypes.byref(n)))
     return tuple(a[:n.value].copy() for a in arrs)
+
+
+MOE_FLAG_EXPERT_ID, MOE_FLAG_DUPLICATE_ID, MOE_FLAG_GATHER_INDEX = 1, 2, 4
+MOE_FLAG_OFFSETS, MOE_FLAG_WAIT_TIMEOUT, MOE_FLAG_TMEM_ALLOC = 8, 16, 32
+
+
+def moe_selftest_bounded_wait(polls, stream=None):
+    """(status, flags) of one kernel whose bounded wait cannot succeed; the
+    expected status is MOE_ERR_TIMEOUT (not raised)."""
+    flags = ctypes.c_uint32(0)
+    st = lib().moe_selftest_bounded_wait(polls, ctypes.byref(flags),
+                                         _stream_ptr(stream) if stream is not None else None)
+    if st not in (MOE_ERR_TIMEOUT, MOE_ERR_INTERNAL, MOE_ERR_INVALID_ARG):
+        _check(st)
+    return st, flags.value
 
 
 def moe_status_string(s) -> str:

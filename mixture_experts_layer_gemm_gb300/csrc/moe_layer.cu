@@ -883,6 +883,8 @@ extern "C" moe_status_t moe_layer_sync_check(moe_layer_t *L, int timeout_ms, uin
     if (word) {
         CUDA_TRY(cudaMemset(L->err_word, 0, 4));
         if (flags) *flags = word;
+        if (word & MOE_FLAG_WAIT_TIMEOUT)
+            return fail(MOE_ERR_TIMEOUT, "a bounded device wait gave up (bits 0x%x)", word);
         return fail(MOE_ERR_INVALID_ARG, "device flagged bad routing data (bits 0x%x)", word);
     }
     return MOE_OK;

@@ -92,3 +92,15 @@ def test_pool_geometry_for_the_mixtral_slot_budget():
     assert moe.moe_pool_geometry(16 << 30, expert, 4) == (12, 48)
     with pytest.raises(moe.MoeError):
         moe.moe_pool_geometry(expert * 3, expert, 4)  # not even one set
+
+
+def test_selftest_rejects_bad_poll_counts_before_touching_the_device():
+    for polls in (0, (1 << 24) + 1):
+        st, flags = moe.moe_selftest_bounded_wait(polls)
+        assert st == moe.MOE_ERR_INVALID_ARG and flags == 0
+
+
+def test_public_error_flags_are_distinct_bits():
+    bits = [moe.MOE_FLAG_EXPERT_ID, moe.MOE_FLAG_DUPLICATE_ID, moe.MOE_FLAG_GATHER_INDEX,
+            moe.MOE_FLAG_OFFSETS, moe.MOE_FLAG_WAIT_TIMEOUT, moe.MOE_FLAG_TMEM_ALLOC]
+    assert all(b & (b - 1) == 0 for b in bits) and len(set(bits)) == len(bits)
