@@ -359,7 +359,7 @@ def run_ours(args, world, rank, local):
     for c in copies:
         c.set_timing(False)
 
-    # ---- algorithmic work per call (SURVEY-style per-unit figures) -------------------
+    # ---- algorithmic work per call (per-unit bytes and flops of each kernel) -----------
     # up: active experts' W1 and W3 (+ int8 scales), token rows read, hidden rows written;
     #     flops 2 * (2 m p) per routed (token, slot) for SwiGLU (2 m p for ReLU)
     # down: active experts' W2 (+ scales), hidden rows read; flops 2 m p per (token, slot)

@@ -35,16 +35,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // ---- memory access ----------------------------------------------------------
-// Streaming 16-byte load of read-once data (expert weights): read-only path,
-// no L1 allocation.
-__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
-
+// 16-byte load through the read-only path (data no kernel of the launch writes).
 __device__ __forceinline__ uint4 ld_nc_v4(const void *p) {
     uint4 r;
     asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
