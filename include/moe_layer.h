@@ -301,7 +301,12 @@ moe_status_t moe_pool_geometry(size_t budget_bytes, size_t expert_bytes, int way
  * soon as its copy has landed, so copies overlap compute.  A slot is never
  * overwritten while a kernel may still read it.  Results are bit-identical
  * to a resident layer's.  A pool may serve many layers (set = layer_id mod N)
- * but one host thread at a time; destroy the layers before the pool. */
+ * but one host thread at a time; destroy the layers before the pool.
+ * Fault injection for tests: if the environment variable MOE_FAULT_COPY_FAIL
+ * holds n when the pool is created, the pool's n-th page copy (0-based,
+ * counting every page of every expert copy) is not issued and the forward call
+ * that needed it returns MOE_ERR_CUDA; the slot it was filling is emptied, so
+ * a later call copies that expert again.  No GPU operation fails. */
 moe_status_t moe_pool_create(size_t budget_bytes, size_t expert_bytes, int ways,
                              size_t page_bytes, moe_pool_t **out);
 moe_status_t moe_pool_destroy(moe_pool_t *pool);

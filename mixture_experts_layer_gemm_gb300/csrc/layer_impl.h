@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <vector>
 
@@ -87,8 +88,17 @@ void decode_plan(const moe_layer *L, int T, int *nt, int *s_up, int *s_down);
 
 // Launch one kernel (f returns its cudaError_t) as phase `phase`: counts the
 // launch and, with timing on, brackets it with events on stream s.
+// A named range on the host timeline of profilers (NVTX; no cost without one).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+
 template <typename F>
 moe_status_t launch_phase(moe_layer *L, int phase, cudaStream_t s, const char *what, F &&f) {
+    NvtxRange range(what);
     cudaEvent_t a = nullptr;
     if (L->timing) {
         a = L->get_event();

@@ -447,6 +447,7 @@ static moe_status_t check_T(const moe_layer_t *L, int T) {
 
 extern "C" moe_status_t moe_route(moe_layer_t *L, const void *x, int T, moe_routing_t *r,
                                   void *stream) {
+    NvtxRange range("moe_route");
     if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
     moe_status_t st = check_T(L, T);
     if (st == MOE_OK) st = check_routing(L, r);
@@ -763,6 +764,7 @@ moe_status_t run_combine(moe_layer_t *L, const moe_routing_t *r, int splits, int
 
 extern "C" moe_status_t moe_forward(moe_layer_t *L, const void *x, const moe_routing_t *r,
                                     void *y, void *stream) {
+    NvtxRange range("moe_forward");
     if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
     moe_status_t st = check_routing(L, r);
     if (st != MOE_OK) return st;

@@ -23,6 +23,7 @@
 // reduction splits) is the one a resident layer uses for the same T, so a paged
 // layer's output is bit-identical to the resident layer's.
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -56,6 +57,8 @@ struct moe_pool {
     std::vector<Slot> slot;
     std::vector<moe_layer *> layer_of;  // attached paged layers by layer id
     int prefetch = 0;                   // experts prefetched for the next layer per call
+    long long fault_page = -1;          // MOE_FAULT_COPY_FAIL: index of the page copy to fail
+    long long pages_issued = 0;
     long long clock = 0;
     std::vector<int32_t> log;  // (layer, expert, hit, slot) per query
     std::mutex mu;
@@ -104,6 +107,7 @@ extern "C" moe_status_t moe_pool_create(size_t budget_bytes, size_t expert_bytes
     P->n_index = n_index;
     P->ways = ways;
     P->n_slots = usable;
+    if (const char *f = std::getenv("MOE_FAULT_COPY_FAIL")) P->fault_page = std::atoll(f);
     cudaError_t e = cudaGetDevice(&P->device);
     if (e == cudaSuccess) e = cudaMalloc(&P->slots, P->slot_bytes * static_cast<size_t>(usable));
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&P->copy_stream, cudaStreamNonBlocking);
@@ -265,6 +269,14 @@ moe_status_t pool_copy_in(moe_pool *P, moe_layer *L, moe_layer *N, int e, int si
     if (c0) err = cudaEventRecord(c0, P->copy_stream);
     const uint8_t *src = N->pinned_weights + N->expert_stride * static_cast<size_t>(e);
     for (size_t off = 0; err == cudaSuccess && off < N->expert_stride; off += P->page_bytes) {
+        if (P->pages_issued++ == P->fault_page) {
+            // injected failure: the slot holds a partial expert, so it must
+            // not be found again; the caller sees the error
+            slot.layer = -1;
+            slot.expert = -1;
+            slot.fetched = false;
+            return fail(MOE_ERR_CUDA, "injected page-copy failure (MOE_FAULT_COPY_FAIL=%lld)", P->fault_page);
+        }
         const size_t n = std::min(P->page_bytes, N->expert_stride - off);
         err = cudaMemcpyAsync(dst + off, src + off, n, cudaMemcpyHostToDevice, P->copy_stream);
     }

@@ -104,3 +104,26 @@ def test_public_error_flags_are_distinct_bits():
     bits = [moe.MOE_FLAG_EXPERT_ID, moe.MOE_FLAG_DUPLICATE_ID, moe.MOE_FLAG_GATHER_INDEX,
             moe.MOE_FLAG_OFFSETS, moe.MOE_FLAG_WAIT_TIMEOUT, moe.MOE_FLAG_TMEM_ALLOC]
     assert all(b & (b - 1) == 0 for b in bits) and len(set(bits)) == len(bits)
+
+
+def test_phi_expert_size_in_binary_units():
+    # the expert-cache article's Phi-3.5-MoE expert: 3 x 4096 x 6400 bf16 values
+    expert = 3 * 4096 * 6400 * 2
+    assert expert == 150 * (1 << 20) and round(expert / 1e6, 1) == 157.3
+
+
+def test_transfer_threshold_is_where_loading_stops_dominating():
+    """HARMOEny write-up, 3.2: an expert is worth fetching over the link when its
+    compute outlasts its transfer, q > phi * dtype / (2 beta).  The crossover of
+    the two times -- load 2 m p dtype / beta, compute 4 q m p / phi (two
+    multiply-adds per weight and token) -- found by search must equal that
+    closed form; with GB300-like numbers decode batches sit far below it."""
+    m, p, dtype = 4096, 14336, 2
+    phi, beta = 1944e12, 211e9
+    load = 2 * m * p * dtype / beta
+    q = 1
+    while 4 * q * m * p / phi <= load:
+        q += 1
+    closed = phi * dtype / (2 * beta)
+    assert q - 1 <= closed < q
+    assert 16 < closed / 100  # decode (q <= 16 per expert) is link-bound by two orders of magnitude

@@ -231,3 +231,35 @@ def test_duplicate_layer_id_in_a_pool_is_rejected():
     b = moe.MoELayer(wl.make_layer(SHAPE, seed=6), 4, pool=pool, layer_id=3)  # id free again
     b.close()
     moe.moe_pool_destroy(pool)
+
+
+def test_injected_page_copy_failure_rolls_back_the_slot(monkeypatch):
+    """MOE_FAULT_COPY_FAIL=n: the n-th page copy is not issued, the forward that
+    needed it returns MOE_ERR_CUDA, the half-filled slot is emptied, and the
+    next calls copy that expert again and match the resident layer bit for bit."""
+    monkeypatch.setenv("MOE_FAULT_COPY_FAIL", "2")  # the third page copy (one page per expert here)
+    eb = _expert_bytes(SHAPE)
+    pool = moe.moe_pool_create(eb * 8, eb, 4, 0)
+    monkeypatch.delenv("MOE_FAULT_COPY_FAIL")
+    layer = wl.make_layer(SHAPE, seed=71)
+    paged = moe.MoELayer(layer, 16, pool=pool, layer_id=0)
+    resident = moe.MoELayer(layer, 16)
+    ids = np.array([[0, 1], [2, 3]], np.int32)  # four experts: copies 0, 1, 2 (fails), ...
+    w = np.full((2, 2), 0.5, np.float32)
+    x = wl.make_tokens(SHAPE, 2, seed=72)
+    with pytest.raises(moe.MoeError) as ei:
+        Run(paged, x, routing="topk", ids=ids, w=w)
+    assert ei.value.status == moe.MOE_ERR_CUDA
+    torch.cuda.synchronize()
+    for _ in range(2):
+        rp = Run(paged, x, routing="topk", ids=ids, w=w)
+        rr = Run(resident, x, routing="topk", ids=ids, w=w)
+        np.testing.assert_array_equal(rp.y_np, rr.y_np)
+    log = moe.moe_pool_query_log(pool)
+    # call 1: experts 0, 1 copied, expert 2 failed (logged as a miss); call 2:
+    # 0, 1 hit, 2 missed again (the slot was emptied), 3 missed; call 3: all hit
+    assert list(log[1]) == [0, 1, 2, 0, 1, 2, 3, 0, 1, 2, 3]
+    assert list(log[2]) == [0, 0, 0, 1, 1, 0, 0, 1, 1, 1, 1]
+    paged.close()
+    resident.close()
+    moe.moe_pool_destroy(pool)

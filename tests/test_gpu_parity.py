@@ -250,6 +250,15 @@ def test_temporal_locality_tokens():
     run, _ = run_and_check(SWIGLU_BF16, 64, seed=12, locality=0.5)
 
 
+def test_expert_bytes_are_the_matrix_bytes():
+    """|E| of the HARMOEny write-up (3.2) for the stored bf16 experts: 2 m p b
+    for the two-matrix expert, 3 m p b with the gate matrix (b = 2 bytes)."""
+    for shape, mats in ((SWIGLU_BF16, 3), (RELU_BF16, 2)):
+        ml = moe.MoELayer(get_layer(shape, seed=40), 4)
+        assert ml.info().expert_bytes == mats * shape.m * shape.p * 2
+        ml.close()
+
+
 # ---- int8 weights ------------------------------------------------------------------------
 I8 = SWIGLU_BF16.with_weight("i8")
 
