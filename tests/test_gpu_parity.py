@@ -236,6 +236,36 @@ def test_odd_shapes_bf16(T):
     run_and_check(ODD_BF16, T, seed=9, regime=moe.REGIME_DECODE)
 
 
+ALL_EXPERTS = wl.LayerShape("k-equals-e", m=256, p=384, E=4, k=4, expert=wl.SWIGLU, act="bf16",
+                            weight="bf16")
+
+
+@pytest.mark.parametrize("T,regime", [(1, moe.REGIME_DECODE), (37, moe.REGIME_DECODE),
+                                      (37, moe.REGIME_BATCH), (300, moe.REGIME_AUTO)])
+def test_every_token_to_every_expert(T, regime):
+    """k = E: every token visits all four experts; the weights are the full
+    softmax; each expert segment is the whole batch in token order."""
+    run, _ = run_and_check(ALL_EXPERTS, T, seed=41, regime=regime)
+    assert np.all(run.counts == T)
+    np.testing.assert_allclose(run.w.sum(axis=1), 1.0, rtol=0, atol=1e-6)
+
+
+def test_batch_beyond_the_gemv_on_a_shape_without_tensor_core_tiles_is_refused():
+    """m = 320 has no 128-row blocks for the tensor-core path and T*k = 600 is
+    more than the weight-streaming kernels take: the call is refused with
+    MOE_ERR_UNSUPPORTED before any launch, and the layer stays usable."""
+    layer = get_layer(ODD_BF16, seed=42)
+    ml = moe.MoELayer(layer, 200)
+    x = wl.make_tokens(ODD_BF16, 200, seed=43)
+    with pytest.raises(moe.MoeError) as ei:
+        Run(ml, x)
+    assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    run_ok = Run(ml, x[:50])
+    assert ml.sync_check()[0] == moe.MOE_OK and run_ok.y_np.shape == (50, ODD_BF16.m)
+    ml.close()
+
+
 def test_64_experts_top4():
     run_and_check(WIDE_E, 50, seed=10)
 
