@@ -216,11 +216,9 @@ def shape_of(args):
 def workload_config(shape, weights, flush_note):
     ts = ",".join(str(t) for t in TOKENS)
     regime = "decode" if max(TOKENS) <= 64 else "batch"
-    return {"workload": f"{shape.name} moe layer {regime}, T in {{{ts}}}, {weights} weights",
-            "model": f"{shape.name}-shaped single MoE FFN layer", "m": shape.m, "p": shape.p,
-            "E": shape.E, "k": shape.k, "expert": "swiglu", "tokens_per_step": sum(TOKENS),
-            "global_batch": sum(TOKENS), "seq_len": 1, "parallelism": "replicas",
-            "l2": flush_note}
+    return {"workload": f"{shape.name}-shaped MoE FFN layer, {regime}, T in {{{ts}}}, {weights} weights",
+            "m": shape.m, "p": shape.p, "E": shape.E, "k": shape.k, "expert": "swiglu",
+            "tokens_per_step": sum(TOKENS), "parallelism": "replicas", "l2": flush_note}
 
 
 def run_reference(args, world, rank):
