@@ -156,6 +156,20 @@ __device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gsrc, uint3
         : "memory");
 }
 
+// The same copy for data read once per launch (streamed expert weights): the
+// lines are marked first to go from L2, so that what the neighbouring
+// launches reuse (activations, partial sums) stays resident.
+__device__ __forceinline__ void bulk_g2s_once(void *smem_dst, const void *gsrc, uint32_t bytes,
+                                              uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .b64 pol;\n\t"
+        "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "pol;\n\t}" ::"r"(smem_u32(smem_dst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ---- programmatic dependent launch -----------------------------------------------
 // Kernels on the forward path are launched so that each may start while its
 // predecessor in the stream finishes.  Protocol: a kernel calls pdl_wait()

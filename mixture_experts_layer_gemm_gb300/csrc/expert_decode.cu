@@ -180,8 +180,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         mbar_arrive_expect_tx(&full_bar[stage], bytes);
                         const size_t blk = static_cast<size_t>(kb) * geo.rg + 8 * U.g8;
-                        bulk_g2s(ring + stage * kStageBytes, w + blk * kBlockBytes, bytes,
-                                 &full_bar[stage]);
+                        if (q <= kTok)  // one token pass: each weight byte is read once
+                            bulk_g2s_once(ring + stage * kStageBytes, w + blk * kBlockBytes, bytes,
+                                          &full_bar[stage]);
+                        else
+                            bulk_g2s(ring + stage * kStageBytes, w + blk * kBlockBytes, bytes,
+                                     &full_bar[stage]);
                         used[stage] = true;
                         last_parity[stage] = phase;
                         if (++stage == kStages) {
