@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ long long s_prefix[kMaxExperts + 1];
     __shared__ int s_nact;
     __shared__ volatile int s_abort;
+    __shared__ float s_w[kEpiWarps][kTcMaxTileTokens];  // down: routing weights of the tile
 
     // 1024-byte aligned operand area (swizzle atoms are address-based)
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -68,7 +69,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t *b_slots = smem + geo.stages * kATileBytes;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int rows_total = a.T * a.k;
     pdl_wait();
     pdl_trigger();
 
@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int R = t.rb * 128 + row_in_tile;  // stored weight row of this thread
             const int tok0 = t.tt * geo.N;
             const int n_valid = min(geo.N, (t.q - tok0 + 15) / 16 * 16);
+            if (PHASE == kDown) tc_stage_weights(a, t.off, tok0, t.q, n_valid, s_w[lq], lane);
             for (int c0 = 0; c0 < n_valid; c0 += 16) {
                 uint32_t v[16];
                 tmem_ld16(tmem_base + (static_cast<uint32_t>(lq * 32) << 16) +
@@ -240,10 +241,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const int tok = tok0 + c0 + j;
                         if (tok < t.q) {
                             const int pos = t.off + tok;
-                            const int fi = a.gather[pos];
-                            const float wgt = (fi >= 0 && fi < rows_total) ? a.topk_w[fi] : 0.0f;
                             a.ypart[(static_cast<size_t>(t.ks) * a.n_rows_cap + pos) * a.m + R] =
-                                wgt * __uint_as_float(v[j]);
+                                s_w[lq][c0 + j] * __uint_as_float(v[j]);
                         }
                     }
                 }

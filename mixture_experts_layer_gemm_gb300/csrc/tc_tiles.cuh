@@ -80,4 +80,30 @@ __device__ __forceinline__ int tc_list_tiles(const ExpertArgs &a, const TcGeom &
     return n;
 }
 
+// Routing weights of a tile's tokens tok0 .. tok0 + n - 1 (n <= 256) of the
+// segment at `off`, read by one warp with independent loads (eight per lane)
+// into that warp's shared-memory row, so that the down projection's store loop
+// does not wait on two dependent global loads per token.  Tokens past the
+// segment, or whose gather index is out of range, get weight 0.
+constexpr int kTcMaxTileTokens = 256;
+
+__device__ __forceinline__ void tc_stage_weights(const ExpertArgs &a, int off, int tok0, int q, int n,
+                                                 float *s_w, int lane) {
+    const int rows_total = a.T * a.k;
+    int fi[kTcMaxTileTokens / 32];
+#pragma unroll
+    for (int ci = 0; ci < kTcMaxTileTokens / 32; ++ci) {
+        const int c = ci * 32 + lane;
+        fi[ci] = (c < n && tok0 + c < q) ? a.gather[off + tok0 + c] : -1;
+    }
+    float wv[kTcMaxTileTokens / 32];
+#pragma unroll
+    for (int ci = 0; ci < kTcMaxTileTokens / 32; ++ci)
+        wv[ci] = (fi[ci] >= 0 && fi[ci] < rows_total) ? a.topk_w[fi[ci]] : 0.0f;
+    __syncwarp();  // every lane is past its reads of the previous tile's row
+#pragma unroll
+    for (int ci = 0; ci < kTcMaxTileTokens / 32; ++ci) s_w[ci * 32 + lane] = wv[ci];
+    __syncwarp();
+}
+
 }  // namespace moe
