@@ -216,16 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait();
                 if (PHASE == kUp && GATED) {
                     const int r16 = R & 15;
-                    const int f = (R >> 4) * 8 + (r16 & 7);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float gv = __uint_as_float(v[j]);
-                        const float uv = __shfl_down_sync(0xffffffffu, gv, 8);
-                        const int tok = tok0 + c0 + j;
-                        if (r16 < 8 && tok < t.q)
-                            static_cast<__nv_bfloat16 *>(a.h)[static_cast<size_t>(t.off + tok) * a.p + f] =
-                                __float2bfloat16_rn(silu(gv) * uv);
-                    }
+                    tc_swiglu_store16(v, 1.0f, r16 < 8, static_cast<__nv_bfloat16 *>(a.h), a.p,
+                                      (R >> 4) * 8 + (r16 & 7), t.off, tok0 + c0, t.q);
                 } else if (PHASE == kUp) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {

@@ -218,18 +218,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                           v);
                 tmem_ld_wait();
                 if (PHASE == kUp && GATED) {
+                    if (geo.splits == 1) {
+                        tc_swiglu_store16(v, scale, r16 < 8, static_cast<__nv_bfloat16 *>(a.h), a.p, f, t.off,
+                                          tok0 + c0, t.q);
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float gv = __uint_as_float(v[j]) * scale;
-                        const float uv = __shfl_down_sync(0xffffffffu, gv, 8);
-                        const int tok = tok0 + c0 + j;
-                        if (r16 < 8 && tok < t.q) {
-                            const int pos = t.off + tok;
-                            if (geo.splits == 1) {
-                                static_cast<__nv_bfloat16 *>(a.h)[static_cast<size_t>(pos) * a.p + f] =
-                                    __float2bfloat16_rn(silu(gv) * uv);
-                            } else {
-                                const size_t o = (static_cast<size_t>(t.ks) * a.n_rows_cap + pos) * a.p + f;
+                        for (int j = 0; j < 16; ++j) {
+                            const float gv = __uint_as_float(v[j]) * scale;
+                            const float uv = __shfl_down_sync(0xffffffffu, gv, 8);
+                            const int tok = tok0 + c0 + j;
+                            if (r16 < 8 && tok < t.q) {
+                                const size_t o =
+                                    (static_cast<size_t>(t.ks) * a.n_rows_cap + t.off + tok) * a.p + f;
                                 a.gate_part[o] = gv;
                                 a.up_part[o] = uv;
                             }

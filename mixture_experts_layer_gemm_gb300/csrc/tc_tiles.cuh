@@ -87,6 +87,34 @@ __device__ __forceinline__ int tc_list_tiles(const ExpertArgs &a, const TcGeom &
 // segment, or whose gather index is out of range, get weight 0.
 constexpr int kTcMaxTileTokens = 256;
 
+// SiLU from the hardware exp2 and reciprocal approximations (the __expf and
+// __fdividef intrinsics): a few instructions instead of the IEEE-accurate
+// sequences, with an error far below the bf16 rounding of h.  For z -> -inf
+// the denominator overflows to +inf and the quotient is 0.
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+// SwiGLU epilogue of 16 accumulator columns, the tokens tok .. tok + 15 of the
+// segment at `off`.  Stored rows interleave 8 gate and 8 up rows, so a lane
+// whose row has bit 3 clear holds gate values and the lane 8 away the matching
+// up values of the same feature f.  The pair swaps half its columns with one
+// shuffle per column pair, after which the gate lane finishes tokens 0..7 and
+// the up lane tokens 8..15: every lane does useful work and each SiLU is
+// evaluated once.  `scale` multiplies this lane's own values (int8 row scales;
+// 1 for bf16 weights).  Tokens at or past q are not stored.
+__device__ __forceinline__ void tc_swiglu_store16(const uint32_t (&v)[16], float scale, bool gate_lane,
+                                                  __nv_bfloat16 *h, int p, int f, int off, int tok,
+                                                  int q) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float lo = __uint_as_float(v[j]) * scale, hi = __uint_as_float(v[j + 8]) * scale;
+        const float recv = __shfl_xor_sync(0xffffffffu, gate_lane ? hi : lo, 8);
+        const float g = gate_lane ? lo : recv;
+        const float u = gate_lane ? recv : hi;
+        const int tk = tok + j + (gate_lane ? 0 : 8);
+        if (tk < q) h[static_cast<size_t>(off + tk) * p + f] = __float2bfloat16_rn(silu_fast(g) * u);
+    }
+}
+
 __device__ __forceinline__ void tc_stage_weights(const ExpertArgs &a, int off, int tok0, int q, int n,
                                                  float *s_w, int lane) {
     const int rows_total = a.T * a.k;
