@@ -246,6 +246,8 @@ typedef struct {
     double forward_ms;   /* summed duration of paged forward calls         */
     uint64_t prefetch_copies; /* experts this layer's calls prefetched for the next layer */
     uint64_t prefetch_hits;   /* lookups of this layer served by a prefetched expert      */
+    uint64_t gemv_runs;       /* expert-MLP passes on the weight-streaming GEMV (decode regime) */
+    uint64_t tc_runs;         /* expert-MLP passes on the tensor-core grouped GEMM (batch regime) */
 } moe_stats_t;
 moe_status_t moe_layer_stats(moe_layer_t *layer, moe_stats_t *out);
 

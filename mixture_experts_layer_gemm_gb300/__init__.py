@@ -67,7 +67,8 @@ class moe_stats_t(ctypes.Structure):
     _fields_ = [("kernel_launches", ctypes.c_uint64), ("forwards", ctypes.c_uint64), ("slot_hits", ctypes.c_uint64),
                 ("slot_misses", ctypes.c_uint64), ("h2d_bytes", ctypes.c_uint64),
                 ("h2d_ms", ctypes.c_double), ("forward_ms", ctypes.c_double),
-                ("prefetch_copies", ctypes.c_uint64), ("prefetch_hits", ctypes.c_uint64)]
+                ("prefetch_copies", ctypes.c_uint64), ("prefetch_hits", ctypes.c_uint64),
+                ("gemv_runs", ctypes.c_uint64), ("tc_runs", ctypes.c_uint64)]
 
 
 class MoeError(RuntimeError):

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -72,6 +73,29 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+
+// The same with fp16 inputs (same fragment ownership).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four signed int8 values b (one word, byte 0 first) -> two fp16x2 words
+// holding 1152 + b for bytes (0,1) and (2,3), exactly: flipping the sign bit
+// gives the byte u = b + 128 in [0, 255], and the fp16 bit pattern 0x6400 | u
+// is 1024 + u (exponent 2^10, u in the low bits of the ten-bit mantissa).
+// Three instructions per word; the constant 1152 is taken out after the dot
+// product (1152 times the sum of the activations).
+__device__ __forceinline__ void i8x4_to_f16x2x2_biased(uint32_t v, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = v ^ 0x80808080u;
+    lo = __byte_perm(u, 0x64646464u, 0x4140);  // {u0, 0x64, u1, 0x64}
+    hi = __byte_perm(u, 0x64646464u, 0x4342);  // {u2, 0x64, u3, 0x64}
+}
+constexpr float kI8F16Bias = 1152.0f;
 
 // Four signed int8 values (one 32-bit word, byte 0 first) -> two bf16x2 words
 // holding bytes (0,1) and (2,3), exactly, with byte permutes and one packed

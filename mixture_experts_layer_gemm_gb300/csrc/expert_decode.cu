@@ -32,10 +32,17 @@
 //     (int8) MMAs under one shared permutation of the reduction index;
 //   - the token rows of the current expert and split are staged once in
 //     shared memory and reused by every unit of that expert;
-//   - int8 weights are widened to bf16 in registers (exact) and the
-//     per-output scale is applied after the dot product.
+//   - int8 weights run the MMAs in fp16: one XOR and two byte permutes turn
+//     four codes b into the exact fp16 values 1152 + b (a third of the
+//     instructions of widening to bf16), the staged token rows are converted
+//     to fp16 under a power-of-two scale per row (exact for every value in
+//     fp16's normal range), and the epilogue takes out 1152 times the row sum
+//     of the scaled activations, undoes the row scale and applies the
+//     per-output weight scale.
 // Every wait is bounded; a wait that gives up sets kErrWaitTimeout in the
 // layer's error word and the CTA drains its copies in flight and returns.
+#include <cmath>
+
 #include "common.cuh"
 #include "kernels.cuh"
 #include "packing.h"
@@ -84,6 +91,51 @@ __device__ __forceinline__ int split_begin(int n, int splits, int ks) {
     return static_cast<int>((static_cast<long long>(n) * ks) / splits);
 }
 
+// int8 weights: convert the staged bf16 token rows to fp16 in place, one warp
+// per row.  The row's largest magnitude sets a power-of-two scale 2^-s that
+// puts it in [2^14, 2^15): every bf16 value whose scaled magnitude is at least
+// 2^-14 is then an exact fp16 value (only values below the row maximum by a
+// factor of 2^28 or more round).  Records 2^s and the sum of the converted
+// values (fixed order) for the epilogue.  A row of zeros, or one holding an
+// infinity or NaN, keeps scale 1.
+template <int kTok>
+__device__ __forceinline__ void stage_rows_f16(uint8_t *bstage, int row_bytes, int vec_per_row, int warp,
+                                               int lane, float *s_xscale, float *s_xsum) {
+    for (int r = warp; r < kTok; r += kConsumerWarps) {
+        uint4 *row = reinterpret_cast<uint4 *>(bstage + static_cast<size_t>(r) * row_bytes);
+        float mx = 0.0f;
+        for (int v = lane; v < vec_per_row; v += 32) {
+            const uint4 q = row[v];
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fmaxf(fabsf(bf16lo(w[i])), fabsf(bf16hi(w[i]))));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const int eb = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu);
+        int sh = (eb == 0 || eb == 255) ? 0 : eb - 127 - 14;
+        sh = sh < -100 ? -100 : (sh > 113 ? 113 : sh);
+        const float down = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);  // 2^-sh
+        float sum = 0.0f;
+        for (int v = lane; v < vec_per_row; v += 32) {
+            const uint4 q = row[v];
+            uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const __half2 hv = __floats2half2_rn(bf16lo(w[i]) * down, bf16hi(w[i]) * down);
+                sum += __low2float(hv) + __high2float(hv);
+                w[i] = *reinterpret_cast<const uint32_t *>(&hv);
+            }
+            row[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        sum = warp_sum(sum);
+        if (lane == 0) {
+            s_xscale[r] = __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);  // 2^sh
+            s_xsum[r] = sum;
+        }
+    }
+}
+
 struct Unit {
     int e, ks, g8, nrg, off, end, kb0, kb1;
     bool ok;
@@ -114,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int s_act[kMaxExperts];
     __shared__ int s_nact;
     __shared__ volatile int s_abort;
+    __shared__ float s_xscale[kTok], s_xsum[kTok];  // int8: per staged row, 2^s and sum of x 2^-s
 
     uint8_t *ring = smem;
     uint8_t *bstage = smem + kStages * kStageBytes;
@@ -250,6 +303,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 staged_ks = U.ks;
                 staged_tp = tp;
                 named_sync(kBarConsumers, kConsumers);
+                if constexpr (WT == WeightType::kI8) {
+                    stage_rows_f16<kTok>(bstage, geo.row_bytes, kcount / 8, warp, lane, s_xscale, s_xsum);
+                    named_sync(kBarConsumers, kConsumers);
+                }
             }
             float acc[NT][4];
 #pragma unroll
@@ -290,18 +347,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t vb[4] = {rb.x, rb.y, rb.z, rb.w};
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
-                                i8x4_to_bf16x2x2(va[i], al[i], ah[i]);
-                                i8x4_to_bf16x2x2(vb[i], bl[i], bh[i]);
+                                i8x4_to_f16x2x2_biased(va[i], al[i], ah[i]);
+                                i8x4_to_f16x2x2_biased(vb[i], bl[i], bh[i]);
                             }
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) {
                                 const uint32_t xa = bsm + (nt * 8 + g) * geo.row_bytes + (kcol + 16 * t) * 2;
                                 const uint4 x0 = lds_v4(xa);
                                 const uint4 x1 = lds_v4(xa + 16);
-                                mma_bf16_16816(acc[nt], al[0], bl[0], ah[0], bh[0], x0.x, x0.y);
-                                mma_bf16_16816(acc[nt], al[1], bl[1], ah[1], bh[1], x0.z, x0.w);
-                                mma_bf16_16816(acc[nt], al[2], bl[2], ah[2], bh[2], x1.x, x1.y);
-                                mma_bf16_16816(acc[nt], al[3], bl[3], ah[3], bh[3], x1.z, x1.w);
+                                mma_f16_16816(acc[nt], al[0], bl[0], ah[0], bh[0], x0.x, x0.y);
+                                mma_f16_16816(acc[nt], al[1], bl[1], ah[1], bh[1], x0.z, x0.w);
+                                mma_f16_16816(acc[nt], al[2], bl[2], ah[2], bh[2], x1.x, x1.y);
+                                mma_f16_16816(acc[nt], al[3], bl[3], ah[3], bh[3], x1.z, x1.w);
                             }
                         }
                     }
@@ -320,9 +377,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
-                        const int pos = U.off + tp * kTok + nt * 8 + 2 * t + h2;
+                        const int tk = nt * 8 + 2 * t + h2;  // token of the pass
+                        const int pos = U.off + tp * kTok + tk;
                         if (pos >= U.end) continue;
                         float v0 = acc[nt][h2], v8 = acc[nt][2 + h2];
+                        if (WT == WeightType::kI8) {  // take out the code bias, undo the row scale
+                            v0 = fmaf(-kI8F16Bias, s_xsum[tk], v0) * s_xscale[tk];
+                            v8 = fmaf(-kI8F16Bias, s_xsum[tk], v8) * s_xscale[tk];
+                        }
                         if (PHASE == kUp && GATED) {
                             const int n = rg * 8 + g;  // feature: gate row g, up row g + 8
                             if (WT == WeightType::kI8) {
@@ -443,12 +505,20 @@ cudaError_t dispatch_nt(const ExpertArgs &a, int nt, int K, int rows, int splits
 
 }  // namespace
 
-// Token tiles per pass, from the mean tokens per expert (T*k/E); experts with
-// more tokens than one pass holds take further passes over their weights.
+// Token tiles per pass.  An expert with more tokens than one pass holds
+// streams its weights once per pass, so the pass is sized for the busier
+// experts, not the mean: under uniform routing an expert's count has mean
+// T k / E and variance T k (1/E)(1 - 1/E), and the pass covers the mean plus
+// 1.5 standard deviations.  Four tiles (32 tokens) stage four times the rows
+// and cost more reduction splits, so two tiles are kept while their 16 tokens
+// cover all but a few experts (Mixtral shape, T = 48: two tiles 362 us, four
+// tiles 495 us; T = 56 with two tiles, where most experts need a second pass:
+// 1040 us).
 int decode_token_tiles(int T, int k, int E) {
-    const int mean_q = (T * k + E - 1) / E;
-    if (mean_q <= 6) return 1;
-    if (mean_q <= 12) return 2;
+    const double mean = static_cast<double>(T) * k / E;
+    const double hi = mean + 1.5 * std::sqrt(mean * (1.0 - 1.0 / E)) + 0.5;
+    if (hi <= 8.0) return 1;
+    if (hi <= 18.0) return 2;
     return 4;
 }
 

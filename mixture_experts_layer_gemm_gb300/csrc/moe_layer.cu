@@ -71,10 +71,12 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
 constexpr int kSplitUpMax = 4, kSplitDownMax = 16;
-// Mean tokens per expert above which the tensor-core path runs.  The int8
-// weight-streaming kernel widens each code once per pass and reuses it for
-// every token tile, so it stays ahead of the tensor cores for longer.
-constexpr int kTcMinMeanTokens = 6;
+// Mean tokens per expert above which the tensor-core path runs (measured
+// crossover, Mixtral shape: bf16 GEMV 446 us vs tensor cores 455 us at T = 16,
+// 473 vs 457 at T = 20).  The int8 weight-streaming kernel widens each code
+// once per pass and reuses it for every token tile, so it stays ahead of the
+// tensor cores for longer (T = 48: 362 vs 485 us; T = 64: 511 vs 488).
+constexpr int kTcMinMeanTokens = 4;
 constexpr int kTcMinMeanTokensI8 = 12;
 
 // Smallest split of a K-long reduction whose staged token rows (8 * nt rows of
@@ -712,7 +714,11 @@ moe_status_t run_experts(moe_layer_t *L, ExpertArgs &a, int regime, int *splits_
         const int min_q = c.weight_dtype == MOE_I8 ? kTcMinMeanTokensI8 : kTcMinMeanTokens;
         use_tc = tc_shape && (mean_q > min_q || !fits_decode);
     }
-    if (use_tc) return run_experts_tc(L, a, splits_out, s);
+    if (use_tc) {
+        L->stats.tc_runs += 1;
+        return run_experts_tc(L, a, splits_out, s);
+    }
+    L->stats.gemv_runs += 1;
     const WeightType wt = (c.weight_dtype == MOE_I8) ? WeightType::kI8 : WeightType::kBF16;
     int nt = decode_token_tiles(a.T, a.k, a.E);
     int s_up, s_down;

@@ -441,3 +441,24 @@ def test_identical_experts_output_is_routing_independent():
     rel, _ = max_token_rel_l2(run.y_np, y1)
     assert rel <= 1e-2
     ml.close()
+
+
+def test_regime_counters_follow_the_choice():
+    """Few tokens per expert take the weight-streaming GEMV, many the tensor
+    cores; a forced regime overrides the choice.  The counters say which ran."""
+    layer = get_layer(SWIGLU_BF16, seed=61)
+    ml = moe.MoELayer(layer, 512)
+
+    def runs(T, regime=moe.REGIME_AUTO):
+        ml.set_regime(regime)
+        s0 = ml.stats()
+        Run(ml, wl.make_tokens(SWIGLU_BF16, T, seed=T))
+        s1 = ml.stats()
+        return int(s1.gemv_runs - s0.gemv_runs), int(s1.tc_runs - s0.tc_runs)
+
+    assert runs(4) == (1, 0)      # 1 token per expert on average
+    assert runs(200) == (0, 1)    # 50 tokens per expert
+    assert runs(200, moe.REGIME_DECODE) == (1, 0)  # T k = 400: within the GEMV's range
+    assert runs(4, moe.REGIME_BATCH) == (0, 1)
+    assert ml.sync_check()[0] == moe.MOE_OK
+    ml.close()
