@@ -462,3 +462,30 @@ def test_regime_counters_follow_the_choice():
     assert runs(4, moe.REGIME_BATCH) == (0, 1)
     assert ml.sync_check()[0] == moe.MOE_OK
     ml.close()
+
+
+@pytest.mark.parametrize("regime", [moe.REGIME_DECODE, moe.REGIME_BATCH])
+def test_int8_activation_range(regime):
+    """Token rows spanning 2^-40 .. 2^40 (the int8 GEMV stages each row in
+    fp16 under its own power-of-two scale; fp16 alone holds neither end).
+    Routing is given, so that scaled logits cannot create near-ties; each
+    token must match the oracle on the oracle's own int8 codes."""
+    layer = get_layer(I8, seed=63)
+    shifts = np.array([-40, -30, -20, -10, 0, 0, 10, 20, 30, 40])
+    T = len(shifts)
+    x = wl.make_tokens(I8, T, seed=64)
+    xf = (x.astype(np.uint32) << 16).view(np.float32) * np.exp2(shifts)[:, None].astype(np.float32)
+    xs = (xf.view(np.uint32) >> 16).astype(np.uint16)  # exact: a power-of-two scale keeps the low bits zero
+    rng = np.random.default_rng(65)
+    ids = np.stack([rng.permutation(I8.E)[:I8.k] for _ in range(T)]).astype(np.int32)
+    w = rng.random((T, I8.k)).astype(np.float32) + 0.1
+    w = (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
+    ml = moe.MoELayer(layer, T)
+    ml.set_regime(regime)
+    run = Run(ml, xs, routing="topk", ids=ids, w=w)
+    assert ml.sync_check()[0] == moe.MOE_OK
+    ref = oracle_y(layer, xs, ids, w, oracle_quantized(layer))
+    assert np.all(np.isfinite(f64(run.y_np)))
+    rel, _ = max_token_rel_l2(run.y_np, ref)
+    assert rel <= 1e-2, rel
+    ml.close()
