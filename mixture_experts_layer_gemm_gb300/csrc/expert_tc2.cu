@@ -54,9 +54,9 @@ constexpr int kMaxStages = 6;
 constexpr int kN = 256;               // tokens per pair tile
 constexpr uint32_t kTmemCols = 512;   // two accumulators of 256 columns
 
-enum Phase { kUp = 0, kDown = 1 };
-
-template <int PHASE, bool GATED>
+// Up projection only: the down projection runs on one CTA per tile, which
+// measured faster for it.
+template <bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
     tc2_kernel(const ExpertTables tab, const ExpertArgs a, const TcGeom geo,
                const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap) {
@@ -75,7 +75,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
     const long long pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-    const int rows_total = a.T * a.k;
     pdl_wait();
     pdl_trigger();
 
@@ -113,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint8_t *wbase = static_cast<const uint8_t *>(a.wbase);
             for (long long u = pair; u < total && !s_abort; u += npairs) {
                 const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
-                const uint8_t *w = static_cast<const uint8_t *>(PHASE == kUp ? tab.w1[t.e] : tab.w2[t.e]);
+                const uint8_t *w = static_cast<const uint8_t *>(tab.w1[t.e]);
                 const int nv = min(kN, (t.q - t.tt * kN + 31) / 32 * 32);
                 const int brow = t.off + t.tt * kN + static_cast<int>(rank) * (nv / 2);
                 const int rb = 2 * t.rb + static_cast<int>(rank);  // this CTA's 128-row block
@@ -214,28 +213,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                               static_cast<uint32_t>(buf * kN + c0),
                           v);
                 tmem_ld_wait();
-                if (PHASE == kUp && GATED) {
+                if (GATED) {
                     const int r16 = R & 15;
                     tc_swiglu_store16(v, 1.0f, r16 < 8, static_cast<__nv_bfloat16 *>(a.h), a.p,
                                       (R >> 4) * 8 + (r16 & 7), t.off, tok0 + c0, t.q);
-                } else if (PHASE == kUp) {
+                } else {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int tok = tok0 + c0 + j;
                         if (tok < t.q)
                             static_cast<__nv_bfloat16 *>(a.h)[static_cast<size_t>(t.off + tok) * a.p + R] =
                                 __float2bfloat16_rn(fmaxf(__uint_as_float(v[j]), 0.0f));
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int tok = tok0 + c0 + j;
-                        if (tok < t.q) {
-                            const int pos = t.off + tok;
-                            const int fi = a.gather[pos];
-                            const float wgt = (fi >= 0 && fi < rows_total) ? a.topk_w[fi] : 0.0f;
-                            a.ypart[static_cast<size_t>(pos) * a.m + R] = wgt * __uint_as_float(v[j]);
-                        }
                     }
                 }
             }
@@ -266,11 +254,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int PHASE, bool GATED>
+template <bool GATED>
 cudaError_t launch_t(const ExpertArgs &a, const TcGeom &g, const CUtensorMap &amap, const CUtensorMap &bmap,
                      int num_sms, cudaStream_t s) {
     const size_t smem = 1024 + static_cast<size_t>(g.stages) * kStageBytes;
-    auto kern = tc2_kernel<PHASE, GATED>;
+    auto kern = tc2_kernel<GATED>;
     static int configured = 0, pairs = 0;
     if (static_cast<int>(smem) > configured) {
         const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -325,8 +313,8 @@ TcGeom make_geom(int K, int rows) {
 cudaError_t launch_tc2_up(const ExpertArgs &a, bool gated, const CUtensorMap &wmap, const CUtensorMap &xmap_half,
                           int num_sms, cudaStream_t s) {
     const TcGeom g = make_geom(a.m, gated ? 2 * a.p : a.p);
-    return gated ? launch_t<kUp, true>(a, g, wmap, xmap_half, num_sms, s)
-                 : launch_t<kUp, false>(a, g, wmap, xmap_half, num_sms, s);
+    return gated ? launch_t<true>(a, g, wmap, xmap_half, num_sms, s)
+                 : launch_t<false>(a, g, wmap, xmap_half, num_sms, s);
 }
 
 }  // namespace moe
