@@ -199,8 +199,18 @@ moe_status_t moe_forward_static_scratch(moe_layer_t *layer, const void *x, const
  *     tiles over two SMs) where the shapes allow (resident bf16 layers,
  *     stored rows a multiple of 256); 0 = one CTA per 128 x 256 tile.  Both
  *     give the same results up to the order of fp32 additions inside the
- *     MMA. */
-typedef enum { MOE_OPT_REGIME = 1, MOE_OPT_TIMING = 2, MOE_OPT_PAIR_TILES = 3 } moe_option_t;
+ *     MMA.
+ *   MOE_OPT_HOST_TIMEOUT_MS: the longest a call of this layer waits on the
+ *     host for device work (the paged forward's read of the token counts and
+ *     of its previous call's timing events), polling the event; past it the
+ *     call returns MOE_ERR_TIMEOUT having changed no slot state, and the layer
+ *     stays usable.  Milliseconds >= 0, or -1 for no limit; default 120000. */
+typedef enum {
+    MOE_OPT_REGIME = 1,
+    MOE_OPT_TIMING = 2,
+    MOE_OPT_PAIR_TILES = 3,
+    MOE_OPT_HOST_TIMEOUT_MS = 4
+} moe_option_t;
 moe_status_t moe_layer_set_option(moe_layer_t *layer, moe_option_t opt, int value);
 
 /* Per-phase device time of the layer's kernels, from the events that

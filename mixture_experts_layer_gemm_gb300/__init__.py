@@ -27,7 +27,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_OOM, MOE_ERR_CUDA, \
     MOE_ERR_TIMEOUT, MOE_ERR_INTERNAL = range(7)
 MOE_F32, MOE_BF16, MOE_I8 = 0, 1, 2
 MOE_EXPERT_RELU2, MOE_EXPERT_SWIGLU = 0, 1
-MOE_OPT_REGIME, MOE_OPT_TIMING, MOE_OPT_PAIR_TILES = 1, 2, 3
+MOE_OPT_REGIME, MOE_OPT_TIMING, MOE_OPT_PAIR_TILES, MOE_OPT_HOST_TIMEOUT_MS = 1, 2, 3, 4
 REGIME_AUTO, REGIME_DECODE, REGIME_BATCH = 0, 1, 2
 
 DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16, "i8": MOE_I8}
@@ -365,6 +365,10 @@ class MoELayer:
 
     def set_pair_tiles(self, on: bool):
         moe_layer_set_option(self.handle, MOE_OPT_PAIR_TILES, int(on))
+
+    def set_host_timeout_ms(self, ms: int):
+        """Longest host wait of this layer's calls (-1: no limit)."""
+        moe_layer_set_option(self.handle, MOE_OPT_HOST_TIMEOUT_MS, int(ms))
 
     def timings(self, reset=True):
         return moe_layer_timings(self.handle, reset)

@@ -16,6 +16,7 @@ struct moe_layer {
     int num_sms = 0;
     int regime = 0;  // MOE_OPT_REGIME
     bool pair_tiles = true;  // MOE_OPT_PAIR_TILES
+    int host_timeout_ms = 120000;  // MOE_OPT_HOST_TIMEOUT_MS (-1: no limit)
 
     // weights (resident copy, or unused for paged layers)
     float *wrt = nullptr;      // router [E x m] fp32
@@ -47,6 +48,7 @@ struct moe_layer {
     uint8_t *pinned_weights = nullptr;  // E experts x expert_stride, pinned host
     int32_t *counts_host = nullptr;     // pinned copy of the routing counts
     cudaEvent_t fwd_t0 = nullptr, fwd_t1 = nullptr;  // bracket a paged forward
+    cudaEvent_t counts_ready = nullptr;              // paged forward: token counts on the host
     bool fwd_pending = false;
 
     moe_stats_t stats{};
@@ -79,6 +81,11 @@ struct moe_layer {
 namespace moe {
 moe_status_t fail(moe_status_t st, const char *fmt, ...);
 moe_status_t cuda_fail(cudaError_t e, const char *where);
+// Host wait for an event with a deadline: polls the event (yielding, then
+// sleeping 20 us between polls), so that device work that does not finish
+// becomes MOE_ERR_TIMEOUT instead of a caller blocked for good.
+// timeout_ms < 0: no limit.
+moe_status_t wait_event(cudaEvent_t ev, int timeout_ms, const char *what);
 
 ExpertArgs make_expert_args(moe_layer *L, const void *x, const moe_routing_t *r);
 moe_status_t run_experts(moe_layer *L, ExpertArgs &a, int regime, int *splits_out, cudaStream_t s);

@@ -51,6 +51,23 @@ moe_status_t cuda_fail(cudaError_t e, const char *where) {
     return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
 }
 
+moe_status_t wait_event(cudaEvent_t ev, int timeout_ms, const char *what) {
+    const auto t0 = std::chrono::steady_clock::now();
+    for (long long polls = 0;; ++polls) {
+        const cudaError_t q = cudaEventQuery(ev);
+        if (q == cudaSuccess) return MOE_OK;
+        if (q != cudaErrorNotReady) return cuda_fail(q, what);
+        const long long el =
+            std::chrono::duration_cast<std::chrono::milliseconds>(std::chrono::steady_clock::now() - t0).count();
+        if (timeout_ms >= 0 && el >= timeout_ms)
+            return fail(MOE_ERR_TIMEOUT, "%s: not finished after %d ms", what, timeout_ms);
+        if (polls < 1000)
+            std::this_thread::yield();
+        else
+            std::this_thread::sleep_for(std::chrono::microseconds(20));
+    }
+}
+
 }  // namespace moe
 
 #define CUDA_TRY(expr)                                      \
@@ -168,6 +185,7 @@ moe_layer::~moe_layer() {
     if (counts_host) cudaFreeHost(counts_host);
     if (fwd_t0) cudaEventDestroy(fwd_t0);
     if (fwd_t1) cudaEventDestroy(fwd_t1);
+    if (counts_ready) cudaEventDestroy(counts_ready);
     for (cudaEvent_t ev : event_pool) cudaEventDestroy(ev);
     for (auto &pe : pending) {
         cudaEventDestroy(pe.a);
@@ -810,6 +828,11 @@ extern "C" moe_status_t moe_layer_set_option(moe_layer_t *L, moe_option_t opt, i
         L->pair_tiles = value != 0;
         return MOE_OK;
     }
+    if (opt == MOE_OPT_HOST_TIMEOUT_MS) {
+        if (value < -1) return fail(MOE_ERR_INVALID_ARG, "host timeout must be >= 0 ms, or -1");
+        L->host_timeout_ms = value;
+        return MOE_OK;
+    }
     return fail(MOE_ERR_INVALID_ARG, "unknown option %d", int(opt));
 }
 
@@ -854,7 +877,8 @@ extern "C" moe_status_t moe_layer_stats(moe_layer_t *L, moe_stats_t *out) {
     if (!L || !out) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
     if (L->fwd_pending) {  // duration of the last paged forward
         cudaSetDevice(L->device);
-        CUDA_TRY(cudaEventSynchronize(L->fwd_t1));
+        const moe_status_t w = wait_event(L->fwd_t1, L->host_timeout_ms, "the last paged call");
+        if (w != MOE_OK) return w;
         float ms = 0.0f;
         CUDA_TRY(cudaEventElapsedTime(&ms, L->fwd_t0, L->fwd_t1));
         L->stats.forward_ms += ms;
@@ -875,17 +899,8 @@ extern "C" moe_status_t moe_layer_sync_check(moe_layer_t *L, int timeout_ms, uin
             return fail(MOE_ERR_INVALID_ARG, "the layer's last stream is being captured into a graph");
         CUDA_TRY(cudaEventRecord(L->done, L->last_stream));
     }
-    const auto t0 = std::chrono::steady_clock::now();
-    for (;;) {
-        cudaError_t q = cudaEventQuery(L->done);
-        if (q == cudaSuccess) break;
-        if (q != cudaErrorNotReady) return cuda_fail(q, "cudaEventQuery");
-        const auto el = std::chrono::duration_cast<std::chrono::milliseconds>(
-            std::chrono::steady_clock::now() - t0);
-        if (timeout_ms >= 0 && el.count() > timeout_ms)
-            return fail(MOE_ERR_TIMEOUT, "layer work not finished after %d ms", timeout_ms);
-        std::this_thread::sleep_for(std::chrono::microseconds(50));
-    }
+    const moe_status_t w = wait_event(L->done, timeout_ms, "layer work");
+    if (w != MOE_OK) return w;
     uint32_t word = 0;
     CUDA_TRY(cudaMemcpy(&word, L->err_word, 4, cudaMemcpyDeviceToHost));
     if (word) {

@@ -341,10 +341,12 @@ moe_status_t paged_forward(moe_layer *L, const void *x, const moe_routing_t *r, 
                              cudaHostAllocDefault));
         PG_TRY(cudaEventCreate(&L->fwd_t0));
         PG_TRY(cudaEventCreate(&L->fwd_t1));
+        PG_TRY(cudaEventCreateWithFlags(&L->counts_ready, cudaEventDisableTiming));
     }
     // 1. token counts to the host: the one synchronisation of a paged call
-    if (L->fwd_pending) {  // the previous call's duration (its events are done after the sync)
-        PG_TRY(cudaEventSynchronize(L->fwd_t1));
+    if (L->fwd_pending) {  // the previous call's duration
+        moe_status_t w = wait_event(L->fwd_t1, L->host_timeout_ms, "the previous paged call");
+        if (w != MOE_OK) return w;
         float ms = 0.0f;
         PG_TRY(cudaEventElapsedTime(&ms, L->fwd_t0, L->fwd_t1));
         L->stats.forward_ms += ms;
@@ -352,7 +354,11 @@ moe_status_t paged_forward(moe_layer *L, const void *x, const moe_routing_t *r, 
     }
     PG_TRY(cudaEventRecord(L->fwd_t0, s));
     PG_TRY(cudaMemcpyAsync(L->counts_host, r->counts, sizeof(int32_t) * c.E, cudaMemcpyDeviceToHost, s));
-    PG_TRY(cudaStreamSynchronize(s));
+    PG_TRY(cudaEventRecord(L->counts_ready, s));
+    {
+        moe_status_t w = wait_event(L->counts_ready, L->host_timeout_ms, "the token counts");
+        if (w != MOE_OK) return w;  // no slot state changed yet
+    }
 
     // the launch plan of a resident layer for the same T (bit-identical results)
     ExpertArgs a = make_expert_args(L, x, r);

@@ -263,3 +263,43 @@ def test_injected_page_copy_failure_rolls_back_the_slot(monkeypatch):
     paged.close()
     resident.close()
     moe.moe_pool_destroy(pool)
+
+
+def test_host_wait_deadline_returns_timeout_and_the_layer_recovers():
+    """A paged forward waits on the host for the token counts with a deadline
+    (MOE_OPT_HOST_TIMEOUT_MS).  Device work queued ahead of the counts copy
+    that outlasts it makes the call return MOE_ERR_TIMEOUT before any slot is
+    looked up; with the limit restored the next calls match the resident
+    layer bit for bit."""
+    eb = _expert_bytes(SHAPE)
+    pool = moe.moe_pool_create(eb * 8, eb, 4, 0)
+    layer = wl.make_layer(SHAPE, seed=81)
+    paged = moe.MoELayer(layer, 16, pool=pool, layer_id=0)
+    resident = moe.MoELayer(layer, 16)
+    ids = np.array([[0, 1], [2, 3]], np.int32)
+    w = np.full((2, 2), 0.5, np.float32)
+    x = wl.make_tokens(SHAPE, 2, seed=82)
+    xd = to_device(x)
+    y = torch.empty((2, SHAPE.m), dtype=torch.bfloat16, device="cuda")
+    paged.route_from_topk(to_device(ids.reshape(-1)), to_device(w.reshape(-1)), T=2)
+    paged.set_host_timeout_ms(0)
+    torch.cuda._sleep(200_000_000)  # about 0.1 s of device time ahead of the counts copy
+    with pytest.raises(moe.MoeError) as ei:
+        paged.forward(xd, y)
+    assert ei.value.status == moe.MOE_ERR_TIMEOUT
+    torch.cuda.synchronize()
+    with pytest.raises(moe.MoeError) as ei:
+        paged.set_host_timeout_ms(-2)
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+    paged.set_host_timeout_ms(120000)
+    for _ in range(2):
+        rp = Run(paged, x, routing="topk", ids=ids, w=w)
+        rr = Run(resident, x, routing="topk", ids=ids, w=w)
+        np.testing.assert_array_equal(rp.y_np, rr.y_np)
+    log = moe.moe_pool_query_log(pool)
+    # the timed-out call looked nothing up: four misses, then four hits
+    assert list(log[1]) == [0, 1, 2, 3, 0, 1, 2, 3]
+    assert list(log[2]) == [0, 0, 0, 0, 1, 1, 1, 1]
+    paged.close()
+    resident.close()
+    moe.moe_pool_destroy(pool)
