@@ -381,6 +381,7 @@ static moe_status_t alloc_workspace(moe_layer_t *L) {
         if (err) return cuda_fail(err, "cudaMalloc(x_perm)");
         L->workspace_bytes += rows * c.m * 2;
     }
+    L->ypart_rows = ypart_rows;
     L->ypart = static_cast<float *>(L->dalloc(ypart_rows * c.m * 4, &err));
     if (err) return cuda_fail(err, "cudaMalloc(ypart)");
     L->err_word = static_cast<uint32_t *>(L->dalloc(8, &err));
@@ -662,7 +663,14 @@ static moe_status_t run_experts_tc(moe_layer_t *L, ExpertArgs &a, int *splits_ou
         s_down = tc_splits(c.p / bk, c.m, N, mean_q, n_act, L->num_sms, L->split_down_max);
         a.n_rows_cap = static_cast<int>(L->decode_rows_cap);
     } else {
+        // batch: the down projection's tiles (128 output rows x a token tile,
+        // the whole reduction of p) can be too few to fill the SMs evenly; it
+        // splits the reduction in two where that evens out the waves and the
+        // partial-sum workspace has room (measured, Mixtral shape T = 2048:
+        // 418 -> 393 us; four splits at T = 512 measured slower than none)
         a.n_rows_cap = rows;
+        if (L->ypart_rows >= 2 * static_cast<size_t>(rows))
+            s_down = tc_splits(c.p / bk, c.m, N, mean_q, c.E, L->num_sms, 2);
     }
     // The up projection's 256-token tiles run on CTA pairs (less shared-memory
     // traffic per SM; measured faster) when its matrix comes in 256-row pair
