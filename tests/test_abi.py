@@ -127,3 +127,74 @@ def test_transfer_threshold_is_where_loading_stops_dominating():
     closed = phi * dtype / (2 * beta)
     assert q - 1 <= closed < q
     assert 16 < closed / 100  # decode (q <= 16 per expert) is link-bound by two orders of magnitude
+
+
+def _header_text():
+    return re.sub(r"/\*.*?\*/", " ", open(moe.HEADER_PATH).read(), flags=re.S)
+
+
+def _int_expr(src):
+    """Value of an integer constant of the header: a literal (decimal or hex,
+    optional u suffix) or a left shift of two of them."""
+    if "<<" in src:
+        a, b = src.split("<<")
+        return _int_expr(a) << _int_expr(b)
+    return int(re.sub(r"[uUlL]+$", "", src.strip()), 0)
+
+
+def _header_constants(text):
+    values = {m.group(1): _int_expr(m.group(2))
+              for m in re.finditer(r"\b(MOE_\w+)\s*=\s*([^,}]+)", text)}
+    values.update({m.group(1): int(m.group(2)) for m in re.finditer(r"#define\s+(MOE_\w+)\s+(\d+)", text)})
+    return values
+
+
+_C_SIZES = {"int": 4, "int32_t": 4, "uint32_t": 4, "uint64_t": 8, "size_t": 8, "double": 8, "float": 4,
+            "moe_dtype_t": 4, "moe_expert_t": 4}
+
+
+def _header_structs(text):
+    """{name: [(member, element bytes, count)]} of every typedef struct { ... } name;"""
+    defines = _header_constants(text)
+    out = {}
+    for m in re.finditer(r"typedef\s+struct\s*\{(.*?)\}\s*(\w+)\s*;", text, flags=re.S):
+        members = []
+        for decl in m.group(1).split(";"):
+            decl = decl.strip()
+            if not decl:
+                continue
+            ctype, rest = decl.split(None, 1)
+            for name in rest.split(","):
+                name = name.strip()
+                size = 8 if name.startswith("*") else _C_SIZES[ctype]
+                name = name.lstrip("*").strip()
+                count = 1
+                arr = re.match(r"(\w+)\s*\[(\w+)\]", name)
+                if arr:
+                    name = arr.group(1)
+                    count = defines.get(arr.group(2)) or int(arr.group(2))
+                members.append((name, size, count))
+        out[m.group(2)] = members
+    return out
+
+
+def test_binding_structs_mirror_the_header():
+    """Every struct the binding passes through the C ABI has the header's
+    members, in order, with the same element sizes."""
+    structs = _header_structs(_header_text())
+    for name in ("moe_config_t", "moe_routing_t", "moe_layer_info_t", "moe_timings_t", "moe_stats_t"):
+        py = getattr(moe, name)
+        got = []
+        for fname, ftype in py._fields_:
+            count = getattr(ftype, "_length_", 1)
+            elem = ftype._type_ if count > 1 else ftype
+            got.append((fname, ctypes.sizeof(elem), count))
+        assert got == structs[name], name
+
+
+def test_binding_constants_match_the_header():
+    values = _header_constants(_header_text())
+    shared = [k for k in values if hasattr(moe, k)]
+    assert len(shared) >= 20, shared
+    for k in shared:
+        assert getattr(moe, k) == values[k], k
