@@ -4,8 +4,14 @@
 // their owner).  The routing weight was applied in the down-projection
 // epilogue; a split-K down projection leaves `splits` partial rows, added
 // here first (in a fixed order over the splits), then the k slots (in
-// ascending j), in fp32,
-// rounded once to the activation type.  Deterministic: no atomics.
+// ascending j), in fp32, rounded once to the activation type.
+// Deterministic: no atomics.
+//
+// The kernel is bound by HBM (the partial rows are read once): each thread
+// reads all k of its token's permuted positions first and then issues every
+// partial-row load of the token before adding any of them, so that the loads
+// of all slots are in flight together instead of one slot's address waiting
+// on the previous slot's data.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -13,75 +19,131 @@ namespace moe {
 
 namespace {
 
-template <bool BF16>
+// W consecutive fp32 values of one partial row, loaded with 16-byte loads
+// that bypass L1 (each partial row is read once).
+template <int W>
+struct Vec {
+    float v[W];
+    __device__ __forceinline__ void load(const float *p) {
+#pragma unroll
+        for (int i = 0; i < W; i += 4) {
+            const float4 q = __ldcg(reinterpret_cast<const float4 *>(p + i));
+            v[i] = q.x;
+            v[i + 1] = q.y;
+            v[i + 2] = q.z;
+            v[i + 3] = q.w;
+        }
+    }
+};
+
+// W outputs per thread (4 or 8 consecutive features of one token); KMAX >= k.
+template <bool BF16, int KMAX, int W>
 __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
     pdl_wait();
     pdl_trigger();
-    const int vec = a.m / 4;  // 4 fp32 per thread
+    const int vec = a.m / W;
     const long long n = static_cast<long long>(a.T) * vec;
     const int rows = a.T * a.k;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int t = static_cast<int>(i / vec), c = static_cast<int>(i % vec) * 4;
-        float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < a.k; ++j) {
-            const int pos = a.scatter[static_cast<size_t>(t) * a.k + j];
-            if (pos < 0 || pos >= rows) {
-                flag_error(a.err, kErrGatherIndex);
-                continue;
+        const int t = static_cast<int>(i / vec), c = static_cast<int>(i % vec) * W;
+        int pos[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            pos[j] = -1;
+            if (j < a.k) {
+                const int p = a.scatter[static_cast<size_t>(t) * a.k + j];
+                if (p < 0 || p >= rows)
+                    flag_error(a.err, kErrGatherIndex);
+                else
+                    pos[j] = p;
             }
-            // partial rows of the split reduction, four loads in flight at a
-            // time, added in a fixed order: ((p0 + p1) + (p2 + p3)) per group,
-            // groups in split order
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float *base = a.ypart + static_cast<size_t>(pos) * a.m + c;
-            int s = 0;
-            for (; s + 4 <= a.splits; s += 4) {
-                const float4 p0 = __ldcg(reinterpret_cast<const float4 *>(base + (s + 0) * a.split_stride));
-                const float4 p1 = __ldcg(reinterpret_cast<const float4 *>(base + (s + 1) * a.split_stride));
-                const float4 p2 = __ldcg(reinterpret_cast<const float4 *>(base + (s + 2) * a.split_stride));
-                const float4 p3 = __ldcg(reinterpret_cast<const float4 *>(base + (s + 3) * a.split_stride));
-                v.x += (p0.x + p1.x) + (p2.x + p3.x);
-                v.y += (p0.y + p1.y) + (p2.y + p3.y);
-                v.z += (p0.z + p1.z) + (p2.z + p3.z);
-                v.w += (p0.w + p1.w) + (p2.w + p3.w);
+        }
+        float y[W];
+#pragma unroll
+        for (int e = 0; e < W; ++e) y[e] = 0.0f;
+        if (a.splits == 1) {
+            Vec<W> q[KMAX];
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+#pragma unroll
+                for (int e = 0; e < W; ++e) q[j].v[e] = 0.0f;
+                if (pos[j] >= 0) q[j].load(a.ypart + static_cast<size_t>(pos[j]) * a.m + c);
             }
-            for (; s < a.splits; ++s) {
-                const float4 p = __ldcg(reinterpret_cast<const float4 *>(base + s * a.split_stride));
-                v.x += p.x;
-                v.y += p.y;
-                v.z += p.z;
-                v.w += p.w;
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                if (pos[j] >= 0)
+#pragma unroll
+                    for (int e = 0; e < W; ++e) y[e] += 0.0f + q[j].v[e];
+        } else {
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                if (pos[j] < 0) continue;
+                // partial rows of the split reduction, four loads in flight at
+                // a time, added in a fixed order: ((p0 + p1) + (p2 + p3)) per
+                // group, groups in split order
+                const float *base = a.ypart + static_cast<size_t>(pos[j]) * a.m + c;
+                float v[W];
+#pragma unroll
+                for (int e = 0; e < W; ++e) v[e] = 0.0f;
+                int s = 0;
+                for (; s + 4 <= a.splits; s += 4) {
+                    Vec<W> p0, p1, p2, p3;
+                    p0.load(base + (s + 0) * a.split_stride);
+                    p1.load(base + (s + 1) * a.split_stride);
+                    p2.load(base + (s + 2) * a.split_stride);
+                    p3.load(base + (s + 3) * a.split_stride);
+#pragma unroll
+                    for (int e = 0; e < W; ++e) v[e] += (p0.v[e] + p1.v[e]) + (p2.v[e] + p3.v[e]);
+                }
+                for (; s < a.splits; ++s) {
+                    Vec<W> p;
+                    p.load(base + s * a.split_stride);
+#pragma unroll
+                    for (int e = 0; e < W; ++e) v[e] += p.v[e];
+                }
+#pragma unroll
+                for (int e = 0; e < W; ++e) y[e] += v[e];
             }
-            y.x += v.x;
-            y.y += v.y;
-            y.z += v.z;
-            y.w += v.w;
         }
         if (BF16) {
-            uint2 o;
-            o.x = pack_bf16x2(y.x, y.y);
-            o.y = pack_bf16x2(y.z, y.w);
-            *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(a.y) +
-                                       static_cast<size_t>(t) * a.m + c) = o;
+            uint32_t o[W / 2];
+#pragma unroll
+            for (int e = 0; e < W / 2; ++e) o[e] = pack_bf16x2(y[2 * e], y[2 * e + 1]);
+            __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.y) + static_cast<size_t>(t) * a.m + c;
+            if (W == 8)
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(o[0], o[1], o[W / 2 - 2], o[W / 2 - 1]);
+            else
+                *reinterpret_cast<uint2 *>(dst) = make_uint2(o[0], o[1]);
         } else {
-            *reinterpret_cast<float4 *>(static_cast<float *>(a.y) + static_cast<size_t>(t) * a.m +
-                                        c) = y;
+            float *dst = static_cast<float *>(a.y) + static_cast<size_t>(t) * a.m + c;
+#pragma unroll
+            for (int e = 0; e < W; e += 4) *reinterpret_cast<float4 *>(dst + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
         }
     }
+}
+
+template <bool BF16, int KMAX>
+cudaError_t launch_w(const CombineArgs &a, cudaStream_t s) {
+    const int w = (a.m % 8 == 0) ? 8 : 4;
+    const long long n = static_cast<long long>(a.T) * (a.m / w);
+    long long blocks = (n + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    const dim3 grid(static_cast<unsigned>(blocks));
+    return w == 8 ? launch_pdl(combine_kernel<BF16, KMAX, 8>, grid, dim3(256), 0, s, a)
+                  : launch_pdl(combine_kernel<BF16, KMAX, 4>, grid, dim3(256), 0, s, a);
+}
+
+template <bool BF16>
+cudaError_t launch_k(const CombineArgs &a, cudaStream_t s) {
+    return a.k <= 2 ? launch_w<BF16, 2>(a, s) : launch_w<BF16, kMaxTopK>(a, s);
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const CombineArgs &a, bool act_bf16, cudaStream_t s) {
-    const long long n = static_cast<long long>(a.T) * (a.m / 4);
-    if (n == 0) return cudaSuccess;
-    long long blocks = (n + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
-    if (act_bf16)
-        return launch_pdl(combine_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, a);
-    else
-        return launch_pdl(combine_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, a);
+    if (static_cast<long long>(a.T) * a.m == 0) return cudaSuccess;
+    return act_bf16 ? launch_k<true>(a, s) : launch_k<false>(a, s);
 }
 
 }  // namespace moe

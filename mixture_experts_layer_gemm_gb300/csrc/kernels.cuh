@@ -45,6 +45,9 @@ struct PermuteArgs {
     const int32_t *ids;  // [T*k]
     int T, k, E;
     int32_t *counts, *offsets, *gather, *scatter;
+    // per-CTA expert counts of a multi-CTA fused router permute
+    // ([ceil(T / 16) x E], overwritten by their prefix over CTAs), or nullptr
+    int32_t *cta_count;
 };
 
 // Router + top-k with the permute fused in (the launch's last CTA runs it).

@@ -18,6 +18,7 @@ struct moe_layer {
     bool pair_tiles = true;  // MOE_OPT_PAIR_TILES
     int host_timeout_ms = 120000;  // MOE_OPT_HOST_TIMEOUT_MS (-1: no limit)
     size_t ypart_rows = 0;  // fp32 partial rows the down projection's workspace holds
+    int32_t *cta_count = nullptr;  // router permute: per-CTA expert counts
 
     // weights (resident copy, or unused for paged layers)
     float *wrt = nullptr;      // router [E x m] fp32

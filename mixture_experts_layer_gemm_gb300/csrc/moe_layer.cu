@@ -384,6 +384,12 @@ static moe_status_t alloc_workspace(moe_layer_t *L) {
     L->ypart_rows = ypart_rows;
     L->ypart = static_cast<float *>(L->dalloc(ypart_rows * c.m * 4, &err));
     if (err) return cuda_fail(err, "cudaMalloc(ypart)");
+    {  // one row of expert counts per 16-token router CTA
+        const size_t n = static_cast<size_t>((c.max_tokens + 15) / 16) * c.E;
+        L->cta_count = static_cast<int32_t *>(L->dalloc(n * 4, &err));
+        if (err) return cuda_fail(err, "cudaMalloc(router permute counts)");
+        L->workspace_bytes += n * 4;
+    }
     L->err_word = static_cast<uint32_t *>(L->dalloc(8, &err));
     if (err) return cuda_fail(err, "cudaMalloc(error word)");
     CUDA_TRY(cudaMemset(L->err_word, 0, 8));
@@ -451,7 +457,7 @@ extern "C" moe_status_t moe_destroy(moe_layer_t *L) {
 // ---- routing ---------------------------------------------------------------------------
 static moe_status_t run_permute(moe_layer_t *L, int T, moe_routing_t *r, cudaStream_t s) {
     PermuteArgs pa{r->topk_ids, T, L->cfg.k, L->cfg.E, r->counts, r->offsets, r->gather_index,
-                   r->scatter_index};
+                   r->scatter_index, nullptr};
     moe_status_t st = launch_phase(L, MOE_PHASE_PERMUTE, s, "permute", [&] { return launch_permute(pa, s); });
     if (st != MOE_OK) return st;
     L->last_stream = s;
@@ -479,7 +485,7 @@ extern "C" moe_status_t moe_route(moe_layer_t *L, const void *x, int T, moe_rout
     RouterArgs ra{x, L->wrt, L->wra, L->bias, T, L->cfg.m, L->cfg.E, L->cfg.k, r->topk_ids,
                   r->topk_w, r->logits, L->ticket, L->err_word};
     PermuteArgs pa{r->topk_ids, T, L->cfg.k, L->cfg.E, r->counts, r->offsets, r->gather_index,
-                   r->scatter_index};
+                   r->scatter_index, L->cta_count};
     st = launch_phase(L, MOE_PHASE_ROUTER, s, "router_topk_permute",
                       [&] { return launch_router_topk(ra, pa, L->cfg.act_dtype == MOE_BF16, s); });
     if (st != MOE_OK) return st;

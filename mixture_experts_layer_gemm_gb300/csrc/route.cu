@@ -187,6 +187,118 @@ __device__ void permute_block(const PermuteArgs &a, PermuteSmem &sm) {
     }
 }
 
+// The permute of a multi-CTA router launch, in two parts, so that no single
+// CTA walks the whole batch with block barriers.  Each CTA first ranks its own
+// (token, slot) pairs [i0, i0 + n): a pair's rank is the number of earlier
+// pairs of the CTA with the same expert (stable by flat index).  Warp 0 only;
+// the rank goes to scatter[i] for now and the CTA's per-expert counts to
+// cta_count[cta][e].  s_cnt: kMaxExperts ints of shared memory.
+__device__ void permute_rank_local(const PermuteArgs &a, int i0, int n, int cta, int *s_cnt, int lane) {
+    for (int e = lane; e < a.E; e += 32) s_cnt[e] = 0;
+    __syncwarp();
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int c0 = 0; c0 < n; c0 += 32) {
+        const bool valid = c0 + lane < n;
+        int id = valid ? __ldcg(a.ids + i0 + c0 + lane) : -1;
+        if (valid && (id < 0 || id >= a.E)) id = 0;  // flagged by whoever produced ids
+        const unsigned peers = __match_any_sync(0xffffffffu, id);
+        const int base = valid ? s_cnt[id] : 0;
+        __syncwarp();
+        if (valid) {
+            a.scatter[i0 + c0 + lane] = base + __popc(peers & lt_mask);
+            if (lane == __ffs(peers) - 1) s_cnt[id] = base + __popc(peers);
+        }
+        __syncwarp();
+    }
+    for (int e = lane; e < a.E; e += 32) a.cta_count[static_cast<size_t>(cta) * a.E + e] = s_cnt[e];
+}
+
+// The launch's last CTA, once every CTA ranked its pairs: per expert, the
+// exclusive prefix of the counts over CTAs (one warp per expert, in place);
+// the expert totals, counts and offsets; then every pair in parallel at
+// offsets[e] + prefix[cta][e] + rank.  The result is the stable counting sort
+// of permute_block.
+__device__ void permute_finish(const PermuteArgs &a, int ncta, int per_cta, PermuteSmem &sm) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    // loads are issued in batches of kB, so that a batch costs one round trip
+    // to L2 instead of one per element
+    constexpr int kB = 8;
+    for (int e = warp; e < a.E; e += nwarps) {
+        int carry = 0;
+        for (int c0 = 0; c0 < ncta; c0 += 32 * kB) {
+            int v[kB];
+#pragma unroll
+            for (int b = 0; b < kB; ++b) {
+                const int c = c0 + 32 * b + lane;
+                v[b] = c < ncta ? __ldcg(a.cta_count + static_cast<size_t>(c) * a.E + e) : 0;
+            }
+#pragma unroll
+            for (int b = 0; b < kB; ++b) {
+                const int c = c0 + 32 * b + lane;
+                int incl = v[b];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int x = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += x;
+                }
+                if (c < ncta) a.cta_count[static_cast<size_t>(c) * a.E + e] = carry + incl - v[b];
+                carry += __shfl_sync(0xffffffffu, incl, 31);
+            }
+        }
+        if (lane == 0) sm.count[e] = carry;
+    }
+    __syncthreads();
+    if (warp == 0) {  // exclusive scan over E <= 64 totals, two per lane
+        const int c0 = (2 * lane < a.E) ? sm.count[2 * lane] : 0;
+        const int c1 = (2 * lane + 1 < a.E) ? sm.count[2 * lane + 1] : 0;
+        int incl = c0 + c1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const int excl = incl - c0 - c1;
+        if (2 * lane < a.E) {
+            sm.base[2 * lane] = excl;
+            a.counts[2 * lane] = c0;
+            a.offsets[2 * lane] = excl;
+        }
+        if (2 * lane + 1 < a.E) {
+            sm.base[2 * lane + 1] = excl + c0;
+            a.counts[2 * lane + 1] = c1;
+            a.offsets[2 * lane + 1] = excl + c0;
+        }
+        if (lane == 31) a.offsets[a.E] = incl;
+    }
+    __syncthreads();
+    const int n = a.T * a.k;
+    const int nthreads = blockDim.x;
+    for (int i0 = 0; i0 < n; i0 += nthreads * kB) {
+        int id[kB], rank[kB], pre[kB];
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            const int i = i0 + b * nthreads + tid;
+            id[b] = i < n ? __ldcg(a.ids + i) : 0;
+            rank[b] = i < n ? __ldcg(a.scatter + i) : 0;
+            if (id[b] < 0 || id[b] >= a.E) id[b] = 0;
+        }
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            const int i = i0 + b * nthreads + tid;
+            pre[b] = i < n ? __ldcg(a.cta_count + static_cast<size_t>(i / per_cta) * a.E + id[b]) : 0;
+        }
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            const int i = i0 + b * nthreads + tid;
+            if (i < n) {
+                const int pos = sm.base[id[b]] + pre[b] + rank[b];
+                a.gather[pos] = i;
+                a.scatter[i] = pos;
+            }
+        }
+    }
+}
+
 // Router GEMM + softmax + top-k, with the permute fused in.
 // One CTA per group of TOK tokens (TOK * EMAX <= 64).  The 256 threads split
 // the hidden dimension into 16-byte chunks (chunk c goes to thread c mod 256);
@@ -436,6 +548,10 @@ __global__ void __launch_bounds__(router_warps<EMAX>() * 32) router_mma_kernel(R
         }
         return;
     }
+    if (pa.cta_count) {  // this CTA ranks its own pairs first
+        __syncthreads();
+        if (warp == 0) permute_rank_local(pa, t0 * a.k, ntok * a.k, blockIdx.x, psm.count, lane);
+    }
     __threadfence();
     __syncthreads();
     if (tid == 0) {
@@ -445,7 +561,10 @@ __global__ void __launch_bounds__(router_warps<EMAX>() * 32) router_mma_kernel(R
     __syncthreads();
     if (s_last) {
         __threadfence();
-        permute_block(pa, psm);
+        if (pa.cta_count)
+            permute_finish(pa, gridDim.x, TOK * a.k, psm);
+        else
+            permute_block(pa, psm);
         if (tid == 0) *a.ticket = 0;  // ready for the next launch
     }
 }
