@@ -268,22 +268,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // x_perm[pos] = x[gather[pos] / k] for the permuted rows (16-byte vectors).
+// HBM-bound: a block takes kR rows at a time, reads their gather indices once,
+// and its threads stride over the 16-byte vectors of the rows with the kR
+// rows' loads issued together before the stores.
+constexpr int kGatherRows = 4;
+
 __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ gather,
                                    int rows, int k, int m, uint16_t *__restrict__ xp, uint32_t *err) {
     pdl_wait();
     pdl_trigger();
     const int vec = m / 8;
-    const long long n = static_cast<long long>(rows) * vec;
-    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
-         i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int pos = static_cast<int>(i / vec), v = static_cast<int>(i % vec);
-        const int fi = gather[pos];
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (fi >= 0 && fi < rows)
-            val = ld_nc_v4(x + static_cast<size_t>(fi / k) * m + v * 8);
-        else if (v == 0)
-            flag_error(err, kErrGatherIndex);
-        *reinterpret_cast<uint4 *>(xp + static_cast<size_t>(pos) * m + v * 8) = val;
+    for (int r0 = blockIdx.x * kGatherRows; r0 < rows; r0 += gridDim.x * kGatherRows) {
+        int fi[kGatherRows];
+#pragma unroll
+        for (int b = 0; b < kGatherRows; ++b) {
+            fi[b] = -1;
+            if (r0 + b < rows) {
+                const int f = gather[r0 + b];
+                if (f >= 0 && f < rows)
+                    fi[b] = f;
+                else if (threadIdx.x == 0)
+                    flag_error(err, kErrGatherIndex);
+            }
+        }
+        for (int v = threadIdx.x; v < vec; v += blockDim.x) {
+            uint4 val[kGatherRows];
+#pragma unroll
+            for (int b = 0; b < kGatherRows; ++b)
+                val[b] = fi[b] >= 0 ? ld_nc_v4(x + static_cast<size_t>(fi[b] / k) * m + v * 8)
+                                    : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int b = 0; b < kGatherRows; ++b)
+                if (r0 + b < rows)
+                    *reinterpret_cast<uint4 *>(xp + static_cast<size_t>(r0 + b) * m + v * 8) = val[b];
+        }
     }
 }
 
@@ -324,9 +342,8 @@ TcGeom make_tc_geom(int K, int rows, int splits, int N) {
 
 cudaError_t launch_gather_rows(const void *x, const int32_t *gather, int rows, int k, int m,
                                void *x_perm, uint32_t *err, cudaStream_t s) {
-    const long long n = static_cast<long long>(rows) * (m / 8);
-    if (n == 0) return cudaSuccess;
-    long long blocks = (n + 255) / 256;
+    if (rows <= 0) return cudaSuccess;
+    long long blocks = (rows + kGatherRows - 1) / kGatherRows;
     if (blocks > 152 * 8) blocks = 152 * 8;
     return launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
                       static_cast<const uint16_t *>(x), gather, rows, k, m,
