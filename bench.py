@@ -229,7 +229,13 @@ def run_reference(args, world, rank):
     import torch
     device = "cuda" if torch.cuda.is_available() else "cpu"
     layer, xs = make_inputs(shape, args.seed, device)
-    sample = {1: 1, 4: 1, 16: 0, 64: 0}   # 2 tokens of experts per step, every token routed
+    # Every token is routed each step; the expert MLPs run for one token per
+    # host thread, taken from the batch that has that many (the oracle runs its
+    # tokens in parallel, so a step costs about one token's MLPs).
+    threads = cpu_threads()
+    t_big = max(TOKENS, key=lambda T: min(T, threads))
+    n_exp = min(t_big, threads)
+    sample = {T: (n_exp if T == t_big else 0) for T in TOKENS}
     for _ in range(args.warmup):
         oracle_sample(layer, xs, sample)
     t0 = time.perf_counter()
@@ -245,8 +251,9 @@ def run_reference(args, world, rank):
             "config": workload_config(shape, args.weights, "n/a (CPU)"),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(),
                              "kind": "oracle",
-                             "sample": "per step: router + top-k for all 85 tokens of the four "
-                                       "batches, expert MLPs for 1 token of T=1 and 1 of T=4"},
+                             "sample": f"per step: router + top-k for all {sum(TOKENS)} tokens of the "
+                                       f"batches, expert MLPs for {n_exp} tokens of the T={t_big} batch "
+                                       "(one per host thread), fp64"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
