@@ -489,3 +489,17 @@ def test_int8_activation_range(regime):
     rel, _ = max_token_rel_l2(run.y_np, ref)
     assert rel <= 1e-2, rel
     ml.close()
+
+
+@pytest.mark.parametrize("T", [4100, 9000])
+def test_routing_of_many_router_ctas(T):
+    """Batches of more than 256 router CTAs (16 tokens each): the distributed
+    permute's prefix over CTAs runs in several batches; ids, counts, offsets
+    and both index tables must equal the oracle's (routing only)."""
+    layer = get_layer(SWIGLU_BF16, seed=67)
+    x = wl.make_tokens(SWIGLU_BF16, T, seed=68)
+    ml = moe.MoELayer(layer, T, with_logits=True)
+    run = Run(ml, x, forward=False)
+    assert ml.sync_check()[0] == moe.MOE_OK
+    check_routing(run, layer, x)
+    ml.close()
