@@ -111,14 +111,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 #pragma unroll
             for (int e = 0; e < W / 2; ++e) o[e] = pack_bf16x2(y[2 * e], y[2 * e + 1]);
             __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.y) + static_cast<size_t>(t) * a.m + c;
-            if (W == 8)
-                *reinterpret_cast<uint4 *>(dst) = make_uint4(o[0], o[1], o[W / 2 - 2], o[W / 2 - 1]);
+            if constexpr (W == 8)
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
             else
                 *reinterpret_cast<uint2 *>(dst) = make_uint2(o[0], o[1]);
         } else {
             float *dst = static_cast<float *>(a.y) + static_cast<size_t>(t) * a.m + c;
 #pragma unroll
-            for (int e = 0; e < W; e += 4) *reinterpret_cast<float4 *>(dst + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
+            for (int e = 0; e < W; e += 4)
+                *reinterpret_cast<float4 *>(dst + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
         }
     }
 }
