@@ -444,8 +444,11 @@ def run_ours(args, world, rank, local):
                     "avg_launch_us": up_ms * 1e3 / max(up_n, 1), "traffic": None}
     else:
         achieved = bytes_up * args.steps / (up_ms * 1e-3) / 1e9
-        roofline = {"kernel": "expert up-projection (W1 and W3 + SiLU*gate): decode GEMV for "
-                              "T <= 16, tcgen05 for larger T",
+        gemv_t = [T for T in TOKENS if work[T]["path"] == "gemv"]
+        tc_t = [T for T in TOKENS if work[T]["path"] != "gemv"]
+        paths = ", ".join(p for p in (f"decode GEMV for T in {gemv_t}" if gemv_t else "",
+                                      f"tcgen05 for T in {tc_t}" if tc_t else "") if p)
+        roofline = {"kernel": f"expert up-projection (W1 and W3 + SiLU*gate): {paths}",
                     "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                     "frac": achieved / hbm, "peak_source": f"{src} (hbm_gbs)",
                     "algorithmic_bytes_per_step": bytes_up,

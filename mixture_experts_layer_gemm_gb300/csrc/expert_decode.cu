@@ -64,13 +64,11 @@ template <WeightType WT>
 struct WTraits;
 template <>
 struct WTraits<WeightType::kBF16> {
-    static constexpr int kElem = 2;
     static constexpr int kBK = 64;      // reduction elements per 2 KB block
     static constexpr int kPad = 64;     // staged token-row padding: conflict-free B reads
 };
 template <>
 struct WTraits<WeightType::kI8> {
-    static constexpr int kElem = 1;
     static constexpr int kBK = 128;
     static constexpr int kPad = 16;
 };
@@ -136,17 +134,26 @@ __device__ __forceinline__ void stage_rows_f16(uint8_t *bstage, int row_bytes, i
     }
 }
 
+// Work entries are (expert, token pass) pairs: an expert with more tokens
+// than one pass holds gets one entry per pass, so that the units of a pass
+// are consecutive and a CTA stages each (pass, split) of token rows once.
+// Passes per expert are at most q / kTok + 1, so at most E + (T k) / 8 entries
+// (T k <= 512 on this path).
+constexpr int kMaxPassEntries = kMaxExperts + 512 / 8;
+
 struct Unit {
-    int e, ks, g8, nrg, off, end, kb0, kb1;
+    int e, tp, ks, g8, nrg, off, end, kb0, kb1;
     bool ok;
 };
 
-__device__ __forceinline__ Unit decode_unit(long long u, const int *s_act, const DecodeGeom &geo,
+__device__ __forceinline__ Unit decode_unit(long long u, const int *s_act, const int *s_tp, const DecodeGeom &geo,
                                             const ExpertArgs &a, int rows_total) {
     Unit U;
     U.g8 = static_cast<int>(u % geo.rg8);
     U.ks = static_cast<int>((u / geo.rg8) % geo.splits);
-    U.e = s_act[static_cast<int>(u / (static_cast<long long>(geo.rg8) * geo.splits))];
+    const int entry = static_cast<int>(u / (static_cast<long long>(geo.rg8) * geo.splits));
+    U.e = s_act[entry];
+    U.tp = s_tp[entry];
     U.nrg = min(8, geo.rg - 8 * U.g8);
     U.off = a.offsets[U.e];
     U.end = a.offsets[U.e + 1];
@@ -163,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kTok = 8 * NT;  // tokens per pass
     constexpr int kBK = WTraits<WT>::kBK;
     __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
-    __shared__ int s_act[kMaxExperts];
+    __shared__ int s_act[kMaxPassEntries], s_tp[kMaxPassEntries];  // (expert, pass) entries
     __shared__ int s_nact;
     __shared__ volatile int s_abort;
     __shared__ float s_xscale[kTok], s_xsum[kTok];  // int8: per staged row, 2^s and sum of x 2^-s
@@ -186,11 +193,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         int n = 0;
+        // one entry per token pass of each expert; a malformed segment keeps
+        // one entry, whose unit then reports it
+        auto add = [&](int e) {
+            const int off = a.offsets[e], end = a.offsets[e + 1];
+            const int q = (off < 0 || end > rows_total || end < off) ? 1 : end - off;
+            for (int tp = 0; tp * kTok < q; ++tp) {
+                if (n == kMaxPassEntries) {
+                    flag_error(a.err, kErrOffsets);
+                    return;
+                }
+                s_act[n] = e;
+                s_tp[n] = tp;
+                ++n;
+            }
+        };
         if (a.n_only > 0) {
-            for (int i = 0; i < a.n_only && i < kMaxExperts; ++i) s_act[n++] = a.only[i];
+            for (int i = 0; i < a.n_only && i < kMaxExperts; ++i) add(a.only[i]);
         } else {
             for (int e = 0; e < a.E; ++e)
-                if (a.offsets[e + 1] > a.offsets[e]) s_act[n++] = e;
+                if (a.offsets[e + 1] > a.offsets[e]) add(e);
         }
         s_nact = n;
         s_abort = 0;
@@ -219,12 +241,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             for (long long u = u_begin; u < u_end && !s_abort; ++u) {
-                const Unit U = decode_unit(u, s_act, geo, a, rows_total);
+                const Unit U = decode_unit(u, s_act, s_tp, geo, a, rows_total);
                 if (!U.ok) continue;
                 const uint8_t *w = static_cast<const uint8_t *>(PHASE == kUp ? tab.w1[U.e] : tab.w2[U.e]);
                 const uint32_t bytes = static_cast<uint32_t>(U.nrg) * kBlockBytes;
                 const int q = U.end - U.off;
-                for (int tp = 0; tp * kTok < q && !s_abort; ++tp) {
+                {  // this unit's pass
                     for (int kb = U.kb0; kb < U.kb1; ++kb) {
                         if (!mbar_wait(&empty_bar[stage], phase ^ 1u)) {
                             flag_error(a.err, kErrWaitTimeout);
@@ -262,17 +284,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (long long u = u_begin; u < u_end; ++u) {
         // one decision for all consumer warps: the named barriers need all of them
         if (named_sync_or(kBarConsumers, kConsumers, s_abort)) break;
-        const Unit U = decode_unit(u, s_act, geo, a, rows_total);
+        const Unit U = decode_unit(u, s_act, s_tp, geo, a, rows_total);
         if (!U.ok) {
             if (tid == 0) flag_error(a.err, kErrOffsets);
             continue;
         }
-        const int q = U.end - U.off;
         const int kbase = U.kb0 * kBK;                 // first reduction element of the split
         const int kcount = (U.kb1 - U.kb0) * kBK;
         const bool mine = warp < U.nrg;
         const int rg = 8 * U.g8 + warp;
-        for (int tp = 0; tp * kTok < q; ++tp) {
+        {
+            const int tp = U.tp;  // this unit's token pass
             // ---- stage this pass's token rows (bf16) in shared memory
             if (staged_e != U.e || staged_ks != U.ks || staged_tp != tp) {
                 named_sync(kBarConsumers, kConsumers);
@@ -499,6 +521,7 @@ cudaError_t dispatch_nt(const ExpertArgs &a, int nt, int K, int rows, int splits
     switch (nt) {
     case 1: return launch_one<WT, PHASE, GATED, 1>(a, K, rows, splits, num_sms, s);
     case 2: return launch_one<WT, PHASE, GATED, 2>(a, K, rows, splits, num_sms, s);
+    case 3: return launch_one<WT, PHASE, GATED, 3>(a, K, rows, splits, num_sms, s);
     default: return launch_one<WT, PHASE, GATED, 4>(a, K, rows, splits, num_sms, s);
     }
 }
@@ -509,16 +532,17 @@ cudaError_t dispatch_nt(const ExpertArgs &a, int nt, int K, int rows, int splits
 // streams its weights once per pass, so the pass is sized for the busier
 // experts, not the mean: under uniform routing an expert's count has mean
 // T k / E and variance T k (1/E)(1 - 1/E), and the pass covers the mean plus
-// 1.5 standard deviations.  Four tiles (32 tokens) stage four times the rows
-// and cost more reduction splits, so two tiles are kept while their 16 tokens
-// cover all but a few experts (Mixtral shape, T = 48: two tiles 362 us, four
-// tiles 495 us; T = 56 with two tiles, where most experts need a second pass:
-// 1040 us).
+// 1.5 standard deviations.  Every tile adds MMAs per widened weight and
+// staged rows, so the smallest pass that covers them is taken (Mixtral shape,
+// int8, T = 64: 24-token passes 456 us per layer, 32-token passes 513 us).  An
+// expert with more tokens still takes further passes (its own work entries),
+// each streaming its weights again.
 int decode_token_tiles(int T, int k, int E) {
     const double mean = static_cast<double>(T) * k / E;
     const double hi = mean + 1.5 * std::sqrt(mean * (1.0 - 1.0 / E)) + 0.5;
     if (hi <= 8.0) return 1;
     if (hi <= 18.0) return 2;
+    if (hi <= 24.0) return 3;
     return 4;
 }
 

@@ -92,7 +92,10 @@ constexpr int kSplitUpMax = 4, kSplitDownMax = 16;
 // crossover, Mixtral shape: bf16 GEMV 446 us vs tensor cores 455 us at T = 16,
 // 473 vs 457 at T = 20).  The int8 weight-streaming kernel widens each code
 // once per pass and reuses it for every token tile, so it stays ahead of the
-// tensor cores for longer (T = 48: 362 vs 485 us; T = 64: 511 vs 488).
+// tensor cores for longer (T = 48: 364 vs 487 us).  At T = 64 it is ahead
+// only while no expert needs a second pass (456 vs 492 us; with one expert of
+// 25 tokens 509 vs 495), which skewed routing makes common, while the tensor
+// cores read each weight once for any count: the crossover stays at 12.
 constexpr int kTcMinMeanTokens = 4;
 constexpr int kTcMinMeanTokensI8 = 12;
 
