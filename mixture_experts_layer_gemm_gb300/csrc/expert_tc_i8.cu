@@ -21,8 +21,8 @@
 //     buffers of 64 columns);
 //   the MMA thread issues 8 MMAs of K = 16 per stage, A from tensor memory,
 //     B from shared memory, D = 128 lanes x N fp32 columns (two buffers).
-// Tensor memory: D buffers at columns [0, 2N) (N <= 128), A buffers at
-// [256, 384); 512 columns allocated (one CTA per SM).
+// Tensor memory: D buffers at columns [0, 2N) (N <= 192), A buffers at
+// [384, 512); 512 columns allocated (one CTA per SM).
 // Warp roles (448 threads): 0 producer, 1 tensor-memory owner + MMA issuer,
 // 2-5 epilogue, 6-13 converters.  Every wait is bounded; a wait that gives up
 // sets kErrWaitTimeout and the CTA drains and returns.
@@ -43,8 +43,9 @@ constexpr int kA8Bytes = 16384;  // 128 rows x 128 int8
 constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 200 * 1024;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kACol = 256;  // first column of the A buffers
-constexpr int kABufs = 2;        // A buffers of 64 columns at [256, 384)
+constexpr uint32_t kACol = 384;  // first column of the A buffers (after two D buffers of N <= 192)
+constexpr int kABufs = 2;        // A buffers of 64 columns at [384, 512)
+static_assert(kACol + kABufs * 64 <= kTmemCols && 2 * kTcI8MaxN <= kACol, "tensor-memory columns");
 
 enum Phase { kUp = 0, kDown = 1 };
 

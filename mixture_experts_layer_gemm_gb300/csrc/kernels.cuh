@@ -125,7 +125,7 @@ cudaError_t launch_tc2_up(const ExpertArgs &a, bool gated, const CUtensorMap &wm
 
 // The same with int8 weights (K a multiple of 128): codes widened to bf16 in
 // tensor memory, per-row scale in the epilogue; N tokens per tile, 16..128.
-constexpr int kTcI8MaxN = 128;
+constexpr int kTcI8MaxN = 192;
 cudaError_t launch_tc_i8_up(const ExpertArgs &a, bool gated, int splits, int N, const CUtensorMap &xmap,
                             int num_sms, cudaStream_t s);
 cudaError_t launch_tc_i8_down(const ExpertArgs &a, int splits, int N, const CUtensorMap &hmap,

@@ -33,8 +33,8 @@ struct moe_layer {
     void *h = nullptr;
     void *x_perm = nullptr;  // [max_tokens*k x m] bf16: token rows in expert order (tensor-core path)
     // tensor maps over x_perm and h for token tiles N = 16, 32, 64, 128, 256
-    bool tmap_ok[5] = {};
-    CUtensorMap tmap_x[5], tmap_h[5];
+    bool tmap_ok[6] = {};
+    CUtensorMap tmap_x[6], tmap_h[6];  // token-row maps, boxes of 16, 32, 64, 128, 256, 192 rows
     bool tmap_w_ok = false;  // the resident weights as 128-byte rows (CTA-pair kernels)
     CUtensorMap tmap_w;
     float *ypart = nullptr;

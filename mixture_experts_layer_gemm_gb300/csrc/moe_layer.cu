@@ -619,9 +619,18 @@ static int tc_tile_n(int mean_q) {
     return 256;
 }
 
+// Token-row maps (x_perm and h) whose boxes are N rows: one pair per width.
 static moe_status_t tc_maps(moe_layer_t *L, int N, const CUtensorMap **xm, const CUtensorMap **hm) {
-    int idx = 0;
-    while ((16 << idx) < N) ++idx;
+    int idx;
+    switch (N) {
+    case 16: idx = 0; break;
+    case 32: idx = 1; break;
+    case 64: idx = 2; break;
+    case 128: idx = 3; break;
+    case 256: idx = 4; break;
+    case 192: idx = 5; break;  // int8 tensor-core tiles
+    default: return fail(MOE_ERR_INTERNAL, "no token-row map of width %d", N);
+    }
     if (!L->tmap_ok[idx]) {
         const size_t rows = static_cast<size_t>(L->cfg.max_tokens) * L->cfg.k;
         moe_status_t st = make_row_map(&L->tmap_x[idx], L->x_perm, L->cfg.m, rows, N);
