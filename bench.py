@@ -36,16 +36,19 @@ METRIC = "MoE-layer tokens/s; HBM GB/s (decode) & tensor TFLOPS (batch) vs GB300
 
 def parse():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=600)
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--weights", default="bf16", choices=["bf16", "i8"])
-    ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="GPUs (one process each under torchrun; each runs the whole step)")
+    ap.add_argument("--steps", type=int, default=600, help="timed steps")
+    ap.add_argument("--warmup", type=int, default=10, help="untimed warm-up steps (at least 3)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"],
+                    help="ours: the CUDA library; reference: the fp64 oracle on the host cores")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "i8"],
+                    help="expert weight type (i8: per-channel symmetric int8)")
+    ap.add_argument("--seed", type=int, default=0, help="seed of the synthetic weights and tokens")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle's timed sample")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--tokens", default="1,4,16,64",
-                    help="decode batches per step (profiling runs use one)")
+                    help="batch sizes of one step, comma-separated (each runs route + forward)")
     ap.add_argument("--copies", type=int, default=2, help="weight copies that alternate")
     ap.add_argument("--pair-tiles", type=int, default=1, choices=[0, 1],
                     help="up-projection 256-token tiles on CTA pairs (1, default) or one CTA each (0)")
