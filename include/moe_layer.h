@@ -213,6 +213,42 @@ typedef enum {
 } moe_option_t;
 moe_status_t moe_layer_set_option(moe_layer_t *layer, moe_option_t opt, int value);
 
+/* Launch plan of moe_forward for T tokens: which expert-MLP kernels run and
+ * how their work is cut.  It is the same host arithmetic that moe_forward
+ * performs (moe_forward takes its plan from this function), computed here
+ * from the configuration alone, without a layer or a device -- for capacity
+ * planning, and so that the choice can be checked off the GPU.
+ *   cfg: a layer configuration (checked as moe_layer_create checks it).
+ *   T: 0 <= T <= cfg->max_tokens.  num_sms: SMs of the device, >= 1 (152 on
+ *   a GB300; moe_layer_info reports a layer's).  regime and pair_tiles: the
+ *   values of MOE_OPT_REGIME (0, 1, 2) and MOE_OPT_PAIR_TILES (0, 1) the
+ *   layer would have.
+ * The decode regime runs the weight-streaming GEMV: token passes of 8, 16,
+ * 24 or 32 tokens (the smallest that covers the mean count per expert plus
+ * 1.5 standard deviations under uniform routing); the batch regime runs the
+ * tcgen05 grouped GEMM with token tiles of N = 16 .. 256 (int8: <= 192).
+ * Automatic choice: the GEMV while ceil(T*k/E) <= 4 (bf16 weights) or <= 12
+ * (int8 weights) and T*k <= 512, the tensor cores beyond, where the shapes
+ * allow (2p or p, m and for int8 p multiples of 128).
+ * Returns MOE_ERR_INVALID_ARG for a bad cfg, T, num_sms, regime or
+ * pair_tiles; MOE_ERR_UNSUPPORTED where moe_forward would refuse the request
+ * (a forced regime the shapes or T do not allow).  Pure host arithmetic. */
+typedef enum {
+    MOE_PATH_NONE = 0,   /* T = 0: no expert kernel runs                      */
+    MOE_PATH_SIMT = 1,   /* fp32 layers: CUDA-core expert kernels             */
+    MOE_PATH_GEMV = 2,   /* decode regime: weight-streaming GEMV              */
+    MOE_PATH_TENSOR = 3  /* batch regime: tcgen05 grouped GEMM                */
+} moe_path_t;
+typedef struct {
+    int path;                    /* a moe_path_t                                   */
+    int mean_tokens;             /* ceil(T*k / E), the count the regime follows    */
+    int tile_up, tile_down;      /* tokens per GEMV pass or per tensor-core tile   */
+    int splits_up, splits_down;  /* reduction splits of each projection (1: none)  */
+    int pair_up;                 /* 1: up-projection tiles on CTA pairs            */
+} moe_plan_t;
+moe_status_t moe_plan_forward(const moe_config_t *cfg, int T, int num_sms, int regime,
+                              int pair_tiles, moe_plan_t *out);
+
 /* Per-phase device time of the layer's kernels, from the events that
  * MOE_OPT_TIMING records.  Waits for the recorded events, sums the elapsed
  * time of every launch per phase, and (reset != 0) forgets them. */

@@ -71,6 +71,16 @@ class moe_stats_t(ctypes.Structure):
                 ("gemv_runs", ctypes.c_uint64), ("tc_runs", ctypes.c_uint64)]
 
 
+MOE_PATH_NONE, MOE_PATH_SIMT, MOE_PATH_GEMV, MOE_PATH_TENSOR = 0, 1, 2, 3
+PATHS = {MOE_PATH_NONE: "none", MOE_PATH_SIMT: "simt", MOE_PATH_GEMV: "gemv", MOE_PATH_TENSOR: "tensor-core"}
+
+
+class moe_plan_t(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("mean_tokens", ctypes.c_int), ("tile_up", ctypes.c_int),
+                ("tile_down", ctypes.c_int), ("splits_up", ctypes.c_int), ("splits_down", ctypes.c_int),
+                ("pair_up", ctypes.c_int)]
+
+
 class MoeError(RuntimeError):
     def __init__(self, status, msg):
         super().__init__(f"{_STATUS_NAMES.get(status, status)}: {msg}")
@@ -91,6 +101,7 @@ _SIGNATURES = {
     "moe_forward": [_vp, _vp, ctypes.POINTER(moe_routing_t), _vp, _vp],
     "moe_forward_static_scratch": [_vp, _vp, ctypes.POINTER(moe_routing_t), _vp, _vp],
     "moe_layer_set_option": [_vp, _i, _i],
+    "moe_plan_forward": [ctypes.POINTER(moe_config_t), _i, _i, _i, _i, ctypes.POINTER(moe_plan_t)],
     "moe_layer_info": [_vp, ctypes.POINTER(moe_layer_info_t)],
     "moe_layer_stats": [_vp, ctypes.POINTER(moe_stats_t)],
     "moe_layer_timings": [_vp, ctypes.POINTER(moe_timings_t), _i],
@@ -209,6 +220,13 @@ def moe_forward_static_scratch(handle, x, routing: moe_routing_t, y, stream=None
 
 def moe_layer_set_option(handle, opt, value):
     _check(lib().moe_layer_set_option(handle, opt, value))
+
+
+def moe_plan_forward(cfg: moe_config_t, T, num_sms=152, regime=REGIME_AUTO, pair_tiles=1) -> moe_plan_t:
+    """The launch plan moe_forward follows for T tokens (host arithmetic only)."""
+    out = moe_plan_t()
+    _check(lib().moe_plan_forward(ctypes.byref(cfg), T, num_sms, regime, pair_tiles, ctypes.byref(out)))
+    return out
 
 
 def moe_layer_info(handle) -> moe_layer_info_t:
@@ -359,12 +377,19 @@ class MoELayer:
 
     def set_regime(self, regime: int):
         moe_layer_set_option(self.handle, MOE_OPT_REGIME, regime)
+        self._regime = regime
+
+    def plan(self, T: int) -> moe_plan_t:
+        """The launch plan this layer's forward takes for T tokens."""
+        return moe_plan_forward(self.cfg, T, moe_layer_info(self.handle).num_sms,
+                                getattr(self, "_regime", REGIME_AUTO), getattr(self, "_pair_tiles", 1))
 
     def set_timing(self, on: bool):
         moe_layer_set_option(self.handle, MOE_OPT_TIMING, int(on))
 
     def set_pair_tiles(self, on: bool):
         moe_layer_set_option(self.handle, MOE_OPT_PAIR_TILES, int(on))
+        self._pair_tiles = int(on)
 
     def set_host_timeout_ms(self, ms: int):
         """Longest host wait of this layer's calls (-1: no limit)."""

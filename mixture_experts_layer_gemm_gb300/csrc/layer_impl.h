@@ -95,6 +95,19 @@ moe_status_t run_combine(moe_layer *L, const moe_routing_t *r, int splits, int n
                          cudaStream_t s);
 void decode_plan(const moe_layer *L, int T, int *nt, int *s_up, int *s_down);
 
+// Workspace a layer of configuration c allocates at create time, and to which
+// its launch plans are cut.
+struct WorkspaceGeom {
+    int split_up_max = 1, split_down_max = 1;  // reduction splits the partial-sum buffers hold
+    size_t decode_rows_cap = 0;                // largest T*k of the split (decode-sized) forms
+    size_t ypart_rows = 0;                     // fp32 rows of the down projection's output
+};
+WorkspaceGeom workspace_geom(const moe_config_t &c);
+// The launch plan of the expert MLPs for T tokens (the rules moe_plan_forward
+// states); MOE_ERR_UNSUPPORTED where a forced regime cannot run.
+moe_status_t plan_forward(const moe_config_t &c, const WorkspaceGeom &w, int num_sms, int T, int regime,
+                          bool pair_tiles, moe_plan_t *out);
+
 // Launch one kernel (f returns its cudaError_t) as phase `phase`: counts the
 // launch and, with timing on, brackets it with events on stream s.
 // A named range on the host timeline of profilers (NVTX; no cost without one).

@@ -350,6 +350,26 @@ static moe_status_t ingest_weights(moe_layer_t *L, const void *w_router, const f
     return MOE_OK;
 }
 
+namespace moe {
+
+WorkspaceGeom workspace_geom(const moe_config_t &c) {
+    WorkspaceGeom g;
+    const size_t rows = static_cast<size_t>(c.max_tokens) * c.k;
+    g.ypart_rows = rows;
+    if (c.act_dtype == MOE_BF16) {
+        g.split_up_max = kSplitUpMax;
+        g.split_down_max = kSplitDownMax;
+        g.decode_rows_cap = rows < static_cast<size_t>(kDecodeMaxRows) ? rows : kDecodeMaxRows;
+        // decode: split_down_max partial rows per permuted row (T*k <= the cap);
+        // batch: one fp32 row per permuted row
+        const size_t need = static_cast<size_t>(g.split_down_max) * g.decode_rows_cap;
+        g.ypart_rows = rows > need ? rows : need;
+    }
+    return g;
+}
+
+}  // namespace moe
+
 static moe_status_t alloc_workspace(moe_layer_t *L) {
     const moe_config_t &c = L->cfg;
     cudaError_t err;
@@ -357,21 +377,14 @@ static moe_status_t alloc_workspace(moe_layer_t *L) {
     const size_t ab = act_bytes(c.act_dtype);
     L->h = L->dalloc(rows * c.p * ab, &err);
     if (err) return cuda_fail(err, "cudaMalloc(h)");
-    size_t ypart_rows = rows;
-    L->split_up_max = 1;
-    L->split_down_max = 1;
+    const WorkspaceGeom g = workspace_geom(c);
+    const size_t ypart_rows = g.ypart_rows;
+    L->split_up_max = g.split_up_max;
+    L->split_down_max = g.split_down_max;
+    L->decode_rows_cap = g.decode_rows_cap;
     if (c.act_dtype == MOE_BF16) {
-        L->split_up_max = kSplitUpMax;
-        L->split_down_max = kSplitDownMax;
-        const size_t drows = rows < kDecodeMaxRows ? rows : kDecodeMaxRows;
-        L->decode_rows_cap = drows;
-        // decode: split_down_max partial rows per permuted row (T*k <= the cap);
-        // batch: one fp32 row per permuted row
-        size_t need = static_cast<size_t>(L->split_down_max) * drows;
-        if (rows > need) need = rows;
-        ypart_rows = need;
         if (L->split_up_max > 1) {
-            const size_t n = static_cast<size_t>(L->split_up_max) * drows * c.p;
+            const size_t n = static_cast<size_t>(L->split_up_max) * g.decode_rows_cap * c.p;
             L->gate_part = static_cast<float *>(L->dalloc(n * 4, &err));
             if (err) return cuda_fail(err, "cudaMalloc(gate partials)");
             L->up_part = static_cast<float *>(L->dalloc(n * 4, &err));
@@ -662,40 +675,102 @@ static int tc_splits(int nkb, int rows, int N, int mean_q, int n_active, int num
     return best;
 }
 
+// The launch plan of the expert MLPs for T tokens (moe_plan_forward states the
+// rules): regime, token tiles or passes, reduction splits, CTA pairs.
+moe_status_t plan_forward(const moe_config_t &c, const WorkspaceGeom &w, int num_sms, int T, int regime,
+                          bool pair_tiles, moe_plan_t *out) {
+    moe_plan_t p{};
+    p.splits_up = p.splits_down = 1;
+    const int rows = T * c.k;
+    p.mean_tokens = (rows + c.E - 1) / c.E;
+    if (T == 0) {
+        p.path = MOE_PATH_NONE;
+    } else if (c.act_dtype == MOE_F32) {
+        p.path = MOE_PATH_SIMT;
+    } else {
+        // regime: the weight-streaming GEMV while experts see few tokens, the
+        // tensor-core grouped GEMM beyond (rows in 128-row blocks; int8 weights
+        // also need K in 128-element blocks, which int8 layers have)
+        const bool gated = c.expert == MOE_EXPERT_SWIGLU;
+        const bool i8 = c.weight_dtype == MOE_I8;
+        const int mean_q = p.mean_tokens;
+        const int rows_up = gated ? 2 * c.p : c.p;
+        const int bk = i8 ? 128 : 64;  // reduction elements per pipeline stage
+        const bool tc_shape = rows_up % 128 == 0 && c.m % 128 == 0 && (!i8 || c.p % 128 == 0);
+        const bool fits_decode = static_cast<size_t>(rows) <= w.decode_rows_cap;
+        bool use_tc = false;
+        if (regime == 2) {
+            if (!tc_shape) return fail(MOE_ERR_UNSUPPORTED, "batch kernels need 128-row blocks");
+            use_tc = true;
+        } else if (regime == 0) {
+            const int min_q = i8 ? kTcMinMeanTokensI8 : kTcMinMeanTokens;
+            use_tc = tc_shape && (mean_q > min_q || !fits_decode);
+        }
+        if (use_tc) {
+            int N = tc_tile_n(mean_q);
+            if (i8 && N > kTcI8MaxN) N = kTcI8MaxN;
+            if (fits_decode) {
+                const int n_act = expected_active(T, c.k, c.E);
+                p.splits_up = tc_splits(c.m / bk, rows_up, N, mean_q, n_act, num_sms, w.split_up_max);
+                p.splits_down = tc_splits(c.p / bk, c.m, N, mean_q, n_act, num_sms, w.split_down_max);
+            } else if (w.ypart_rows >= 2 * static_cast<size_t>(rows)) {
+                // batch: the down projection's tiles (128 output rows x a token
+                // tile, the whole reduction of p) can be too few to fill the SMs
+                // evenly; it splits the reduction in two where that evens out the
+                // waves and the partial-sum workspace has room (measured, Mixtral
+                // shape T = 2048: 418 -> 393 us; four splits at T = 512 measured
+                // slower than none)
+                p.splits_down = tc_splits(c.p / bk, c.m, N, mean_q, c.E, num_sms, 2);
+            }
+            // The up projection's 256-token tiles run on CTA pairs (less
+            // shared-memory traffic per SM; measured faster) for resident
+            // weights in 256-row pair blocks with nothing split; the down
+            // projection stays on one CTA per tile, which measured faster for it.
+            p.pair_up = (!i8 && pair_tiles && !c.paged && N == 256 && p.splits_up == 1 && rows_up % 256 == 0);
+            // The down projection streams its weights while experts see a few
+            // hundred tokens (HBM-bound): 128-token tiles halve each stage's
+            // token fill, so more weight stages fit in flight (Mixtral shape,
+            // Zipf 1.2, T = 512: down 256.5 -> 244.5 us).
+            p.tile_up = N;
+            p.tile_down = (!i8 && N == 256 && mean_q <= 192) ? 128 : N;
+            p.path = MOE_PATH_TENSOR;
+        } else {
+            if (!fits_decode) return fail(MOE_ERR_UNSUPPORTED, "decode kernels take T*k <= %d", kDecodeMaxRows);
+            const int nt = decode_token_tiles(T, c.k, c.E);
+            const int n_act = expected_active(T, c.k, c.E);
+            p.splits_up = choose_splits(c.m, bk, rows_up, nt, n_act, num_sms, w.split_up_max);
+            p.splits_down = choose_splits(c.p, bk, c.m, nt, n_act, num_sms, w.split_down_max);
+            if (p.splits_up > w.split_up_max || p.splits_down > w.split_down_max)
+                return fail(MOE_ERR_INTERNAL, "split count exceeds workspace");
+            p.tile_up = p.tile_down = 8 * nt;
+            p.path = MOE_PATH_GEMV;
+        }
+    }
+    *out = p;
+    return MOE_OK;
+}
+
+static WorkspaceGeom layer_geom(const moe_layer_t *L) {
+    WorkspaceGeom w;
+    w.split_up_max = L->split_up_max;
+    w.split_down_max = L->split_down_max;
+    w.decode_rows_cap = L->decode_rows_cap;
+    w.ypart_rows = L->ypart_rows;
+    return w;
+}
+
 // Tensor-core path: gather the token rows into expert order, then the grouped
 // GEMMs (up with the activation fused, down with the routing weight fused).
-static moe_status_t run_experts_tc(moe_layer_t *L, ExpertArgs &a, int *splits_out, cudaStream_t s) {
+static moe_status_t run_experts_tc(moe_layer_t *L, ExpertArgs &a, const moe_plan_t &plan, int *splits_out,
+                                   cudaStream_t s) {
     const moe_config_t &c = L->cfg;
     const bool gated = c.expert == MOE_EXPERT_SWIGLU;
     const int rows = a.T * a.k;
     const bool i8 = c.weight_dtype == MOE_I8;
-    const int mean_q = (rows + c.E - 1) / c.E;
-    int N = tc_tile_n(mean_q);
-    if (i8 && N > kTcI8MaxN) N = kTcI8MaxN;
-    const int bk = i8 ? 128 : 64;  // reduction elements per pipeline stage
-    const int rows_up = gated ? 2 * c.p : c.p;
-    int s_up = 1, s_down = 1;
-    if (rows <= static_cast<int>(L->decode_rows_cap)) {
-        const int n_act = expected_active(a.T, a.k, a.E);
-        s_up = tc_splits(c.m / bk, rows_up, N, mean_q, n_act, L->num_sms, L->split_up_max);
-        s_down = tc_splits(c.p / bk, c.m, N, mean_q, n_act, L->num_sms, L->split_down_max);
-        a.n_rows_cap = static_cast<int>(L->decode_rows_cap);
-    } else {
-        // batch: the down projection's tiles (128 output rows x a token tile,
-        // the whole reduction of p) can be too few to fill the SMs evenly; it
-        // splits the reduction in two where that evens out the waves and the
-        // partial-sum workspace has room (measured, Mixtral shape T = 2048:
-        // 418 -> 393 us; four splits at T = 512 measured slower than none)
-        a.n_rows_cap = rows;
-        if (L->ypart_rows >= 2 * static_cast<size_t>(rows))
-            s_down = tc_splits(c.p / bk, c.m, N, mean_q, c.E, L->num_sms, 2);
-    }
-    // The up projection's 256-token tiles run on CTA pairs (less shared-memory
-    // traffic per SM; measured faster) when its matrix comes in 256-row pair
-    // blocks and nothing is split; the down projection stays on one CTA per
-    // tile, which measured faster for it.
-    const bool pair_up = !i8 && L->pair_tiles && !L->pool && L->weights && N == 256 && s_up == 1 &&
-                         rows_up % 256 == 0;
+    const int N = plan.tile_up, N_down = plan.tile_down;
+    const int s_up = plan.splits_up, s_down = plan.splits_down;
+    const bool pair_up = plan.pair_up != 0;
+    a.n_rows_cap = static_cast<size_t>(rows) <= L->decode_rows_cap ? static_cast<int>(L->decode_rows_cap) : rows;
     const CUtensorMap *xm = nullptr, *hm = nullptr, *xm_half = nullptr, *hm_half = nullptr;
     moe_status_t st = tc_maps(L, N, &xm, &hm);
     if (st == MOE_OK && pair_up) st = tc_maps(L, N / 2, &xm_half, &hm_half);
@@ -719,11 +794,6 @@ static moe_status_t run_experts_tc(moe_layer_t *L, ExpertArgs &a, int *splits_ou
     if (st == MOE_OK && s_up > 1)
         st = launch_phase(L, MOE_PHASE_UP_FINISH, s, "up_finish",
                           [&] { return launch_decode_up_finish(a, gated, s_up, s); });
-    // The down projection streams its weights while experts see a few hundred
-    // tokens (HBM-bound): 128-token tiles halve each stage's token fill, so
-    // more weight stages fit in flight (Mixtral shape, Zipf 1.2, T = 512:
-    // down 256.5 -> 244.5 us).
-    const int N_down = (!i8 && N == 256 && mean_q <= 192) ? 128 : N;
     const CUtensorMap *hm_down = hm;
     if (st == MOE_OK && N_down != N) {
         const CUtensorMap *unused = nullptr;
@@ -731,7 +801,7 @@ static moe_status_t run_experts_tc(moe_layer_t *L, ExpertArgs &a, int *splits_ou
     }
     if (st == MOE_OK)
         st = launch_phase(L, MOE_PHASE_DOWN, s, "tc_down", [&] {
-            return i8 ? launch_tc_i8_down(a, s_down, N, *hm, L->num_sms, s)
+            return i8 ? launch_tc_i8_down(a, s_down, N_down, *hm_down, L->num_sms, s)
                       : launch_tc_down(a, s_down, N_down, *hm_down, L->num_sms, s);
         });
     *splits_out = s_down;
@@ -744,50 +814,26 @@ moe_status_t run_experts(moe_layer_t *L, ExpertArgs &a, int regime, int *splits_
                          cudaStream_t s) {
     const moe_config_t &c = L->cfg;
     const bool gated = c.expert == MOE_EXPERT_SWIGLU;
-    const int rows = a.T * a.k;
-    if (c.act_dtype == MOE_F32) {
-        a.n_rows_cap = rows;
+    moe_plan_t plan;
+    moe_status_t plan_st = plan_forward(c, layer_geom(L), L->num_sms, a.T, regime, L->pair_tiles, &plan);
+    if (plan_st != MOE_OK) return plan_st;
+    *splits_out = 1;
+    if (plan.path == MOE_PATH_NONE) return MOE_OK;
+    if (plan.path == MOE_PATH_SIMT) {
+        a.n_rows_cap = a.T * a.k;
         moe_status_t st = launch_phase(L, MOE_PHASE_UP, s, "simt_up", [&] { return launch_simt_up(a, gated, s); });
         if (st == MOE_OK)
             st = launch_phase(L, MOE_PHASE_DOWN, s, "simt_down", [&] { return launch_simt_down(a, s); });
-        *splits_out = 1;
         return st;
     }
-    // regime: the weight-streaming GEMV while experts see few tokens, the
-    // tensor-core grouped GEMM beyond (rows in 128-row blocks; int8 weights
-    // also need K in 128-element blocks, which int8 layers have)
-    const int mean_q = (rows + c.E - 1) / c.E;
-    const bool tc_shape = L->x_perm && (gated ? (2 * c.p) % 128 : c.p % 128) == 0 &&
-                          c.m % 128 == 0 && (c.weight_dtype != MOE_I8 || c.p % 128 == 0);
-    const bool fits_decode = rows <= static_cast<int>(L->decode_rows_cap);
-    bool use_tc = false;
-    if (regime == 2) {
-        if (!tc_shape) return fail(MOE_ERR_UNSUPPORTED, "batch kernels need 128-row blocks");
-        use_tc = true;
-    } else if (regime == 0) {
-        const int min_q = c.weight_dtype == MOE_I8 ? kTcMinMeanTokensI8 : kTcMinMeanTokens;
-        use_tc = tc_shape && (mean_q > min_q || !fits_decode);
-    }
-    if (use_tc) {
+    if (plan.path == MOE_PATH_TENSOR) {
         L->stats.tc_runs += 1;
-        return run_experts_tc(L, a, splits_out, s);
+        return run_experts_tc(L, a, plan, splits_out, s);
     }
     L->stats.gemv_runs += 1;
     const WeightType wt = (c.weight_dtype == MOE_I8) ? WeightType::kI8 : WeightType::kBF16;
-    int nt = decode_token_tiles(a.T, a.k, a.E);
-    int s_up, s_down;
-    if (rows <= static_cast<int>(L->decode_rows_cap)) {
-        const int bk = (c.weight_dtype == MOE_I8) ? 128 : 64;
-        const int n_act = expected_active(a.T, a.k, a.E);
-        const int rows_up = gated ? 2 * c.p : c.p;
-        s_up = choose_splits(c.m, bk, rows_up, nt, n_act, L->num_sms, L->split_up_max);
-        s_down = choose_splits(c.p, bk, c.m, nt, n_act, L->num_sms, L->split_down_max);
-        a.n_rows_cap = static_cast<int>(L->decode_rows_cap);
-    } else {
-        return fail(MOE_ERR_UNSUPPORTED, "decode kernels take T*k <= %d", kDecodeMaxRows);
-    }
-    if (s_up > L->split_up_max || s_down > L->split_down_max)
-        return fail(MOE_ERR_INTERNAL, "split count exceeds workspace");
+    const int s_up = plan.splits_up, s_down = plan.splits_down;
+    a.n_rows_cap = static_cast<int>(L->decode_rows_cap);
     moe_status_t st = launch_phase(L, MOE_PHASE_UP, s, "decode_up",
                                    [&] { return launch_decode_up(a, wt, gated, s_up, L->num_sms, s); });
     if (st == MOE_OK && s_up > 1)
@@ -844,6 +890,19 @@ extern "C" moe_status_t moe_forward(moe_layer_t *L, const void *x, const moe_rou
     L->last_stream = s;
     L->launched = true;
     return MOE_OK;
+}
+
+extern "C" moe_status_t moe_plan_forward(const moe_config_t *cfg, int T, int num_sms, int regime,
+                                         int pair_tiles, moe_plan_t *out) {
+    if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+    moe_status_t st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    if (T < 0 || T > cfg->max_tokens)
+        return fail(MOE_ERR_INVALID_ARG, "T = %d outside [0, max_tokens = %d]", T, cfg->max_tokens);
+    if (num_sms < 1) return fail(MOE_ERR_INVALID_ARG, "num_sms must be >= 1");
+    if (regime < 0 || regime > 2) return fail(MOE_ERR_INVALID_ARG, "regime must be 0, 1 or 2");
+    if (pair_tiles != 0 && pair_tiles != 1) return fail(MOE_ERR_INVALID_ARG, "pair_tiles must be 0 or 1");
+    return plan_forward(*cfg, workspace_geom(*cfg), num_sms, T, regime, pair_tiles != 0, out);
 }
 
 // ---- options, info, stats, checks ----------------------------------------------------

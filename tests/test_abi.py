@@ -182,7 +182,8 @@ def test_binding_structs_mirror_the_header():
     """Every struct the binding passes through the C ABI has the header's
     members, in order, with the same element sizes."""
     structs = _header_structs(_header_text())
-    for name in ("moe_config_t", "moe_routing_t", "moe_layer_info_t", "moe_timings_t", "moe_stats_t"):
+    for name in ("moe_config_t", "moe_routing_t", "moe_layer_info_t", "moe_timings_t", "moe_stats_t",
+                 "moe_plan_t"):
         py = getattr(moe, name)
         got = []
         for fname, ftype in py._fields_:

@@ -464,6 +464,31 @@ def test_regime_counters_follow_the_choice():
     ml.close()
 
 
+@pytest.mark.parametrize("shape", [SWIGLU_BF16, I8], ids=["bf16", "i8"])
+def test_forward_follows_its_plan(shape):
+    """moe_plan_forward is the plan a forward call takes: over batch sizes and
+    forced regimes, the path counters and the kernels launched (router, token
+    gather on the tensor-core path, up projection, its split finish, down
+    projection, combine) are the ones the plan names."""
+    layer = get_layer(shape, seed=66)
+    ml = moe.MoELayer(layer, 256)
+    for regime in (moe.REGIME_AUTO, moe.REGIME_DECODE, moe.REGIME_BATCH):
+        ml.set_regime(regime)
+        for T in (1, 4, 16, 20, 48, 64, 200, 256):
+            plan = ml.plan(T)
+            s0 = ml.stats()
+            Run(ml, wl.make_tokens(shape, T, seed=T))
+            s1 = ml.stats()
+            tc = plan.path == moe.MOE_PATH_TENSOR
+            assert plan.path in (moe.MOE_PATH_GEMV, moe.MOE_PATH_TENSOR)
+            ran = (int(s1.gemv_runs - s0.gemv_runs), int(s1.tc_runs - s0.tc_runs))
+            assert ran == ((0, 1) if tc else (1, 0)), (T, regime)
+            launched = int(s1.kernel_launches - s0.kernel_launches)
+            assert launched == 1 + int(tc) + 1 + int(plan.splits_up > 1) + 1 + 1, (T, regime)
+    assert ml.sync_check()[0] == moe.MOE_OK
+    ml.close()
+
+
 @pytest.mark.parametrize("regime", [moe.REGIME_DECODE, moe.REGIME_BATCH])
 def test_int8_activation_range(regime):
     """Token rows spanning 2^-40 .. 2^40 (the int8 GEMV stages each row in
