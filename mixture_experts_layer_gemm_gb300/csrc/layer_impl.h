@@ -93,7 +93,6 @@ ExpertArgs make_expert_args(moe_layer *L, const void *x, const moe_routing_t *r)
 moe_status_t run_experts(moe_layer *L, ExpertArgs &a, int regime, int *splits_out, cudaStream_t s);
 moe_status_t run_combine(moe_layer *L, const moe_routing_t *r, int splits, int n_rows_cap, void *y,
                          cudaStream_t s);
-void decode_plan(const moe_layer *L, int T, int *nt, int *s_up, int *s_down);
 
 // Workspace a layer of configuration c allocates at create time, and to which
 // its launch plans are cut.
@@ -103,6 +102,7 @@ struct WorkspaceGeom {
     size_t ypart_rows = 0;                     // fp32 rows of the down projection's output
 };
 WorkspaceGeom workspace_geom(const moe_config_t &c);
+WorkspaceGeom layer_geom(const moe_layer *L);  // the workspace this layer allocated
 // The launch plan of the expert MLPs for T tokens (the rules moe_plan_forward
 // states); MOE_ERR_UNSUPPORTED where a forced regime cannot run.
 moe_status_t plan_forward(const moe_config_t &c, const WorkspaceGeom &w, int num_sms, int T, int regime,

@@ -750,7 +750,7 @@ moe_status_t plan_forward(const moe_config_t &c, const WorkspaceGeom &w, int num
     return MOE_OK;
 }
 
-static WorkspaceGeom layer_geom(const moe_layer_t *L) {
+WorkspaceGeom layer_geom(const moe_layer_t *L) {
     WorkspaceGeom w;
     w.split_up_max = L->split_up_max;
     w.split_down_max = L->split_down_max;
@@ -844,18 +844,6 @@ moe_status_t run_experts(moe_layer_t *L, ExpertArgs &a, int regime, int *splits_
                           [&] { return launch_decode_down(a, wt, s_down, L->num_sms, s); });
     *splits_out = s_down;
     return st;
-}
-
-// The decode-regime launch plan that run_experts uses for T tokens: token
-// tiles per pass and the reduction splits of the up and down projections.
-void decode_plan(const moe_layer_t *L, int T, int *nt, int *s_up, int *s_down) {
-    const moe_config_t &c = L->cfg;
-    const bool gated = c.expert == MOE_EXPERT_SWIGLU;
-    const int bk = (c.weight_dtype == MOE_I8) ? 128 : 64;
-    const int n_act = expected_active(T, c.k, c.E);
-    *nt = decode_token_tiles(T, c.k, c.E);
-    *s_up = choose_splits(c.m, bk, gated ? 2 * c.p : c.p, *nt, n_act, L->num_sms, L->split_up_max);
-    *s_down = choose_splits(c.p, bk, c.m, *nt, n_act, L->num_sms, L->split_down_max);
 }
 
 moe_status_t run_combine(moe_layer_t *L, const moe_routing_t *r, int splits, int n_rows_cap,

@@ -85,8 +85,11 @@ extern "C" moe_status_t moe_forward_static_scratch(moe_layer_t *L, const void *x
         return fail(MOE_ERR_INVALID_ARG, "T*k = %d exceeds the decode limit %zu", rows,
                     L->decode_rows_cap);
 
-    int nt = 1, s_up = 1, s_down = 1;
-    decode_plan(L, r->T, &nt, &s_up, &s_down);
+    // the decode regime's plan, as moe_forward would take it
+    moe_plan_t plan;
+    moe_status_t st = plan_forward(c, layer_geom(L), L->num_sms, r->T, 1, false, &plan);
+    if (st != MOE_OK) return st;
+    const int s_up = plan.splits_up, s_down = plan.splits_down;
     const size_t h_bytes = round256(static_cast<size_t>(rows) * c.p * 2);
     const size_t y_bytes = round256(static_cast<size_t>(s_down) * rows * c.m * 4);
     const size_t part_bytes = (s_up > 1) ? round256(static_cast<size_t>(s_up) * rows * c.p * 4) : 0;
@@ -97,7 +100,7 @@ extern "C" moe_status_t moe_forward_static_scratch(moe_layer_t *L, const void *x
                     r->T, need, kStaticScratchBytes);
 
     void *base = nullptr;
-    moe_status_t st = scratch_address(&base);
+    st = scratch_address(&base);
     if (st != MOE_OK) return st;
     uint8_t *b = static_cast<uint8_t *>(base);
 
