@@ -424,7 +424,11 @@ def run_ours(args, world, rank, local):
         d_ms = sum(t["down"][0] for t in tt) / 20
         tot = sum(sum(v[0] for v in t.values()) for t in tt) / 20
         w = work[T]
-        per_t[str(T)] = {"path": w["path"], "active_experts": active[T], "layer_us": tot * 1e3,
+        pl = copies[0].plan(T)  # the launch plan the forward took (moe_plan_forward)
+        plan = {f: int(getattr(pl, f)) for f in ("tile_up", "tile_down", "splits_up", "splits_down", "pair_up")}
+        if moe.PATHS[pl.path] != w["path"]:
+            raise RuntimeError(f"T = {T}: plan says {moe.PATHS[pl.path]}, the forward ran {w['path']}")
+        per_t[str(T)] = {"path": w["path"], "plan": plan, "active_experts": active[T], "layer_us": tot * 1e3,
                          "up_us": u_ms * 1e3, "down_us": d_ms * 1e3,
                          "up_gbs": w["up_bytes"] / (u_ms * 1e-3) / 1e9,
                          "down_gbs": w["down_bytes"] / (d_ms * 1e-3) / 1e9,
