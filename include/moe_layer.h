@@ -224,9 +224,10 @@ moe_status_t moe_layer_set_option(moe_layer_t *layer, moe_option_t opt, int valu
  *   values of MOE_OPT_REGIME (0, 1, 2) and MOE_OPT_PAIR_TILES (0, 1) the
  *   layer would have.
  * The decode regime runs the weight-streaming GEMV: token passes of 8, 16,
- * 24 or 32 tokens (the smallest that covers the mean count per expert plus
- * 1.5 standard deviations under uniform routing); the batch regime runs the
- * tcgen05 grouped GEMM with token tiles of N = 16 .. 256 (int8: <= 192).
+ * 24 or 32 tokens, sized to the mean count per expert plus 1.5 standard
+ * deviations under uniform routing (an expert with more tokens takes further
+ * passes); the batch regime runs the tcgen05 grouped GEMM with token tiles of
+ * N = 16 .. 256 (int8: <= 192).
  * Automatic choice: the GEMV while ceil(T*k/E) <= 4 (bf16 weights) or <= 12
  * (int8 weights) and T*k <= 512, the tensor cores beyond, where the shapes
  * allow (2p or p, m and for int8 p multiples of 128).
