@@ -157,14 +157,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
+                    // the stage's two 64-column token halves; a half's K slices are
+                    // 32 bytes apart, +2 in the descriptor's address field (the
+                    // shared-memory addresses stay far below its 256 KB range, so
+                    // the field never carries).  One MMA thread issues every MMA,
+                    // so its loop is kept to an add per MMA.
                     const uint32_t bbase = smem_u32(smem + stage * stage_bytes + kA8Bytes);
+                    const uint64_t bd0 = smem_desc(bbase, 16, 1024, kLayoutSw128);
+                    const uint64_t bd1 = smem_desc(bbase + geo.b_bytes, 16, 1024, kLayoutSw128);
                     const uint32_t acol = tmem_base + kACol + static_cast<uint32_t>(abuf * 64);
+                    tc_mma_tmem_a(d, acol, bd0, idesc, kb > t.kb0 ? 1u : 0u);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t bd = smem_desc(bbase + (kk >> 2) * geo.b_bytes + (kk & 3) * 32, 16,
-                                                      1024, kLayoutSw128);
-                        tc_mma_tmem_a(d, acol + kk * 8, bd, idesc, (kb > t.kb0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 1; kk < 8; ++kk)
+                        tc_mma_tmem_a(d, acol + kk * 8, (kk < 4 ? bd0 : bd1) + 2u * (kk & 3), idesc, 1u);
                     tc_commit(&empty_bar[stage]);   // B slot read
                     tc_commit(&aempty_bar[abuf]);   // A buffer read
                     if (++stage == geo.stages) {
