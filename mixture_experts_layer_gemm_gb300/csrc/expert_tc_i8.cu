@@ -23,8 +23,12 @@
 //     B from shared memory, D = 128 lanes x N fp32 columns (two buffers).
 // Tensor memory: D buffers at columns [0, 2N) (N <= 192), A buffers at
 // [384, 512); 512 columns allocated (one CTA per SM).
-// Warp roles (448 threads): 0 producer, 1 tensor-memory owner + MMA issuer,
-// 2-5 epilogue, 6-13 converters.  Every wait is bounded; a wait that gives up
+// Warp roles (480 threads): 0 producer, 1 tensor-memory owner + MMA issuer,
+// 2-5 epilogue, 6-13 converters, 14 second MMA issuer.  A small-N MMA stream
+// from one thread is paced by that thread's instructions, so where four
+// accumulators fit below the A buffers (N <= 96) the K blocks of a tile
+// alternate between the two issuers, each with its own accumulator, and the
+// epilogue adds the two.  Every wait is bounded; a wait that gives up
 // sets kErrWaitTimeout and the CTA drains and returns.
 #include "common.cuh"
 #include "kernels.cuh"
@@ -36,7 +40,8 @@ namespace moe {
 
 namespace {
 
-constexpr int kThreads = 448;
+constexpr int kThreads = 480;
+constexpr int kMma2Warp = 14;  // second MMA issuer
 constexpr int kEpiWarps = 4;
 constexpr int kCvtWarps = 8;  // two per TMEM lane quarter, one K half each
 constexpr int kA8Bytes = 16384;  // 128 rows x 128 int8
@@ -56,7 +61,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
     __shared__ uint64_t afull_bar[kABufs], aempty_bar[kABufs];
-    __shared__ uint64_t tfull_bar[2], tempty_bar[2], done_bar;
+    __shared__ uint64_t tfull_bar[2], tempty_bar[2], done_bar[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_act[kMaxExperts], s_off[kMaxExperts], s_q[kMaxExperts];
     __shared__ long long s_prefix[kMaxExperts + 1];
@@ -69,6 +74,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int stage_bytes = kA8Bytes + 2 * geo.b_bytes;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // MMA issuers: two where both accumulator buffers of both fit below the A buffers
+    const int nis = (4 * geo.N <= static_cast<int>(kACol)) ? 2 : 1;
     pdl_wait();
     pdl_trigger();
 
@@ -84,10 +91,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&aempty_bar[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&tfull_bar[i], 1);
+            mbar_init(&tfull_bar[i], nis);  // one commit per issuer
             mbar_init(&tempty_bar[i], kEpiWarps);
+            mbar_init(&done_bar[i], 1);
         }
-        mbar_init(&done_bar, 1);
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(&s_tmem, kTmemCols);
@@ -131,9 +138,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp == 1) {
-        // ======================= MMA issuer =====================================
-        if (lane == 0) {
+    } else if (warp == 1 || warp == kMma2Warp) {
+        // ======================= MMA issuers ====================================
+        // issuer `me` takes the K blocks kb0 + me, kb0 + me + nis, ... of every
+        // tile into its own accumulator; both walk every stage and A buffer so
+        // that their ring positions and phases agree
+        const int me = warp == 1 ? 0 : 1;
+        if (lane == 0 && me < nis) {
             int stage = 0, abuf = 0;
             uint32_t phase = 0, aphase = 0;
             int ntile = 0;
@@ -147,10 +158,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = tmem_base + static_cast<uint32_t>(buf * geo.N);
+                const uint32_t d = tmem_base + static_cast<uint32_t>((buf * nis + me) * geo.N);
                 const int n_valid = min(geo.N, (t.q - t.tt * geo.N + 15) / 16 * 16);
                 const uint32_t idesc = idesc_bf16_f32(128, n_valid);
+                uint32_t accum = 0;  // this issuer's first block of the tile starts the sum
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                    if (((kb - t.kb0) & (nis - 1)) != me) {  // the other issuer's block (nis is 1 or 2)
+                        if (++stage == geo.stages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        if (++abuf == kABufs) {
+                            abuf = 0;
+                            aphase ^= 1u;
+                        }
+                        continue;
+                    }
                     if (!mbar_wait(&full_bar[stage], phase) || !mbar_wait(&afull_bar[abuf], aphase)) {
                         flag_error(a.err, kErrWaitTimeout);
                         s_abort = 1;
@@ -166,7 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bd0 = smem_desc(bbase, 16, 1024, kLayoutSw128);
                     const uint64_t bd1 = smem_desc(bbase + geo.b_bytes, 16, 1024, kLayoutSw128);
                     const uint32_t acol = tmem_base + kACol + static_cast<uint32_t>(abuf * 64);
-                    tc_mma_tmem_a(d, acol, bd0, idesc, kb > t.kb0 ? 1u : 0u);
+                    tc_mma_tmem_a(d, acol, bd0, idesc, accum);
+                    accum = 1;
 #pragma unroll
                     for (int kk = 1; kk < 8; ++kk)
                         tc_mma_tmem_a(d, acol + kk * 8, (kk < 4 ? bd0 : bd1) + 2u * (kk & 3), idesc, 1u);
@@ -183,8 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_commit(&tfull_bar[buf]);
             }
-            tc_commit(&done_bar);
-            if (!mbar_wait(&done_bar, 0)) flag_error(a.err, kErrWaitTimeout);
+            tc_commit(&done_bar[me]);
+            if (!mbar_wait(&done_bar[me], 0)) flag_error(a.err, kErrWaitTimeout);
         }
     } else if (warp < 2 + kEpiWarps) {
         // ======================= epilogue =======================================
@@ -217,12 +241,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tok0 = t.tt * geo.N;
             const int n_valid = min(geo.N, (t.q - tok0 + 15) / 16 * 16);
             if (PHASE == kDown) tc_stage_weights(a, t.off, tok0, t.q, n_valid, s_w[lq], lane);
+            // the tile's accumulators: the second issuer's holds a partial sum
+            // when the tile has two or more K blocks (a warp-uniform choice)
+            const uint32_t dcol = (static_cast<uint32_t>(lq * 32) << 16) + static_cast<uint32_t>(buf * nis * geo.N);
+            const bool two = nis == 2 && t.kb1 - t.kb0 >= 2;
             for (int c0 = 0; c0 < n_valid; c0 += 16) {
                 uint32_t v[16];
-                tmem_ld16(tmem_base + (static_cast<uint32_t>(lq * 32) << 16) +
-                              static_cast<uint32_t>(buf * geo.N + c0),
-                          v);
-                tmem_ld_wait();
+                tmem_ld16(tmem_base + dcol + static_cast<uint32_t>(c0), v);
+                if (two) {
+                    uint32_t v1[16];
+                    tmem_ld16(tmem_base + dcol + static_cast<uint32_t>(geo.N + c0), v1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v1[j]));
+                } else {
+                    tmem_ld_wait();
+                }
                 if (PHASE == kUp && GATED) {
                     if (geo.splits == 1) {
                         tc_swiglu_store16(v, scale, r16 < 8, static_cast<__nv_bfloat16 *>(a.h), a.p, f, t.off,
