@@ -19,9 +19,11 @@
 //     and one half of the stage's reduction range) widen 64 codes to 32
 //     bf16x2 words and store them to an A buffer in tensor memory (two
 //     buffers of 64 columns);
-//   the MMA thread issues 8 MMAs of K = 16 per stage, A from tensor memory,
-//     B from shared memory, D = 128 lanes x N fp32 columns (two buffers).
-// Tensor memory: D buffers at columns [0, 2N) (N <= 192), A buffers at
+//   an MMA thread issues 8 MMAs of K = 16 per stage, A from tensor memory,
+//     B from shared memory, D = 128 lanes x N fp32 columns (two buffers, one
+//     accumulator per MMA issuer in each).
+// Tensor memory: D buffers at columns [0, 2N) with one issuer (N <= 192) or
+// [0, 4N) with two (N <= 96; buffer b, issuer i at (2b + i) N), A buffers at
 // [384, 512); 512 columns allocated (one CTA per SM).
 // Warp roles (480 threads): 0 producer, 1 tensor-memory owner + MMA issuer,
 // 2-5 epilogue, 6-13 converters, 14 second MMA issuer.  A small-N MMA stream
