@@ -95,7 +95,9 @@ constexpr int kSplitUpMax = 4, kSplitDownMax = 16;
 // tensor cores for longer (T = 48: 364 vs 487 us).  At T = 64 it is ahead
 // only while no expert needs a second pass (456 vs 492 us; with one expert of
 // 25 tokens 509 vs 495), which skewed routing makes common, while the tensor
-// cores read each weight once for any count: the crossover stays at 12.
+// cores read each weight once for any count: the crossover stays at 12.  With
+// two MMA-issuing warps on small tiles the int8 tensor cores take 371 us at
+// T = 48 and 376 us at T = 64, so 12 is now about where the paths are even.
 constexpr int kTcMinMeanTokens = 4;
 constexpr int kTcMinMeanTokensI8 = 12;
 
