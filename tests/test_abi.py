@@ -92,6 +92,12 @@ def test_pool_geometry_for_the_mixtral_slot_budget():
     assert moe.moe_pool_geometry(16 << 30, expert, 4) == (12, 48)
     with pytest.raises(moe.MoeError):
         moe.moe_pool_geometry(expert * 3, expert, 4)  # not even one set
+    assert moe.moe_pool_geometry(expert * 4, expert, 4) == (1, 4)    # exactly one set
+    assert moe.moe_pool_geometry(expert * 11, expert, 4) == (2, 8)   # 3 slots that fill no set stay unused
+    for expert_b, ways in ((0, 4), (expert, 0)):
+        with pytest.raises(moe.MoeError) as e:
+            moe.moe_pool_geometry(16 << 30, expert_b, ways)
+        assert e.value.status == moe.MOE_ERR_INVALID_ARG
 
 
 def test_selftest_rejects_bad_poll_counts_before_touching_the_device():
