@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0, help="seed of the synthetic weights and tokens")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle's timed sample")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="skip the int8-decode and batch sub-records of the default run")
     ap.add_argument("--tokens", default="1,4,16,64",
                     help="batch sizes of one step, comma-separated (each runs route + forward)")
     ap.add_argument("--copies", type=int, default=2, help="weight copies that alternate")
@@ -198,11 +200,15 @@ def cpu_threads():
         return os.cpu_count() or 1
 
 
-def make_inputs(shape, seed, device):
+def make_tokens_for(shape, tokens, seed, device):
+    import workloads as wl
+    return {T: wl.make_tokens(shape, T, seed=seed + 1, device=device) for T in tokens}
+
+
+def make_inputs(shape, seed, device, tokens):
     import workloads as wl
     layer = wl.make_layer(shape, seed=seed, device=device)
-    xs = {T: wl.make_tokens(shape, T, seed=seed + 1, device=device) for T in TOKENS}
-    return layer, xs
+    return layer, make_tokens_for(shape, tokens, seed, device)
 
 
 def shape_of(args):
@@ -216,22 +222,26 @@ def shape_of(args):
     return base if args.weights == "bf16" else base.with_weight("i8")
 
 
-def workload_config(shape, weights, flush_note):
-    ts = ",".join(str(t) for t in TOKENS)
-    regime = "decode" if max(TOKENS) <= 64 else "batch"
+def workload_config(shape, weights, tokens):
+    """The workload both arms time: layer shape, batches of one step, and how
+    the inputs relate to L2 (identical for the GPU and the CPU arm)."""
+    ts = ",".join(str(t) for t in tokens)
+    regime = "decode" if max(tokens) <= 64 else "batch"
+    b = 1 if weights == "i8" else 2
+    min_gb = shape.k * (3 if shape.has_w3 else 2) * shape.m * shape.p * b / 1e9
     return {"workload": f"{shape.name}-shaped MoE FFN layer, {regime}, T in {{{ts}}}, {weights} weights",
             "m": shape.m, "p": shape.p, "E": shape.E, "k": shape.k, "expert": "swiglu",
-            "tokens_per_step": sum(TOKENS), "parallelism": "replicas", "l2": flush_note}
+            "tokens_per_step": sum(tokens), "parallelism": "replicas",
+            "l2": f"inputs larger than L2: every call streams >= {min_gb:.2f} GB of expert weights"}
 
 
 def run_reference(args, world, rank):
-    import workloads as wl
     if rank != 0:
         return
     shape = shape_of(args)
     import torch
     device = "cuda" if torch.cuda.is_available() else "cpu"
-    layer, xs = make_inputs(shape, args.seed, device)
+    layer, xs = make_inputs(shape, args.seed, device, TOKENS)
     # Every token is routed each step; the expert MLPs run for one token per
     # host thread, taken from the batch that has that many (the oracle runs its
     # tokens in parallel, so a step costs about one token's MLPs).
@@ -251,7 +261,7 @@ def run_reference(args, world, rank):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(shape, args.weights, "n/a (CPU)"),
+            "config": workload_config(shape, args.weights, TOKENS),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(),
                              "kind": "oracle",
                              "sample": f"per step: router + top-k for all {sum(TOKENS)} tokens of the "
@@ -288,42 +298,45 @@ def capture(torch, fn, layers):
     return g, sum(c.stats().kernel_launches for c in layers) - n0
 
 
-def run_ours(args, world, rank, local):
+def measure(args, world, local, shape, layer, tokens, xs_np, steps, warmup, weights,
+            graph=False, e2e=False, traffic=None):
+    """Time `steps` steps, each route + forward for every batch size of
+    `tokens` on its own seeded tokens, over two (--copies) alternating copies
+    of `layer`'s weights.  Returns the measured record: whole-step time (CUDA
+    events on the launch stream, no per-launch events), the dominant kernel's
+    roofline and the per-batch breakdown from an event-timed second pass,
+    sampled clocks, launches, and optionally the end-to-end leg with host
+    buffers."""
     import numpy as np
     import torch
 
     import mixture_experts_layer_gemm_gb300 as moe
-    import workloads as wl
-    from mixture_experts_layer_gemm_gb300 import build as lib_build
 
-    lib_build.build()
-    shape = shape_of(args)
-    layer, xs_np = make_inputs(shape, args.seed + rank, f"cuda:{local}")
-    max_t = max(TOKENS)
+    max_t = max(tokens)
     copies = [moe.MoELayer(layer, max_t) for _ in range(max(args.copies, 1))]
     for c in copies:
         c.set_pair_tiles(bool(args.pair_tiles))
     dev = torch.device("cuda", local)
     xs = {T: torch.from_numpy(xs_np[T].view(np.int16).copy()).view(torch.bfloat16).to(dev)
-          for T in TOKENS}
-    ys = {T: torch.empty((T, shape.m), dtype=torch.bfloat16, device=dev) for T in TOKENS}
+          for T in tokens}
+    ys = {T: torch.empty((T, shape.m), dtype=torch.bfloat16, device=dev) for T in tokens}
     stream = torch.cuda.current_stream()
 
     def step():  # on the current stream (the capture stream while a graph is captured)
-        for i, T in enumerate(TOKENS):
+        for i, T in enumerate(tokens):
             c = copies[i % len(copies)]
             c.route(xs[T])
             c.forward(xs[T], ys[T])
 
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(max(warmup, 3)):
         step()
     torch.cuda.synchronize()
     launches_per_step = None
     run_step = step
-    if args.graph:
-        graph, launches_per_step = capture(torch, step, copies)
-        run_step = graph.replay
-        for _ in range(max(args.warmup, 3)):
+    if graph:
+        g, launches_per_step = capture(torch, step, copies)
+        run_step = g.replay
+        for _ in range(max(warmup, 3)):
             run_step()
         torch.cuda.synchronize()
     for c in copies:
@@ -339,7 +352,7 @@ def run_ours(args, world, rank, local):
     time.sleep(0.3)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         run_step()
     ev1.record(stream)
     torch.cuda.synchronize()
@@ -347,20 +360,20 @@ def run_ours(args, world, rank, local):
     barrier(world)
     ms = ev0.elapsed_time(ev1)
     ms_max = max_over_ranks(world, ms)
-    launches = (launches_per_step * args.steps if args.graph
+    launches = (launches_per_step * steps if graph
                 else sum(c.stats().kernel_launches for c in copies) - launches0)
 
     # Per-launch kernel durations.  Kernels of one call are launched with
     # programmatic dependent launch, so each may start while its predecessor
     # drains; an event recorded between two launches breaks that overlap.  The
-    # headline region above therefore runs without per-launch events, and the
+    # timed region above therefore runs without per-launch events, and the
     # same steps run again here with them, for the roofline and the breakdown.
     for c in copies:
         c.set_timing(True)
         c.timings(reset=True)
     ev2, ev3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev2.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         step()
     ev3.record(stream)
     torch.cuda.synchronize()
@@ -373,10 +386,13 @@ def run_ours(args, world, rank, local):
     # up: active experts' W1 and W3 (+ int8 scales), token rows read, hidden rows written;
     #     flops 2 * (2 m p) per routed (token, slot) for SwiGLU (2 m p for ReLU)
     # down: active experts' W2 (+ scales), hidden rows read; flops 2 m p per (token, slot)
-    wbytes = 1 if args.weights == "i8" else 2
+    # layer (the per-batch roof): active experts' weights plus x in and y out at
+    #     decode; weights plus T k (m + p + m) bf16 activations on the tensor-core
+    #     path (permuted rows, hidden rows, expert outputs)
+    wbytes = 1 if weights == "i8" else 2
     n_up = 2 if shape.has_w3 else 1
     work, active = {}, {}
-    for i, T in enumerate(TOKENS):
+    for i, T in enumerate(tokens):
         c = copies[i % len(copies)]
         c.route(xs[T], stream=stream)
         tc0 = c.stats().tc_runs
@@ -385,30 +401,35 @@ def run_ours(args, world, rank, local):
         path = "tensor-core" if c.stats().tc_runs > tc0 else "gemv"
         n_act = int((c.counts.cpu() > 0).sum())
         active[T] = n_act
-        scale_up = n_up * shape.p * 4 if args.weights == "i8" else 0
-        scale_dn = shape.m * 4 if args.weights == "i8" else 0
+        scale_up = n_up * shape.p * 4 if weights == "i8" else 0
+        scale_dn = shape.m * 4 if weights == "i8" else 0
         rows = T * shape.k
+        w_all = n_act * ((n_up + 1) * shape.m * shape.p * wbytes + scale_up + scale_dn)
         work[T] = {
             "up_bytes": n_act * (n_up * shape.m * shape.p * wbytes + scale_up) + T * shape.m * 2
             + rows * shape.p * 2,
             "down_bytes": n_act * (shape.m * shape.p * wbytes + scale_dn) + rows * shape.p * 2,
             "up_flops": 2.0 * n_up * shape.m * shape.p * rows,
             "down_flops": 2.0 * shape.m * shape.p * rows,
+            "layer_bytes": w_all + (T * shape.m * 2 * 2 if path == "gemv"
+                                    else rows * (2 * shape.m + shape.p) * 2),
             "path": path}
+        work[T]["layer_flops"] = work[T]["up_flops"] + work[T]["down_flops"]
     bytes_up = sum(w["up_bytes"] for w in work.values())
     bytes_down = sum(w["down_bytes"] for w in work.values())
     flops_up = sum(w["up_flops"] for w in work.values())
     up_ms = sum(t["up"][0] for t in tim)
     up_n = sum(t["up"][1] for t in tim)
-    phase_ms = {k: sum(t[k][0] for t in tim) / args.steps for k in tim[0]}
+    phase_ms = {k: sum(t[k][0] for t in tim) / steps for k in tim[0]}
     hbm, tf, tf_sus, src = peaks()
     layer_bytes = bytes_up + bytes_down
-    layer_gbs = layer_bytes * args.steps / (ms * 1e-3) / 1e9
-    layer_tf = (flops_up + sum(w["down_flops"] for w in work.values())) * args.steps / (ms * 1e-3) / 1e12
+    layer_gbs = layer_bytes * steps / (ms * 1e-3) / 1e9
+    layer_flops = flops_up + sum(w["down_flops"] for w in work.values())
+    layer_tf = layer_flops * steps / (ms * 1e-3) / 1e12
 
     # per-T breakdown: each batch alone, event-timed per launch
     per_t = {}
-    for i, T in enumerate(TOKENS):
+    for i, T in enumerate(tokens):
         for c in copies:
             c.timings(reset=True)
             c.set_timing(True)
@@ -428,31 +449,41 @@ def run_ours(args, world, rank, local):
         plan = {f: int(getattr(pl, f)) for f in ("tile_up", "tile_down", "splits_up", "splits_down", "pair_up")}
         if moe.PATHS[pl.path] != w["path"]:
             raise RuntimeError(f"T = {T}: plan says {moe.PATHS[pl.path]}, the forward ran {w['path']}")
+        # the batch's own roof: min(tensor peak, HBM peak x intensity), as a time
+        t_hbm = w["layer_bytes"] / (hbm * 1e9) * 1e6
+        t_tc = w["layer_flops"] / (tf * 1e12) * 1e6
+        roof_us = max(t_hbm, t_tc)
         per_t[str(T)] = {"path": w["path"], "plan": plan, "active_experts": active[T], "layer_us": tot * 1e3,
                          "up_us": u_ms * 1e3, "down_us": d_ms * 1e3,
                          "up_gbs": w["up_bytes"] / (u_ms * 1e-3) / 1e9,
                          "down_gbs": w["down_bytes"] / (d_ms * 1e-3) / 1e9,
                          "up_tflops": w["up_flops"] / (u_ms * 1e-3) / 1e12,
-                         "down_tflops": w["down_flops"] / (d_ms * 1e-3) / 1e12}
+                         "down_tflops": w["down_flops"] / (d_ms * 1e-3) / 1e12,
+                         "layer_gbs": w["layer_bytes"] / (tot * 1e-3) / 1e9,
+                         "layer_tflops": w["layer_flops"] / (tot * 1e-3) / 1e12,
+                         "roof": {"bound": "tensor" if t_tc > t_hbm else "hbm", "us": roof_us,
+                                  "frac": roof_us / (tot * 1e3)}}
 
     # the dominant kernel: the expert up-projection; HBM-bound while the batch is
     # weight-streaming, tensor-bound once most of the work runs on the tensor-core path
     tensor_bound = sum(w["up_flops"] for w in work.values() if w["path"] == "tensor-core") > \
-        0.5 * flops_up and max(TOKENS) >= 256
-    trec = traffic_record() if (args.shape == "mixtral" and args.weights == "bf16"
-                                and TOKENS == (1, 4, 16, 64)) else None
+        0.5 * flops_up and max(tokens) >= 256
     if tensor_bound:
-        achieved = flops_up * args.steps / (up_ms * 1e-3) / 1e12
-        roofline = {"kernel": "tc_up (tcgen05 grouped GEMM, W1 and W3 + SiLU*gate)",
-                    "bound": "tensor", "achieved": achieved, "peak": tf, "unit": "TFLOP/s",
-                    "frac": achieved / tf, "peak_source": f"{src} (bf16_tflops burst)",
-                    "frac_of_sustained": achieved / tf_sus if tf_sus else None,
+        # each up-projection launch runs for milliseconds inside a multi-ms step:
+        # the sustained (power-capped) peak is the denominator, the burst one beside it
+        achieved = flops_up * steps / (up_ms * 1e-3) / 1e12
+        peak = tf_sus or tf
+        roofline = {"kernel": "expert up-projection (W1 and W3 + SiLU*gate), tcgen05 grouped GEMM",
+                    "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak,
+                    "peak_source": f"{src} (bf16_tflops_sustained)" if tf_sus else f"{src} (bf16_tflops)",
+                    "frac_of_burst": achieved / tf, "peak_burst": tf,
                     "algorithmic_flops_per_step": flops_up,
                     "avg_launch_us": up_ms * 1e3 / max(up_n, 1), "traffic": None}
     else:
-        achieved = bytes_up * args.steps / (up_ms * 1e-3) / 1e9
-        gemv_t = [T for T in TOKENS if work[T]["path"] == "gemv"]
-        tc_t = [T for T in TOKENS if work[T]["path"] != "gemv"]
+        achieved = bytes_up * steps / (up_ms * 1e-3) / 1e9
+        gemv_t = [T for T in tokens if work[T]["path"] == "gemv"]
+        tc_t = [T for T in tokens if work[T]["path"] != "gemv"]
         paths = ", ".join(p for p in (f"decode GEMV for T in {gemv_t}" if gemv_t else "",
                                       f"tcgen05 for T in {tc_t}" if tc_t else "") if p)
         roofline = {"kernel": f"expert up-projection (W1 and W3 + SiLU*gate): {paths}",
@@ -460,15 +491,45 @@ def run_ours(args, world, rank, local):
                     "frac": achieved / hbm, "peak_source": f"{src} (hbm_gbs)",
                     "algorithmic_bytes_per_step": bytes_up,
                     "avg_launch_us": up_ms * 1e3 / max(up_n, 1),
-                    "traffic": None if trec is None else trec.get("bytes_per_step")}
+                    "traffic": None if traffic is None else traffic.get("bytes_per_step")}
 
-    # end to end: pinned host buffers, H2D of x and D2H of y inside the timed region
-    xh = {T: xs[T].cpu().pin_memory() for T in TOKENS}
-    yh = {T: torch.empty((T, shape.m), dtype=torch.bfloat16).pin_memory() for T in TOKENS}
-    xd = {T: torch.empty_like(xs[T]) for T in TOKENS}
+    tokens_step = sum(tokens)
+    rec = {"value": job_value(world, tokens_step, steps, ms_max), "unit": "tokens/s",
+           "steps": steps, "warmup": warmup, "ms_per_step": ms_max / steps,
+           "config": workload_config(shape, weights, tokens),
+           "roofline": roofline,
+           "layer_hbm": {"achieved": layer_gbs, "unit": "GB/s", "frac": layer_gbs / hbm,
+                         "algorithmic_bytes_per_step": layer_bytes,
+                         "note": "whole step: expert weights + activations / step time"},
+           "layer_tflops": layer_tf,
+           "phase_ms_per_step": phase_ms,
+           "ms_per_step_with_launch_events": ms_events / steps,
+           "active_experts": active, "per_T": per_t,
+           "gpu_launches": launches, "clocks": clk}
+    if tensor_bound:
+        rec["layer_tensor"] = {"achieved": layer_tf, "unit": "TFLOP/s",
+                               "frac": layer_tf / (tf_sus or tf), "frac_of_burst": layer_tf / tf,
+                               "note": "whole step: all expert flops / step time"}
+
+    if e2e and not args.no_e2e:
+        rec["e2e"] = measure_e2e(args, world, copies, shape, tokens, xs, ys, stream, steps, graph)
+    for c in copies:
+        c.close()
+    return rec
+
+
+def measure_e2e(args, world, copies, shape, tokens, xs, ys, stream, steps, graph):
+    """The same step through the public API with pinned host buffers: every
+    step copies its inputs in and reads its result back inside the timed
+    region, which ends once the last result is on the host."""
+    import torch
+
+    xh = {T: xs[T].cpu().pin_memory() for T in tokens}
+    yh = {T: torch.empty((T, shape.m), dtype=torch.bfloat16).pin_memory() for T in tokens}
+    xd = {T: torch.empty_like(xs[T]) for T in tokens}
 
     def step_e2e():  # one stream: copy in, compute, copy out (the form a graph captures)
-        for i, T in enumerate(TOKENS):
+        for i, T in enumerate(tokens):
             c = copies[i % len(copies)]
             xd[T].copy_(xh[T], non_blocking=True)
             c.route(xd[T])
@@ -482,8 +543,8 @@ def run_ours(args, world, rank, local):
     # inputs in and reads its result back inside the timed region, which ends
     # when the last result is on the host.
     h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
-    xd2 = [{T: torch.empty_like(xs[T]) for T in TOKENS} for _ in range(2)]
-    yd2 = [{T: torch.empty_like(ys[T]) for T in TOKENS} for _ in range(2)]
+    xd2 = [{T: torch.empty_like(xs[T]) for T in tokens} for _ in range(2)]
+    yd2 = [{T: torch.empty_like(ys[T]) for T in tokens} for _ in range(2)]
     ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of buffer b on the device
     ev_done = [torch.cuda.Event() for _ in range(2)]  # compute on buffer b finished
     ev_back = [torch.cuda.Event() for _ in range(2)]  # outputs of buffer b on the host
@@ -494,52 +555,68 @@ def run_ours(args, world, rank, local):
         pipe["it"] += 1
         with torch.cuda.stream(h2d_stream):
             h2d_stream.wait_event(ev_done[b])  # the step two back finished reading buffer b
-            for T in TOKENS:
+            for T in tokens:
                 xd2[b][T].copy_(xh[T], non_blocking=True)
             ev_in[b].record(h2d_stream)
         stream.wait_event(ev_in[b])
         stream.wait_event(ev_back[b])  # buffer b's previous outputs have been read back
-        for i, T in enumerate(TOKENS):
+        for i, T in enumerate(tokens):
             c = copies[i % len(copies)]
             c.route(xd2[b][T])
             c.forward(xd2[b][T], yd2[b][T])
         ev_done[b].record(stream)
         with torch.cuda.stream(d2h_stream):
             d2h_stream.wait_event(ev_done[b])
-            for T in TOKENS:
+            for T in tokens:
                 yh[T].copy_(yd2[b][T], non_blocking=True)
             ev_back[b].record(d2h_stream)
 
     def e2e_drain():  # the timed region closes once the last result is on the host
         stream.wait_event(ev_back[(pipe["it"] - 1) % 2])
 
-    k_e2e = max(args.steps // 2, 1)
-    e2e_ms = None
-    if not args.no_e2e:
-        run_step, drain = step_e2e_pipelined, e2e_drain
-        if args.graph:
-            for _ in range(3):
-                step_e2e()
-            torch.cuda.synchronize()
-            run_step, drain = capture(torch, step_e2e, copies)[0].replay, (lambda: None)
+    k_e2e = max(steps // 2, 1)
+    run_step, drain = step_e2e_pipelined, e2e_drain
+    if graph:
         for _ in range(3):
-            run_step()
-        drain()
+            step_e2e()
         torch.cuda.synchronize()
-        barrier(world)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(k_e2e):
-            run_step()
-        drain()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(world, e0.elapsed_time(e1))
-    io_bytes = sum(T * shape.m * 2 for T in TOKENS)
+        run_step, drain = capture(torch, step_e2e, copies)[0].replay, (lambda: None)
+    for _ in range(3):
+        run_step()
+    drain()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(k_e2e):
+        run_step()
+    drain()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1))
+    io_bytes = sum(T * shape.m * 2 for T in tokens)
+    return {"value": job_value(world, sum(tokens), k_e2e, e2e_ms), "unit": "tokens/s",
+            "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes,
+            "copies": ("on the compute stream, inside the captured step" if graph else
+                       "pinned host buffers, on two side streams overlapped with the "
+                       "neighbouring steps' compute (double-buffered device inputs and outputs)")}
 
-    tokens_step = sum(TOKENS)
-    value = job_value(world, tokens_step, args.steps, ms_max)
-    e2e_value = job_value(world, tokens_step, k_e2e, e2e_ms) if e2e_ms else None
+
+def run_ours(args, world, rank, local):
+    import dataclasses
+
+    import workloads as wl
+    from mixture_experts_layer_gemm_gb300 import build as lib_build
+
+    lib_build.build()
+    shape = shape_of(args)
+    device = f"cuda:{local}"
+    layer, xs_np = make_inputs(shape, args.seed + rank, device, TOKENS)
+    headline_default = (args.shape == "mixtral" and args.weights == "bf16" and args.zipf is None
+                        and TOKENS == wl.DECODE_TOKENS)
+    trec = traffic_record() if headline_default else None
+    rec = measure(args, world, local, shape, layer, TOKENS, xs_np, args.steps, args.warmup,
+                  args.weights, graph=args.graph, e2e=True, traffic=trec)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -558,35 +635,45 @@ def run_ours(args, world, rank, local):
         cpu = {"value": n / dt, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
                "sample": f"{what}, fp64, one pass"}
 
+    # The metric's other halves, measured in the same run on the same layer
+    # weights: the int8 repeat of the decode step, and the batch regime
+    # (T = 512, 2048, 8192 with a Zipf(1.2) router bias), whose expert GEMMs
+    # are tensor-bound.  Each is its own timed region with its own clocks.
+    subs = {}
+    if headline_default and not args.no_sub:
+        lay_i8 = dataclasses.replace(layer, shape=shape.with_weight("i8"))
+        subs["int8_decode"] = measure(args, world, local, lay_i8.shape, lay_i8, TOKENS, xs_np,
+                                      max(args.steps, 200), args.warmup, "i8")
+        zshape = shape.with_zipf(1.2)
+        lay_b = dataclasses.replace(layer, shape=zshape, b_router=wl.zipf_bias(zshape.E, 1.2))
+        bt = wl.BATCH_TOKENS
+        xb = make_tokens_for(zshape, bt, args.seed + rank, device)
+        subs["batch"] = measure(args, world, local, zshape, lay_b, bt, xb, max(args.steps, 40),
+                                args.warmup, "bf16")
+
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+        line = {"metric": METRIC, "value": rec["value"], "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": rec["ms_per_step"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 # MMA input type (fp32 accumulation): int8 weights are widened
                 # exactly to fp16 in the GEMV and to bf16 on the tensor cores
                 "dtype": "bf16" if args.weights == "bf16" else "i8->f16/bf16", "data": "synthetic",
-                "config": dict(workload_config(shape, args.weights,
-                                               "inputs larger than L2: two weight copies alternate"),
-                               launch="one CUDA graph per step, replayed" if args.graph
-                               else "stream launches with programmatic dependent launch"),
-                "roofline": roofline,
-                "layer_hbm": {"achieved": layer_gbs, "unit": "GB/s", "frac": layer_gbs / hbm,
-                              "algorithmic_bytes_per_step": layer_bytes,
-                              "note": "whole step: expert weights + activations / step time"},
-                "layer_tflops": layer_tf,
-                "phase_ms_per_step": phase_ms,
-                "ms_per_step_with_launch_events": ms_events / args.steps,
-                "active_experts": active, "per_T": per_t,
-                "cpu_baseline": cpu,
-                "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
-                        "d2h_bytes_per_step": io_bytes,
-                        "copies": ("on the compute stream, inside the captured step" if args.graph else
-                                   "pinned host buffers, on two side streams overlapped with the "
-                                   "neighbouring steps' compute (double-buffered device inputs and outputs)")},
-                "gpu_launches": launches, "clocks": clk}
+                "config": rec["config"],
+                "timing": {"weight_copies": max(args.copies, 1),
+                           "launch": "one CUDA graph per step, replayed" if args.graph
+                           else "stream launches with programmatic dependent launch"}}
+        for key in ("roofline", "layer_hbm", "layer_tensor", "layer_tflops", "phase_ms_per_step",
+                    "ms_per_step_with_launch_events", "active_experts", "per_T"):
+            if key in rec:
+                line[key] = rec[key]
+        line["cpu_baseline"] = cpu
+        line["e2e"] = rec.get("e2e")
+        line["gpu_launches"] = rec["gpu_launches"]
+        line["clocks"] = rec["clocks"]
+        for name, sub in subs.items():
+            sub["dtype"] = "i8->f16/bf16" if name == "int8_decode" else "bf16"
+            line[name] = sub
         print(json.dumps(line), flush=True)
-    for c in copies:
-        c.close()
 
 
 

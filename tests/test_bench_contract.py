@@ -34,3 +34,20 @@ def test_our_arm_refuses_to_run_without_a_gpu():
     out = _bench("--steps", "1", "--warmup", "0", "--no-cpu-baseline", timeout=600)
     assert out.returncode != 0
     assert not out.stdout.strip().startswith("{")
+
+
+def test_both_arms_describe_the_workload_with_the_same_config():
+    """The reference arm's config is the one our arm prints for the same
+    flags: workload_config depends on the layer shape, weight type and batch
+    sizes alone (timing details live outside config)."""
+    out = _bench("--impl", "reference", "--shape", "small", "--steps", "1", "--warmup", "0")
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as wl
+    import dataclasses
+    shape = dataclasses.replace(wl.MIXTRAL, name="profile-small", p=3584)
+    assert line["config"] == bench.workload_config(shape, "bf16", wl.DECODE_TOKENS)
+    assert set(line["config"]) == {"workload", "m", "p", "E", "k", "expert", "tokens_per_step",
+                                   "parallelism", "l2"}
