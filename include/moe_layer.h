@@ -176,12 +176,19 @@ moe_status_t moe_forward(moe_layer_t *layer, const void *x, const moe_routing_t 
  *   sums) lives in a 16 MiB array compiled into the library, one per device,
  *   held until the process exits.  No cudaMalloc, cudaFree or other
  *   allocating routine is called.
- *   Limits: resident bf16/int8 layers only; T*k at most 512 and the scratch
- *   need (about T*k*(2p + 4*m*splits) bytes) at most 16 MiB -- e.g. T <= 16
- *   for a Mixtral-shaped layer.  Larger requests return MOE_ERR_INVALID_ARG
- *   with both sizes in moe_last_error().
- *   The first call on a device looks up the array's device address with that
- *   device current; make it before any stream capture begins.
+ *   Limits: resident bf16/int8 layers only; T*k at most 512 and a scratch
+ *   need of at most 16 MiB, where, with R = T*k and the decode plan's
+ *   reduction splits S_up and S_down (moe_plan_forward, regime 1), the need is
+ *     r256(2*R*p) + r256(4*S_down*R*m) + (S_up > 1 ? 2*r256(4*S_up*R*p) : 0)
+ *   bytes (r256 rounds up to a multiple of 256; the last term holds the split
+ *   up projection's gate and up partial sums) -- e.g. T <= 16 for a
+ *   Mixtral-shaped layer.  Larger requests return MOE_ERR_INVALID_ARG with
+ *   both sizes in moe_last_error().
+ *   The call must be made with the layer's device current (else
+ *   MOE_ERR_INVALID_ARG).  The first call on a device looks up the array's
+ *   device address with that device current; make it before any stream
+ *   capture begins.  The address is cached for the process: after a device
+ *   reset the library has to be unloaded and loaded again.
  *   Every call on a device uses the same array: calls whose GPU work overlaps
  *   (other streams, other host threads) race on it and must be serialised.
  *   Nothing needs clearing between calls. */

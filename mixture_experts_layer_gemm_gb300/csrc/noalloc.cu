@@ -26,7 +26,10 @@
 //
 // Set-up: the first call on each device looks up the device address of the
 // array (cudaGetSymbolAddress) with that device current; later calls reuse
-// it.  Make that first call before any stream capture begins.
+// it.  Make that first call before any stream capture begins.  A call must be
+// made with the layer's device current (else MOE_ERR_INVALID_ARG).  The
+// cached address belongs to the device's primary context: after a context
+// reset (cudaDeviceReset) the library must be unloaded and loaded again.
 #include <mutex>
 
 #include "../../include/moe_layer.h"
@@ -48,11 +51,17 @@ void *g_scratch_addr[kMaxDevices] = {};
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
-// Device address of the scratch array on the current device (set-up once).
-moe_status_t scratch_address(void **out) {
+// Device address of the scratch array on the layer's device (set-up once per
+// device).  The symbol lookup answers for the current device, so a call made
+// with another device current is refused rather than handed an address of the
+// wrong GPU's copy.
+moe_status_t scratch_address(int layer_device, void **out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != layer_device)
+        return fail(MOE_ERR_INVALID_ARG, "current device %d is not the layer's device %d", dev,
+                    layer_device);
     if (dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_UNSUPPORTED, "device index %d", dev);
     std::lock_guard<std::mutex> lock(g_scratch_mu);
     if (!g_scratch_addr[dev]) {
@@ -100,7 +109,7 @@ extern "C" moe_status_t moe_forward_static_scratch(moe_layer_t *L, const void *x
                     r->T, need, kStaticScratchBytes);
 
     void *base = nullptr;
-    st = scratch_address(&base);
+    st = scratch_address(L->device, &base);
     if (st != MOE_OK) return st;
     uint8_t *b = static_cast<uint8_t *>(base);
 
@@ -113,6 +122,7 @@ extern "C" moe_status_t moe_forward_static_scratch(moe_layer_t *L, const void *x
     a.n_rows_cap = rows;
     const bool gated = c.expert == MOE_EXPERT_SWIGLU;
     const WeightType wt = (c.weight_dtype == MOE_I8) ? WeightType::kI8 : WeightType::kBF16;
+    L->stats.gemv_runs += 1;
     st = launch_phase(L, MOE_PHASE_UP, s, "decode_up",
                       [&] { return launch_decode_up(a, wt, gated, s_up, L->num_sms, s); });
     if (st == MOE_OK && s_up > 1)
