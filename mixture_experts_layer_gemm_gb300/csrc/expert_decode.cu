@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kTok = 8 * NT;  // tokens per pass
     constexpr int kBK = WTraits<WT>::kBK;
     __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
+    __shared__ uint64_t rows_bar;  // token rows of the current (expert, split, pass) staged
     __shared__ int s_act[kMaxPassEntries], s_tp[kMaxPassEntries];  // (expert, pass) entries
     __shared__ int s_nact;
     __shared__ volatile int s_abort;
@@ -191,36 +192,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         pdl_trigger();
     }
 
-    if (tid == 0) {
+    if (warp == 0) {
+        // One warp lists the (expert, token pass) entries: lane l takes the
+        // candidate experts l, l + 32 (all experts, or those of a.only, in
+        // order), so their offsets are read in one round trip.  A malformed
+        // segment keeps one entry, whose unit then reports it.
+        const bool only = a.n_only > 0;
+        const int ncand = only ? min(a.n_only, kMaxExperts) : a.E;
         int n = 0;
-        // one entry per token pass of each expert; a malformed segment keeps
-        // one entry, whose unit then reports it
-        auto add = [&](int e) {
-            const int off = a.offsets[e], end = a.offsets[e + 1];
-            const int q = (off < 0 || end > rows_total || end < off) ? 1 : end - off;
-            for (int tp = 0; tp * kTok < q; ++tp) {
-                if (n == kMaxPassEntries) {
-                    flag_error(a.err, kErrOffsets);
-                    return;
-                }
-                s_act[n] = e;
-                s_tp[n] = tp;
-                ++n;
+        for (int c0 = 0; c0 < ncand; c0 += 32) {
+            const int ci = c0 + lane;
+            int e = -1, np = 0;
+            if (ci < ncand) {
+                e = only ? a.only[ci] : ci;
+                const int off = a.offsets[e], end = a.offsets[e + 1];
+                const bool bad = off < 0 || end > rows_total || end < off;
+                if (only || end > off) np = ((bad ? 1 : end - off) + kTok - 1) / kTok;
             }
-        };
-        if (a.n_only > 0) {
-            for (int i = 0; i < a.n_only && i < kMaxExperts; ++i) add(a.only[i]);
-        } else {
-            for (int e = 0; e < a.E; ++e)
-                if (a.offsets[e + 1] > a.offsets[e]) add(e);
+            int incl = np;  // inclusive prefix sum of the pass counts over lanes
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            const int base = n + incl - np;
+            for (int tp = 0; tp < np; ++tp) {
+                if (base + tp >= kMaxPassEntries) {
+                    flag_error(a.err, kErrOffsets);
+                    break;
+                }
+                s_act[base + tp] = e;
+                s_tp[base + tp] = tp;
+            }
+            n += __shfl_sync(0xffffffffu, incl, 31);
         }
-        s_nact = n;
-        s_abort = 0;
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], kConsumerWarps);
+        if (lane == 0) {
+            s_nact = min(n, kMaxPassEntries);
+            s_abort = 0;
+            for (int i = 0; i < kStages; ++i) {
+                mbar_init(&full_bar[i], 1);
+                mbar_init(&empty_bar[i], kConsumerWarps);
+            }
+            mbar_init(&rows_bar, 1);
+            fence_barrier_init();
         }
-        fence_barrier_init();
     }
     __syncthreads();
     const long long units = static_cast<long long>(s_nact) * geo.splits * geo.rg8;
@@ -234,6 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // one phase in flight, the last one issued.
     uint32_t last_parity[kStages];
     bool used[kStages];
+    uint32_t rows_phase = 0, rows_last = 0;  // token-row staging: next and last issued parity
+    bool rows_issued = false;
     for (int i = 0; i < kStages; ++i) used[i] = false;
     if (warp == kConsumerWarps) {
         // ================= producer: stream weight stages into the ring ==========
@@ -295,36 +312,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rg = 8 * U.g8 + warp;
         {
             const int tp = U.tp;  // this unit's token pass
-            // ---- stage this pass's token rows (bf16) in shared memory
+            // ---- stage this pass's token rows (bf16) in shared memory: one
+            // bulk copy per row (the copy engine, a single round trip), issued
+            // by the lanes of consumer warp 0.  Rows past the segment are not
+            // copied: their MMA columns are tokens whose results are never
+            // stored.
             if (staged_e != U.e || staged_ks != U.ks || staged_tp != tp) {
+                // every consumer is past its reads (and the int8 in-place
+                // conversion) of the previous rows before the copy engine
+                // overwrites them
+                fence_proxy_async_smem();
                 named_sync(kBarConsumers, kConsumers);
-                const int vec_per_row = kcount / 8;
-                for (int idx = tid; idx < kTok * vec_per_row; idx += kConsumers) {
-                    const int r = idx / vec_per_row, v = idx - r * vec_per_row;
-                    const int pos = U.off + tp * kTok + r;
-                    uint4 val = make_uint4(0, 0, 0, 0);
-                    if (pos < U.end) {
+                if (warp == 0) {
+                    const int pos = U.off + tp * kTok + lane;
+                    const bool row = lane < kTok && pos < U.end;
+                    const uint16_t *src = nullptr;
+                    if (row) {
                         if (PHASE == kUp) {
-                            const int fi = a.gather[pos];
-                            if (fi >= 0 && fi < rows_total) {
-                                const uint16_t *src = static_cast<const uint16_t *>(a.x) +
-                                                      static_cast<size_t>(fi / a.k) * geo.K;
-                                val = ld_nc_v4(src + kbase + v * 8);
-                            } else if (v == 0) {
+                            int fi = a.gather[pos];
+                            if (fi < 0 || fi >= rows_total) {  // reported; a valid row stands in
                                 flag_error(a.err, kErrGatherIndex);
+                                fi = 0;
                             }
+                            src = static_cast<const uint16_t *>(a.x) + static_cast<size_t>(fi / a.k) * geo.K + kbase;
                         } else {
-                            const uint16_t *src =
-                                static_cast<const uint16_t *>(a.h) + static_cast<size_t>(pos) * geo.K;
-                            val = ld_nc_v4(src + kbase + v * 8);
+                            src = static_cast<const uint16_t *>(a.h) + static_cast<size_t>(pos) * geo.K + kbase;
                         }
                     }
-                    *reinterpret_cast<uint4 *>(bstage + static_cast<size_t>(r) * geo.row_bytes + v * 16) = val;
+                    const uint32_t nrows = __popc(__ballot_sync(0xffffffffu, row));
+                    if (lane == 0) mbar_arrive_expect_tx(&rows_bar, nrows * static_cast<uint32_t>(kcount) * 2u);
+                    __syncwarp();
+                    if (row)
+                        bulk_g2s(bstage + static_cast<size_t>(lane) * geo.row_bytes, src,
+                                 static_cast<uint32_t>(kcount) * 2u, &rows_bar);
                 }
+                rows_issued = true;
+                rows_last = rows_phase;
+                const bool landed = mbar_wait(&rows_bar, rows_phase);
+                if (named_sync_or(kBarConsumers, kConsumers, !landed)) {
+                    if (tid == 0) flag_error(a.err, kErrWaitTimeout);
+                    s_abort = 1;
+                    break;
+                }
+                rows_phase ^= 1u;
                 staged_e = U.e;
                 staged_ks = U.ks;
                 staged_tp = tp;
-                named_sync(kBarConsumers, kConsumers);
                 if constexpr (WT == WeightType::kI8) {
                     stage_rows_f16<kTok>(bstage, geo.row_bytes, kcount / 8, warp, lane, s_xscale, s_xsum);
                     named_sync(kBarConsumers, kConsumers);
@@ -461,6 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kConsumerWarps && lane == 0)
         for (int i = 0; i < kStages; ++i)
             if (used[i]) mbar_wait(&full_bar[i], last_parity[i]);
+    // a token-row staging whose wait gave up may still be landing
+    if (tid == 0 && rows_issued) mbar_wait(&rows_bar, rows_last);
 }
 
 // h = act(sum_s gate_part[s]) [* sum_s up_part[s]] for split-K up projections.

@@ -72,19 +72,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pdl_wait();
     pdl_trigger();
 
-    if (tid == 0) {
-        s_nact = tc_list_tiles(a, geo, s_act, s_off, s_q, s_prefix);
-        s_abort = 0;
-        for (int i = 0; i < geo.stages; ++i) {
-            mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], 1);
+    if (warp == 0) {
+        // the whole warp lists the tiles (one round trip for the offsets)
+        const int n_listed = tc_list_tiles(a, geo, s_act, s_off, s_q, s_prefix, lane);
+        if (lane == 0) {
+            s_nact = n_listed;
+            s_abort = 0;
+            for (int i = 0; i < geo.stages; ++i) {
+                mbar_init(&full_bar[i], 1);
+                mbar_init(&empty_bar[i], 1);
+            }
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&tfull_bar[i], 1);
+                mbar_init(&tempty_bar[i], kEpiWarps);
+            }
+            mbar_init(&done_bar, 1);
+            fence_barrier_init();
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&tfull_bar[i], 1);
-            mbar_init(&tempty_bar[i], kEpiWarps);
-        }
-        mbar_init(&done_bar, 1);
-        fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(&s_tmem, geo.tmem_cols);
     tc_fence_before();

@@ -117,12 +117,6 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Order this thread's generic-proxy shared-memory accesses before later
-// async-proxy (bulk copy, tensor core) accesses of the same memory.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ---- tensor-map bulk copy (2D tile, global -> shared) ----------------------------------
 __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, int c0, int c1,
                                             uint64_t *bar) {

@@ -49,33 +49,53 @@ __device__ __forceinline__ TcTile tc_tile(long long u, const long long *prefix, 
     return t;
 }
 
-// One thread: list the experts this launch covers (all with tokens, or those
-// in a.only), their segments, and the prefix sums of their tile counts.
-// Returns the number of experts listed.
+// One warp (all 32 lanes): list the experts this launch covers (all with
+// tokens, or those in a.only), in ascending expert order, their segments, and
+// the prefix sums of their tile counts.  Lane l examines experts l and l + 32,
+// so every offset is read in one round trip; a ballot compacts the list and a
+// shuffle scan sums the tiles.  Returns the number of experts listed (in
+// every lane).
 __device__ __forceinline__ int tc_list_tiles(const ExpertArgs &a, const TcGeom &geo, int *act,
-                                             int *offs, int *qs, long long *prefix) {
+                                             int *offs, int *qs, long long *prefix, int lane) {
     const int rows_total = a.T * a.k;
     int n = 0;
     long long acc = 0;
-    prefix[0] = 0;
-    for (int e = 0; e < a.E; ++e) {
-        const int off = a.offsets[e], end = a.offsets[e + 1];
-        if (off < 0 || end > rows_total || end < off) {
-            flag_error(a.err, kErrOffsets);
-            continue;
+    if (lane == 0) prefix[0] = 0;
+    for (int e0 = 0; e0 < a.E; e0 += 32) {
+        const int e = e0 + lane;
+        bool take = false;
+        int off = 0, q = 0;
+        if (e < a.E) {
+            off = a.offsets[e];
+            const int end = a.offsets[e + 1];
+            if (off < 0 || end > rows_total || end < off) {
+                flag_error(a.err, kErrOffsets);
+            } else {
+                q = end - off;
+                take = q > 0;
+                if (take && a.n_only > 0) {
+                    bool listed = false;
+                    for (int i = 0; i < a.n_only; ++i) listed |= a.only[i] == e;
+                    take = listed;
+                }
+            }
         }
-        const int q = end - off;
-        bool take = q > 0;
-        if (a.n_only > 0) {
-            take = false;
-            for (int i = 0; i < a.n_only; ++i) take |= (a.only[i] == e && q > 0);
+        const unsigned mask = __ballot_sync(0xffffffffu, take);
+        const int idx = n + __popc(mask & ((1u << lane) - 1u));
+        long long incl = take ? static_cast<long long>(geo.splits) * geo.n_rb * ((q + geo.N - 1) / geo.N) : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
         }
-        if (!take) continue;
-        act[n] = e;
-        offs[n] = off;
-        qs[n] = q;
-        acc += static_cast<long long>(geo.splits) * geo.n_rb * ((q + geo.N - 1) / geo.N);
-        prefix[++n] = acc;
+        if (take) {
+            act[idx] = e;
+            offs[idx] = off;
+            qs[idx] = q;
+            prefix[idx + 1] = acc + incl;
+        }
+        acc += __shfl_sync(0xffffffffu, incl, 31);
+        n += __popc(mask);
     }
     return n;
 }
