@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             s_abort = 0;
             for (int i = 0; i < kStages; ++i) {
                 mbar_init(&full_bar[i], 1);
-                mbar_init(&empty_bar[i], kConsumerWarps);
+                mbar_init(&empty_bar[i], kConsumers);  // every consumer lane releases
             }
             mbar_init(&rows_bar, 1);
             fence_barrier_init();
@@ -380,46 +380,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                         s_abort = 1;
                     }
                 }
-                if (have && mine) {
-                    const uint32_t blk = ring_sm + stage * kStageBytes + warp * kBlockBytes;
+                if (have) {
+                    // This warp's weight fragments of the stage into registers,
+                    // then the slot goes back to the producer at once (each
+                    // lane's arrive releases its own reads), so the copy
+                    // engine refills it while the MMAs below run.  The token
+                    // operands live in the staged rows, outside the ring.
+                    uint4 ra[2], rb[2];
+                    if (mine) {
+                        const uint32_t blk = ring_sm + stage * kStageBytes + warp * kBlockBytes;
 #pragma unroll
-                    for (int sh = 0; sh < 2; ++sh) {
-                        const uint32_t atom = blk + sh * 512 + atom_chunk_offset(g, t);
-                        const uint4 ra = lds_v4(atom);         // row g
-                        const uint4 rb = lds_v4(atom + 1024);  // row g + 8
-                        const int kcol = (kb - U.kb0) * kBK + sh * (kBK / 2);  // in the staged rows
-                        if constexpr (WT == WeightType::kBF16) {
+                        for (int sh = 0; sh < 2; ++sh) {
+                            const uint32_t atom = blk + sh * 512 + atom_chunk_offset(g, t);
+                            ra[sh] = lds_v4(atom);         // row g
+                            rb[sh] = lds_v4(atom + 1024);  // row g + 8
+                        }
+                    }
+                    mbar_arrive(&empty_bar[stage]);
+                    if (mine) {
 #pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) {
-                                const uint4 xb =
-                                    lds_v4(bsm + (nt * 8 + g) * geo.row_bytes + (kcol + 8 * t) * 2);
-                                mma_bf16_16816(acc[nt], ra.x, rb.x, ra.y, rb.y, xb.x, xb.y);
-                                mma_bf16_16816(acc[nt], ra.z, rb.z, ra.w, rb.w, xb.z, xb.w);
-                            }
-                        } else {
-                            uint32_t al[4], ah[4], bl[4], bh[4];
-                            const uint32_t va[4] = {ra.x, ra.y, ra.z, ra.w};
-                            const uint32_t vb[4] = {rb.x, rb.y, rb.z, rb.w};
+                        for (int sh = 0; sh < 2; ++sh) {
+                            const int kcol = (kb - U.kb0) * kBK + sh * (kBK / 2);  // in the staged rows
+                            if constexpr (WT == WeightType::kBF16) {
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                i8x4_to_f16x2x2_biased(va[i], al[i], ah[i]);
-                                i8x4_to_f16x2x2_biased(vb[i], bl[i], bh[i]);
-                            }
+                                for (int nt = 0; nt < NT; ++nt) {
+                                    const uint4 xb =
+                                        lds_v4(bsm + (nt * 8 + g) * geo.row_bytes + (kcol + 8 * t) * 2);
+                                    mma_bf16_16816(acc[nt], ra[sh].x, rb[sh].x, ra[sh].y, rb[sh].y, xb.x, xb.y);
+                                    mma_bf16_16816(acc[nt], ra[sh].z, rb[sh].z, ra[sh].w, rb[sh].w, xb.z, xb.w);
+                                }
+                            } else {
+                                uint32_t al[4], ah[4], bl[4], bh[4];
+                                const uint32_t va[4] = {ra[sh].x, ra[sh].y, ra[sh].z, ra[sh].w};
+                                const uint32_t vb[4] = {rb[sh].x, rb[sh].y, rb[sh].z, rb[sh].w};
 #pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) {
-                                const uint32_t xa = bsm + (nt * 8 + g) * geo.row_bytes + (kcol + 16 * t) * 2;
-                                const uint4 x0 = lds_v4(xa);
-                                const uint4 x1 = lds_v4(xa + 16);
-                                mma_f16_16816(acc[nt], al[0], bl[0], ah[0], bh[0], x0.x, x0.y);
-                                mma_f16_16816(acc[nt], al[1], bl[1], ah[1], bh[1], x0.z, x0.w);
-                                mma_f16_16816(acc[nt], al[2], bl[2], ah[2], bh[2], x1.x, x1.y);
-                                mma_f16_16816(acc[nt], al[3], bl[3], ah[3], bh[3], x1.z, x1.w);
+                                for (int i = 0; i < 4; ++i) {
+                                    i8x4_to_f16x2x2_biased(va[i], al[i], ah[i]);
+                                    i8x4_to_f16x2x2_biased(vb[i], bl[i], bh[i]);
+                                }
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt) {
+                                    const uint32_t xa = bsm + (nt * 8 + g) * geo.row_bytes + (kcol + 16 * t) * 2;
+                                    const uint4 x0 = lds_v4(xa);
+                                    const uint4 x1 = lds_v4(xa + 16);
+                                    mma_f16_16816(acc[nt], al[0], bl[0], ah[0], bh[0], x0.x, x0.y);
+                                    mma_f16_16816(acc[nt], al[1], bl[1], ah[1], bh[1], x0.z, x0.w);
+                                    mma_f16_16816(acc[nt], al[2], bl[2], ah[2], bh[2], x1.x, x1.y);
+                                    mma_f16_16816(acc[nt], al[3], bl[3], ah[3], bh[3], x1.z, x1.w);
+                                }
                             }
                         }
                     }
                 }
-                __syncwarp();
-                if (have && lane == 0) mbar_arrive(&empty_bar[stage]);
                 if (++stage == kStages) {
                     stage = 0;
                     phase ^= 1u;
