@@ -168,10 +168,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// true when the phase with the given parity completed, false after the limit
+// Non-blocking test of a phase.  A try_wait on a phase that has already
+// completed returns at once in isolation (~23 cycles), but costs ~235 cycles
+// when issued by a thread with tensor-core MMAs or commits in flight, which
+// is exactly what the MMA-issuing threads do between stages; test_wait stays
+// at ~23 cycles there (measured: an int8 MMA issuer's stage, two ready waits
+// plus 8 MMAs and 2 commits, 919 cycles with try_wait, 526 with test_wait).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// true when the phase with the given parity completed, false after the limit.
+// A completed phase is caught by the cheap test; otherwise the thread polls
+// with try_wait, which may suspend it and so leaves issue slots to the
+// other warps.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_test_wait(bar, parity)) return true;
     for (uint32_t i = 0; i < kWaitLimit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// The same wait by spinning on test_wait, for a single thread on the critical
+// path (an MMA issuer) that should notice the phase as soon as it completes.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kWaitLimit; ++i)
+        if (mbar_test_wait(bar, parity)) return true;
     return false;
 }
 

@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
                 const int buf = ntile & 1;
                 const uint32_t use_parity = (ntile >> 1) & 1;
-                if (!mbar_wait(&tempty_bar[buf], use_parity ^ 1u)) {
+                if (!mbar_wait_spin(&tempty_bar[buf], use_parity ^ 1u)) {
                     flag_error(a.err, kErrWaitTimeout);
                     s_abort = 1;
                     break;
@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int n_valid = min(geo.N, (t.q - t.tt * geo.N + 15) / 16 * 16);
                 const uint32_t idesc = idesc_bf16_f32(128, n_valid);
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
-                    if (!mbar_wait(&full_bar[stage], phase)) {
+                    if (!mbar_wait_spin(&full_bar[stage], phase)) {
                         flag_error(a.err, kErrWaitTimeout);
                         s_abort = 1;
                         break;

@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
                 const int buf = ntile & 1;
                 const uint32_t use_parity = (ntile >> 1) & 1;
-                if (!mbar_wait_cluster(&tempty_bar[buf], use_parity ^ 1u)) {
+                if (!mbar_wait_cluster_spin(&tempty_bar[buf], use_parity ^ 1u)) {
                     flag_error(a.err, kErrWaitTimeout);
                     s_abort = 1;
                     break;
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nv = min(kN, (t.q - t.tt * kN + 31) / 32 * 32);
                 const uint32_t idesc = idesc_bf16_f32(256, nv);
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
-                    if (!mbar_wait_cluster(&full_bar[stage], phase)) {
+                    if (!mbar_wait_cluster_spin(&full_bar[stage], phase)) {
                         flag_error(a.err, kErrWaitTimeout);
                         s_abort = 1;
                         break;

@@ -23,8 +23,9 @@
 //     B from shared memory, D = 128 lanes x N fp32 columns (two buffers, one
 //     accumulator per MMA issuer in each).
 // Tensor memory: D buffers at columns [0, 2N) with one issuer (N <= 192) or
-// [0, 4N) with two (N <= 96; buffer b, issuer i at (2b + i) N), A buffers at
-// [384, 512); 512 columns allocated (one CTA per SM).
+// [0, 4N) with two (N <= 96; buffer b, issuer i at (2b + i) N), A buffers of
+// 64 columns from the next multiple of 64 up to column 512 (two at N = 192,
+// six at N = 32); 512 columns allocated (one CTA per SM).
 // Warp roles (480 threads): 0 producer, 1 tensor-memory owner + MMA issuer,
 // 2-5 epilogue, 6-13 converters, 14 second MMA issuer.  A small-N MMA stream
 // from one thread is paced by that thread's instructions, so where four
@@ -50,9 +51,12 @@ constexpr int kA8Bytes = 16384;  // 128 rows x 128 int8
 constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 200 * 1024;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kACol = 384;  // first column of the A buffers (after two D buffers of N <= 192)
-constexpr int kABufs = 2;        // A buffers of 64 columns at [384, 512)
-static_assert(kACol + kABufs * 64 <= kTmemCols && 2 * kTcI8MaxN <= kACol, "tensor-memory columns");
+// A buffers (64 columns each) fill the columns above the accumulators, from
+// the first multiple of 64 at or past them: two at N = 192, up to seven at
+// N = 16, so that the converters can run ahead of the MMAs.
+constexpr int kMaxABufs = 7;
+constexpr uint32_t kTwoIssuerCols = 384;  // two issuers while their four D buffers fit here
+static_assert(2 * kTcI8MaxN + 2 * 64 <= kTmemCols, "tensor-memory columns: two A buffers at N = max");
 
 enum Phase { kUp = 0, kDown = 1 };
 
@@ -62,7 +66,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const __grid_constant__ CUtensorMap bmap) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
-    __shared__ uint64_t afull_bar[kABufs], aempty_bar[kABufs];
+    __shared__ uint64_t afull_bar[kMaxABufs], aempty_bar[kMaxABufs];
     __shared__ uint64_t tfull_bar[2], tempty_bar[2], done_bar[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_act[kMaxExperts], s_off[kMaxExperts], s_q[kMaxExperts];
@@ -77,7 +81,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // MMA issuers: two where both accumulator buffers of both fit below the A buffers
-    const int nis = (4 * geo.N <= static_cast<int>(kACol)) ? 2 : 1;
+    const int nis = (4 * geo.N <= static_cast<int>(kTwoIssuerCols)) ? 2 : 1;
+    const uint32_t a_col0 = static_cast<uint32_t>((2 * nis * geo.N + 63) / 64 * 64);
+    const int nab = min(kMaxABufs, static_cast<int>((kTmemCols - a_col0) / 64));
     pdl_wait();
     pdl_trigger();
 
@@ -91,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_init(&full_bar[i], 1);
                 mbar_init(&empty_bar[i], 1 + kCvtWarps);  // MMA commit + converter warps
             }
-            for (int i = 0; i < kABufs; ++i) {
+            for (int i = 0; i < nab; ++i) {
                 mbar_init(&afull_bar[i], kCvtWarps);
                 mbar_init(&aempty_bar[i], 1);
             }
@@ -158,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
                 const int buf = ntile & 1;
                 const uint32_t use_parity = (ntile >> 1) & 1;
-                if (!mbar_wait(&tempty_bar[buf], use_parity ^ 1u)) {
+                if (!mbar_wait_spin(&tempty_bar[buf], use_parity ^ 1u)) {
                     flag_error(a.err, kErrWaitTimeout);
                     s_abort = 1;
                     break;
@@ -174,13 +180,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             stage = 0;
                             phase ^= 1u;
                         }
-                        if (++abuf == kABufs) {
+                        if (++abuf == nab) {
                             abuf = 0;
                             aphase ^= 1u;
                         }
                         continue;
                     }
-                    if (!mbar_wait(&full_bar[stage], phase) || !mbar_wait(&afull_bar[abuf], aphase)) {
+                    if (!mbar_wait_spin(&full_bar[stage], phase) || !mbar_wait_spin(&afull_bar[abuf], aphase)) {
                         flag_error(a.err, kErrWaitTimeout);
                         s_abort = 1;
                         break;
@@ -194,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t bbase = smem_u32(smem + stage * stage_bytes + kA8Bytes);
                     const uint64_t bd0 = smem_desc(bbase, 16, 1024, kLayoutSw128);
                     const uint64_t bd1 = smem_desc(bbase + geo.b_bytes, 16, 1024, kLayoutSw128);
-                    const uint32_t acol = tmem_base + kACol + static_cast<uint32_t>(abuf * 64);
+                    const uint32_t acol = tmem_base + a_col0 + static_cast<uint32_t>(abuf * 64);
                     tc_mma_tmem_a(d, acol, bd0, idesc, accum);
                     accum = 1;
 #pragma unroll
@@ -206,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         stage = 0;
                         phase ^= 1u;
                     }
-                    if (++abuf == kABufs) {
+                    if (++abuf == nab) {
                         abuf = 0;
                         aphase ^= 1u;
                     }
@@ -348,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     i8x4_to_bf16x2x2(q.w, wv[c * 8 + 6], wv[c * 8 + 7]);
                 }
                 tc_fence_after();
-                tmem_st32(tmem_base + (static_cast<uint32_t>(lq * 32) << 16) + kACol +
+                tmem_st32(tmem_base + (static_cast<uint32_t>(lq * 32) << 16) + a_col0 +
                               static_cast<uint32_t>(abuf * 64 + hk * 32),
                           wv);
                 tmem_st_wait();
@@ -363,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     stage = 0;
                     phase ^= 1u;
                 }
-                if (++abuf == kABufs) {
+                if (++abuf == nab) {
                     abuf = 0;
                     aphase ^= 1u;
                 }

@@ -163,9 +163,23 @@ __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorM
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Non-blocking test (acquire at cluster scope) of a phase that the other CTA
+// of the pair may have completed.
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Wait (acquire at cluster scope) for a phase that the other CTA of the pair
-// may have completed; bounded like mbar_wait.
+// may have completed; bounded like mbar_wait, with the same cheap test first.
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity) {
+    if (mbar_test_wait_cluster(bar, parity)) return true;
     for (uint32_t i = 0; i < kWaitLimit; ++i) {
         uint32_t ok;
         asm volatile(
@@ -177,6 +191,12 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
             : "memory");
         if (ok) return true;
     }
+    return false;
+}
+// The spinning form for the pair's MMA-issuing thread (see mbar_wait_spin).
+__device__ __forceinline__ bool mbar_wait_cluster_spin(uint64_t *bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kWaitLimit; ++i)
+        if (mbar_test_wait_cluster(bar, parity)) return true;
     return false;
 }
 
