@@ -427,9 +427,20 @@ def measure(args, world, local, shape, layer, tokens, xs_np, steps, warmup, weig
     layer_flops = flops_up + sum(w["down_flops"] for w in work.values())
     layer_tf = layer_flops * steps / (ms * 1e-3) / 1e12
 
-    # per-T breakdown: each batch alone, event-timed per launch
+    # per-T breakdown: each batch alone; first its wall time per layer call
+    # (route + forward, no per-launch events, so programmatic launch overlaps
+    # the kernels as in the timed region), then every launch event-timed
     per_t = {}
     for i, T in enumerate(tokens):
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0.record(stream)
+        for it in range(20):
+            c = copies[it % len(copies)]
+            c.route(xs[T], stream=stream)
+            c.forward(xs[T], ys[T], stream=stream)
+        w1.record(stream)
+        torch.cuda.synchronize()
+        wall_us = w0.elapsed_time(w1) / 20 * 1e3
         for c in copies:
             c.timings(reset=True)
             c.set_timing(True)
@@ -453,7 +464,8 @@ def measure(args, world, local, shape, layer, tokens, xs_np, steps, warmup, weig
         t_hbm = w["layer_bytes"] / (hbm * 1e9) * 1e6
         t_tc = w["layer_flops"] / (tf * 1e12) * 1e6
         roof_us = max(t_hbm, t_tc)
-        per_t[str(T)] = {"path": w["path"], "plan": plan, "active_experts": active[T], "layer_us": tot * 1e3,
+        per_t[str(T)] = {"path": w["path"], "plan": plan, "active_experts": active[T],
+                         "layer_us_wall": wall_us, "layer_us": tot * 1e3,
                          "up_us": u_ms * 1e3, "down_us": d_ms * 1e3,
                          "up_gbs": w["up_bytes"] / (u_ms * 1e-3) / 1e9,
                          "down_gbs": w["down_bytes"] / (d_ms * 1e-3) / 1e9,
@@ -462,7 +474,7 @@ def measure(args, world, local, shape, layer, tokens, xs_np, steps, warmup, weig
                          "layer_gbs": w["layer_bytes"] / (tot * 1e-3) / 1e9,
                          "layer_tflops": w["layer_flops"] / (tot * 1e-3) / 1e12,
                          "roof": {"bound": "tensor" if t_tc > t_hbm else "hbm", "us": roof_us,
-                                  "frac": roof_us / (tot * 1e3)}}
+                                  "frac": roof_us / (tot * 1e3), "frac_wall": roof_us / wall_us}}
 
     # the dominant kernel: the expert up-projection; HBM-bound while the batch is
     # weight-streaming, tensor-bound once most of the work runs on the tensor-core path

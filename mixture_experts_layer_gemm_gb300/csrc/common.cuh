@@ -97,6 +97,20 @@ __device__ __forceinline__ void i8x4_to_f16x2x2_biased(uint32_t v, uint32_t &lo,
 }
 constexpr float kI8F16Bias = 1152.0f;
 
+// Power-of-two scaling of a row of bf16 activations into fp16 for the int8
+// paths whose MMAs run in fp16: the shift s puts the row's largest magnitude mx
+// in [2^14, 2^15), so every bf16 value of the row whose scaled magnitude is at
+// least 2^-17 (all within a factor 2^31 of mx) is an exact fp16 value.  A row of
+// zeros, or one holding an infinity or NaN, keeps s = 0.
+__device__ __forceinline__ int f16_row_shift(float mx) {
+    const int eb = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu);
+    const int sh = (eb == 0 || eb == 255) ? 0 : eb - 127 - 14;
+    return sh < -100 ? -100 : (sh > 113 ? 113 : sh);
+}
+__device__ __forceinline__ float pow2f(int e) {  // 2^e for e in [-126, 127]
+    return __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+}
+
 // Four signed int8 values (one 32-bit word, byte 0 first) -> two bf16x2 words
 // holding bytes (0,1) and (2,3), exactly, with byte permutes and one packed
 // bf16 FMA per pair (no int-to-float or float-to-bf16 conversions).

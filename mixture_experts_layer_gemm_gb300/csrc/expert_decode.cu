@@ -110,10 +110,8 @@ __device__ __forceinline__ void stage_rows_f16(uint8_t *bstage, int row_bytes, i
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const int eb = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu);
-        int sh = (eb == 0 || eb == 255) ? 0 : eb - 127 - 14;
-        sh = sh < -100 ? -100 : (sh > 113 ? 113 : sh);
-        const float down = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);  // 2^-sh
+        const int sh = f16_row_shift(mx);
+        const float down = pow2f(-sh);
         float sum = 0.0f;
         for (int v = lane; v < vec_per_row; v += 32) {
             const uint4 q = row[v];
@@ -128,7 +126,7 @@ __device__ __forceinline__ void stage_rows_f16(uint8_t *bstage, int row_bytes, i
         }
         sum = warp_sum(sum);
         if (lane == 0) {
-            s_xscale[r] = __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);  // 2^sh
+            s_xscale[r] = pow2f(sh);
             s_xsum[r] = sum;
         }
     }

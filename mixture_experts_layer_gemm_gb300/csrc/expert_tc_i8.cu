@@ -2,10 +2,17 @@
 // (per-output-channel symmetric codes; DeepSpeed-Inference article, part 4:
 // INT8 weights dequantised inside the kernel).
 //
-// Numerics: the codes q (|q| <= 127) are exact in bf16, so the tensor cores
-// compute sum_k q[row, k] x[token, k] in fp32 from bf16 operands, and the
-// epilogue multiplies by the row's scale -- the same "scale after the dot
-// product" as the int8 weight-streaming GEMV.
+// Numerics.  Down projection: the codes q (|q| <= 127) are exact in bf16, so
+// the tensor cores compute sum_k q[row, k] h[token, k] in fp32 from bf16
+// operands, and the epilogue multiplies by the row's scale -- the same "scale
+// after the dot product" as the int8 weight-streaming GEMV.  Up projection:
+// the operands are fp16, which widens codes in a third of the instructions of
+// bf16 (the converters bound this kernel at small token tiles): the A operand
+// is 1152 + q (exact; fp16 bit pattern 0x6400 | (q + 128)), the B operand the
+// token row times 2^-s (gather_rows_f16_kernel: exact for every value within a
+// factor 2^31 of the row's largest), and the epilogue forms
+// (acc - 1152 * sum_k x'[token, k]) * 2^s * scale[row], the row sum x' taken
+// over the tile's reduction split.
 //
 // Shared-memory traffic, not the tensor pipe, bounds the bf16 grouped GEMM
 // (TMA fill + operand reads).  Widening int8 to bf16 in shared memory would
@@ -17,8 +24,8 @@
 //     swizzle);
 //   converter warps (two per TMEM lane quarter; a thread takes one weight row
 //     and one half of the stage's reduction range) widen 64 codes to 32
-//     bf16x2 words and store them to an A buffer in tensor memory (two
-//     buffers of 64 columns);
+//     fp16x2 (up) or bf16x2 (down) words and store them to an A buffer in
+//     tensor memory (buffers of 64 columns);
 //   an MMA thread issues 8 MMAs of K = 16 per stage, A from tensor memory,
 //     B from shared memory, D = 128 lanes x N fp32 columns (two buffers, one
 //     accumulator per MMA issuer in each).
@@ -60,6 +67,26 @@ static_assert(2 * kTcI8MaxN + 2 * 64 <= kTmemCols, "tensor-memory columns: two A
 
 enum Phase { kUp = 0, kDown = 1 };
 
+// The fp16 token rows of a tile (up projection): the scale of each row (into
+// sc) and its sum over reduction split ks (into sm), one lane per token; zero
+// for tokens past the segment.
+__device__ __forceinline__ void stage_row_factors(const ExpertArgs &a, int off, int tok0, int q, int n, int ks,
+                                                  float *sc, float *sm, int lane) {
+    __syncwarp();  // every lane is past its reads of the previous tile's factors
+    for (int c = lane; c < n; c += 32) {
+        const int tok = tok0 + c;
+        float f = 0.0f, sum = 0.0f;
+        if (tok < q) {
+            const int pos = off + tok;
+            f = a.x_scale[pos];
+            sum = a.x_sum[static_cast<size_t>(ks) * a.xsum_stride + pos];
+        }
+        sc[c] = f;
+        sm[c] = sum;
+    }
+    __syncwarp();
+}
+
 template <int PHASE, bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_i8_kernel(const ExpertTables tab, const ExpertArgs a, const TcGeom geo,
@@ -73,7 +100,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ long long s_prefix[kMaxExperts + 1];
     __shared__ int s_nact;
     __shared__ volatile int s_abort;
-    __shared__ float s_w[kEpiWarps][kTcMaxTileTokens];  // down: routing weights of the tile
+    // down: routing weights of the tile's tokens; up: the scales of their fp16 rows
+    __shared__ float s_w[kEpiWarps][kTcMaxTileTokens];
+    __shared__ float s_xs[kEpiWarps][kTcMaxTileTokens];  // up: the rows' sums over the tile's split
 
     const uint32_t raw_s = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
@@ -172,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>((buf * nis + me) * geo.N);
                 const int n_valid = min(geo.N, (t.q - t.tt * geo.N + 15) / 16 * 16);
-                const uint32_t idesc = idesc_bf16_f32(128, n_valid);
+                const uint32_t idesc = PHASE == kUp ? idesc_f16_f32(128, n_valid) : idesc_bf16_f32(128, n_valid);
                 uint32_t accum = 0;  // this issuer's first block of the tile starts the sum
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
                     if (((kb - t.kb0) & (nis - 1)) != me) {  // the other issuer's block (nis is 1 or 2)
@@ -252,7 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 scale = tab.s2[t.e][R];
             const int tok0 = t.tt * geo.N;
             const int n_valid = min(geo.N, (t.q - tok0 + 15) / 16 * 16);
-            if (PHASE == kDown) tc_stage_weights(a, t.off, tok0, t.q, n_valid, s_w[lq], lane);
+            if (PHASE == kDown)
+                tc_stage_weights(a, t.off, tok0, t.q, n_valid, s_w[lq], lane);
+            else
+                stage_row_factors(a, t.off, tok0, t.q, n_valid, t.ks, s_w[lq], s_xs[lq], lane);
             // the tile's accumulators: the second issuer's holds a partial sum
             // when the tile has two or more K blocks (a warp-uniform choice)
             const uint32_t dcol = (static_cast<uint32_t>(lq * 32) << 16) + static_cast<uint32_t>(buf * nis * geo.N);
@@ -268,6 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v1[j]));
                 } else {
                     tmem_ld_wait();
+                }
+                if (PHASE == kUp) {  // fp16 operands: take out the code bias, undo the token scales
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        v[j] = __float_as_uint((__uint_as_float(v[j]) - kI8F16Bias * s_xs[lq][c0 + j]) *
+                                               s_w[lq][c0 + j]);
                 }
                 if (PHASE == kUp && GATED) {
                     if (geo.splits == 1) {
@@ -348,10 +386,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 4; ++c) {
                     const uint4 q = lds_v4(a8_s + atom_chunk_offset(g, c));
                     // codes 16c .. 16c + 15 of this half -> columns 8c .. 8c + 7
-                    i8x4_to_bf16x2x2(q.x, wv[c * 8 + 0], wv[c * 8 + 1]);
-                    i8x4_to_bf16x2x2(q.y, wv[c * 8 + 2], wv[c * 8 + 3]);
-                    i8x4_to_bf16x2x2(q.z, wv[c * 8 + 4], wv[c * 8 + 5]);
-                    i8x4_to_bf16x2x2(q.w, wv[c * 8 + 6], wv[c * 8 + 7]);
+                    if (PHASE == kUp) {  // fp16 1152 + code, three instructions per four codes
+                        i8x4_to_f16x2x2_biased(q.x, wv[c * 8 + 0], wv[c * 8 + 1]);
+                        i8x4_to_f16x2x2_biased(q.y, wv[c * 8 + 2], wv[c * 8 + 3]);
+                        i8x4_to_f16x2x2_biased(q.z, wv[c * 8 + 4], wv[c * 8 + 5]);
+                        i8x4_to_f16x2x2_biased(q.w, wv[c * 8 + 6], wv[c * 8 + 7]);
+                    } else {
+                        i8x4_to_bf16x2x2(q.x, wv[c * 8 + 0], wv[c * 8 + 1]);
+                        i8x4_to_bf16x2x2(q.y, wv[c * 8 + 2], wv[c * 8 + 3]);
+                        i8x4_to_bf16x2x2(q.z, wv[c * 8 + 4], wv[c * 8 + 5]);
+                        i8x4_to_bf16x2x2(q.w, wv[c * 8 + 6], wv[c * 8 + 7]);
+                    }
                 }
                 tc_fence_after();
                 tmem_st32(tmem_base + (static_cast<uint32_t>(lq * 32) << 16) + a_col0 +
@@ -392,6 +437,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+constexpr int kGatherThreads = 128;
+constexpr int kMaxSumSplits = 4;  // reduction splits of an int8 tensor-core up projection
+
+// One CTA per permuted row (grid-stride): the row's largest magnitude, then
+// the fp16 row under the power-of-two scale that puts it in [2^14, 2^15), the
+// scale, and the scaled row's sum over each reduction split (fixed order: each
+// thread in element order, the warps' sums in warp order).
+__global__ void __launch_bounds__(kGatherThreads)
+    gather_rows_f16_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ gather, int rows, int k,
+                           int m, int splits, uint16_t *__restrict__ xp, float *__restrict__ x_scale,
+                           float *__restrict__ x_sum, int xsum_stride, uint32_t *err) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float s_red[kGatherThreads / 32][kMaxSumSplits];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int vec = m / 8;     // 16-byte chunks of a row
+    const int nkb = m / 128;   // reduction blocks of 128 elements
+    for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+        const int f = gather[r];
+        const bool ok = f >= 0 && f < rows;
+        if (!ok && tid == 0) flag_error(err, kErrGatherIndex);
+        const uint16_t *src = x + static_cast<size_t>(ok ? f / k : 0) * m;  // a valid row stands in
+        float mx = 0.0f;
+        for (int v = tid; v < vec; v += kGatherThreads) {
+            const uint4 q = ld_nc_v4(src + v * 8);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fmaxf(fabsf(bf16lo(w[i])), fabsf(bf16hi(w[i]))));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) s_red[warp][0] = mx;
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < kGatherThreads / 32; ++w) mx = fmaxf(mx, s_red[w][0]);
+        const int sh = f16_row_shift(mx);
+        const float down = pow2f(-sh);
+        __syncthreads();  // s_red is reused for the sums
+        float sum[kMaxSumSplits];
+#pragma unroll
+        for (int sp = 0; sp < kMaxSumSplits; ++sp) sum[sp] = 0.0f;
+        for (int v = tid; v < vec; v += kGatherThreads) {
+            const int kb = v / 16;  // 16 chunks of 8 elements per reduction block
+            int sp = 0;
+            while (sp + 1 < splits && kb >= (nkb * (sp + 1)) / splits) ++sp;
+            const uint4 q = ld_nc_v4(src + v * 8);
+            uint32_t w[4] = {q.x, q.y, q.z, q.w};
+            float part = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const __half2 hv = __floats2half2_rn(bf16lo(w[i]) * down, bf16hi(w[i]) * down);
+                part += __low2float(hv) + __high2float(hv);
+                w[i] = *reinterpret_cast<const uint32_t *>(&hv);
+            }
+#pragma unroll
+            for (int i = 0; i < kMaxSumSplits; ++i)
+                if (i == sp) sum[i] += part;
+            *reinterpret_cast<uint4 *>(xp + static_cast<size_t>(r) * m + v * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+#pragma unroll
+        for (int sp = 0; sp < kMaxSumSplits; ++sp) {
+            const float v = warp_sum(sum[sp]);
+            if (lane == 0) s_red[warp][sp] = v;
+        }
+        __syncthreads();
+        if (tid < splits) {
+            float tot = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kGatherThreads / 32; ++w) tot += s_red[w][tid];
+            x_sum[static_cast<size_t>(tid) * xsum_stride + r] = tot;
+        }
+        if (tid == 0) x_scale[r] = pow2f(sh);
+        __syncthreads();
+    }
+}
+
 template <int PHASE, bool GATED>
 cudaError_t launch_t(const ExpertArgs &a, const TcGeom &g, const CUtensorMap &bmap, int num_sms,
                      cudaStream_t s) {
@@ -426,6 +547,17 @@ TcGeom make_geom(int K, int rows, int splits, int N) {
 }
 
 }  // namespace
+
+cudaError_t launch_gather_rows_f16(const void *x, const int32_t *gather, int rows, int k, int m, int splits,
+                                   void *x_perm, float *x_scale, float *x_sum, int xsum_stride, uint32_t *err,
+                                   cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    if (splits < 1 || splits > kMaxSumSplits || m % 128) return cudaErrorInvalidValue;
+    const int blocks = rows < 8192 ? rows : 8192;
+    return launch_pdl(gather_rows_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kGatherThreads), 0, s,
+                      static_cast<const uint16_t *>(x), gather, rows, k, m, splits, static_cast<uint16_t *>(x_perm),
+                      x_scale, x_sum, xsum_stride, err);
+}
 
 cudaError_t launch_tc_i8_up(const ExpertArgs &a, bool gated, int splits, int N, const CUtensorMap &xmap,
                             int num_sms, cudaStream_t s) {

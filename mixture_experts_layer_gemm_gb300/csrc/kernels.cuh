@@ -92,6 +92,12 @@ struct ExpertArgs {
     int only[kExpertTableMax];
     int n_only;
     const void *wbase;           // start of the resident weight buffer (CTA-pair kernels)
+    // int8 weights, tensor-core up projection: x_perm holds the permuted token
+    // rows in fp16 under a power-of-two scale per row; x_scale[pos] is that
+    // scale and x_sum[s * xsum_stride + pos] the row's sum over reduction split s
+    const float *x_scale;
+    const float *x_sum;
+    int xsum_stride;
 };
 
 enum class WeightType { kF32, kBF16, kI8 };
@@ -123,9 +129,18 @@ cudaError_t launch_tc_down(const ExpertArgs &a, int splits, int N, const CUtenso
 cudaError_t launch_tc2_up(const ExpertArgs &a, bool gated, const CUtensorMap &wmap, const CUtensorMap &xmap_half,
                           int num_sms, cudaStream_t s);
 
-// The same with int8 weights (K a multiple of 128): codes widened to bf16 in
-// tensor memory, per-row scale in the epilogue; N tokens per tile, 16..128.
+// The same with int8 weights (K a multiple of 128): codes widened exactly in
+// tensor memory -- to fp16 (1152 + code) against the fp16 token rows of
+// launch_gather_rows_f16 in the up projection, to bf16 against the bf16 hidden
+// rows in the down projection -- with the bias, the token scales and the
+// per-row weight scale taken out in the epilogue; N tokens per tile, 16..192.
 constexpr int kTcI8MaxN = 192;
+// x_perm[pos] = x[gather[pos] / k] in fp16 times 2^-s (s from the row's largest
+// magnitude, f16_row_shift), x_scale[pos] = 2^s, and the sums of the scaled
+// row over each of `splits` reduction splits (K blocks of 128) into x_sum.
+cudaError_t launch_gather_rows_f16(const void *x, const int32_t *gather, int rows, int k, int m, int splits,
+                                   void *x_perm, float *x_scale, float *x_sum, int xsum_stride, uint32_t *err,
+                                   cudaStream_t s);
 cudaError_t launch_tc_i8_up(const ExpertArgs &a, bool gated, int splits, int N, const CUtensorMap &xmap,
                             int num_sms, cudaStream_t s);
 cudaError_t launch_tc_i8_down(const ExpertArgs &a, int splits, int N, const CUtensorMap &hmap,

@@ -39,6 +39,9 @@ struct moe_layer {
     CUtensorMap tmap_w;
     float *ypart = nullptr;
     float *gate_part = nullptr, *up_part = nullptr;
+    // int8 layers: per permuted row, the fp16 token rows' power-of-two scale and
+    // their sums per up-projection reduction split ([split_up_max x rows])
+    float *x_scale = nullptr, *x_sum = nullptr;
     size_t decode_rows_cap = 0;
     int split_up_max = 1, split_down_max = 1;
     size_t workspace_bytes = 0;

@@ -398,6 +398,13 @@ static moe_status_t alloc_workspace(moe_layer_t *L) {
         L->x_perm = L->dalloc(rows * c.m * 2, &err);
         if (err) return cuda_fail(err, "cudaMalloc(x_perm)");
         L->workspace_bytes += rows * c.m * 2;
+        if (c.weight_dtype == MOE_I8) {  // scales and split sums of its fp16 form
+            const size_t n = rows * (1 + static_cast<size_t>(L->split_up_max));
+            L->x_scale = static_cast<float *>(L->dalloc(n * 4, &err));
+            if (err) return cuda_fail(err, "cudaMalloc(token row scales)");
+            L->x_sum = L->x_scale + rows;
+            L->workspace_bytes += n * 4;
+        }
     }
     L->ypart_rows = ypart_rows;
     L->ypart = static_cast<float *>(L->dalloc(ypart_rows * c.m * 4, &err));
@@ -777,9 +784,19 @@ static moe_status_t run_experts_tc(moe_layer_t *L, ExpertArgs &a, const moe_plan
     moe_status_t st = tc_maps(L, N, &xm, &hm);
     if (st == MOE_OK && pair_up) st = tc_maps(L, N / 2, &xm_half, &hm_half);
     if (st != MOE_OK) return st;
-    st = launch_phase(L, MOE_PHASE_GATHER, s, "gather_rows", [&] {
-        return launch_gather_rows(a.x, a.gather, rows, a.k, c.m, L->x_perm, L->err_word, s);
-    });
+    if (i8) {  // fp16 token rows, their scales and split sums (the up projection's MMAs run in fp16)
+        a.x_scale = L->x_scale;
+        a.x_sum = L->x_sum;
+        a.xsum_stride = static_cast<int>(static_cast<size_t>(c.max_tokens) * c.k);
+        st = launch_phase(L, MOE_PHASE_GATHER, s, "gather_rows_f16", [&] {
+            return launch_gather_rows_f16(a.x, a.gather, rows, a.k, c.m, s_up, L->x_perm, L->x_scale, L->x_sum,
+                                          a.xsum_stride, L->err_word, s);
+        });
+    } else {
+        st = launch_phase(L, MOE_PHASE_GATHER, s, "gather_rows", [&] {
+            return launch_gather_rows(a.x, a.gather, rows, a.k, c.m, L->x_perm, L->err_word, s);
+        });
+    }
     if (pair_up) {
         const CUtensorMap *wm = nullptr;
         if (st == MOE_OK) st = weight_map(L, &wm);
