@@ -69,6 +69,9 @@ def parse():
                     help="granularity of the host-to-device page copies, MiB")
     ap.add_argument("--paged-prefetch", type=int, default=0,
                     help="experts each paged layer prefetches for the next layer (0: off)")
+    ap.add_argument("--paged-route-inline", action="store_true",
+                    help="route each paged layer on the compute stream right before its forward "
+                         "(default: a step's routing is issued ahead on a side stream)")
     ap.add_argument("--zipf", type=float, default=None,
                     help="router bias making expert popularity Zipf(s) (batch workloads)")
     ap.add_argument("--shape", default="mixtral", choices=["mixtral", "phi", "small"],
@@ -757,10 +760,28 @@ def run_paged(args, world, rank, local):
     # fresh N(0,1) token rows per (step, layer), drawn before the timed region
     xs = torch.randn((S + 1, L, T, shape.m), generator=gen, device=dev).to(torch.bfloat16)
 
+    # The trace's routing does not depend on the previous layer's output, so
+    # by default a step routes all its layers first on a side stream (after
+    # the previous step's compute, whose tables it overwrites); each paged
+    # forward then reads its counts there and issues its page copies while
+    # the earlier layers still compute.  --paged-route-inline routes each
+    # layer on the compute stream just before its forward, as a model whose
+    # next routing waits for this layer's output would.
+    route_stream = torch.cuda.Stream(device=dev)
+    step_done = torch.cuda.Event()
+
     def step(s):
+        if args.paged_route_inline:
+            for l, ml in enumerate(layers):
+                ml.route_from_topk(ids_d[s, l], w_d[s, l], T=T, stream=stream)
+                ml.forward(xs[s, l], y, stream=stream)
+            return
+        route_stream.wait_event(step_done)
         for l, ml in enumerate(layers):
-            ml.route_from_topk(ids_d[s, l], w_d[s, l], T=T, stream=stream)
+            ml.route_from_topk(ids_d[s, l], w_d[s, l], T=T, stream=route_stream)
+        for l, ml in enumerate(layers):
             ml.forward(xs[s, l], y, stream=stream)
+        step_done.record(stream)
 
     step(0)  # warm-up: kernels, tensor maps, first slot fills
     torch.cuda.synchronize()
@@ -768,12 +789,16 @@ def run_paged(args, world, rank, local):
         ml.set_timing(True)
         ml.timings(reset=True)
     st0 = [ml.stats() for ml in layers]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for s_ in range(1, S + 1):
         step(s_)
     e1.record(stream)
     torch.cuda.synchronize()
+    clk = clocks.stop()
     wall_ms = e0.elapsed_time(e1)
     st1 = [ml.stats() for ml in layers]
     tim = [ml.timings(reset=True) for ml in layers]
@@ -798,6 +823,8 @@ def run_paged(args, world, rank, local):
                                    f"{n_index} sets x {args.paged_ways} ways, "
                                    f"prefetch {args.paged_prefetch}",
                        "layers": L, "T": T, "trace": "p_layer=0.44, p_token=0.5, seeded",
+                       "routing": ("each layer on the compute stream before its forward" if args.paged_route_inline
+                                   else "a step's layers routed ahead on a side stream"),
                        "tokens_per_step": T},
             "paged": {"sets": n_index, "ways": args.paged_ways, "slots": n_slots,
                       "expert_bytes": eb, "hit_rate": hits / max(hits + misses, 1),
@@ -812,7 +839,8 @@ def run_paged(args, world, rank, local):
                       "link_frac": (h2d / max(copy_ms * 1e-3, 1e-12) / 1e9) / link,
                       "copy_ms": copy_ms, "compute_ms": compute_ms, "wall_ms": wall_ms,
                       "overlap_frac": max(0.0, min(1.0, overlap)),
-                      "bounds_ms": [max(copy_ms, compute_ms), copy_ms + compute_ms]}}
+                      "bounds_ms": [max(copy_ms, compute_ms), copy_ms + compute_ms]},
+            "clocks": clk}
     print(json.dumps(line), flush=True)
 
 

@@ -159,8 +159,13 @@ moe_status_t moe_route_from_topk(moe_layer_t *layer, const int32_t *ids, const f
  *   x: device [r->T x m] (the same x that was routed); y: device [r->T x m].
  *   The regime (decode: weight-streaming GEMV; batch: grouped tensor-core
  *   GEMM) is chosen on the host from T alone, so a resident layer never
- *   synchronises the host.  A paged layer copies counts to the host once
- *   (one synchronisation of `stream`) to decide which experts to fetch. */
+ *   synchronises the host.  A paged layer copies counts to the host once to
+ *   decide which experts to fetch, and the host waits for that copy: it runs
+ *   on the stream of the routing call that wrote r (when r comes from this
+ *   layer's last routing call; else on `stream`), and `stream` waits for it
+ *   before any expert kernel.  A caller that knows the routing early can
+ *   route on a side stream ahead of time, so that the wait does not also wait
+ *   for the compute already queued on `stream`. */
 moe_status_t moe_forward(moe_layer_t *layer, const void *x, const moe_routing_t *r,
                          void *y, void *stream);
 

@@ -75,6 +75,12 @@ struct moe_layer {
     // of the last kernel of one call with the first of the next.
     // moe_layer_sync_check records `done` on this stream when it is called.
     cudaStream_t last_stream = nullptr;
+    // The stream and the counts of the last routing call, until a forward call
+    // consumes them: a paged forward reads the token counts on the routing
+    // call's stream, so a caller that routes ahead on a side stream does not
+    // make that read wait for the compute queued on the forward's stream.
+    cudaStream_t route_stream = nullptr;
+    const int32_t *route_counts = nullptr;
     bool launched = false;
     cudaStream_t ingest_stream = nullptr;
     std::vector<void *> allocations;

@@ -486,6 +486,8 @@ static moe_status_t run_permute(moe_layer_t *L, int T, moe_routing_t *r, cudaStr
     moe_status_t st = launch_phase(L, MOE_PHASE_PERMUTE, s, "permute", [&] { return launch_permute(pa, s); });
     if (st != MOE_OK) return st;
     L->last_stream = s;
+    L->route_stream = s;
+    L->route_counts = r->counts;
     L->launched = true;
     r->T = T;
     return MOE_OK;
@@ -515,6 +517,8 @@ extern "C" moe_status_t moe_route(moe_layer_t *L, const void *x, int T, moe_rout
                       [&] { return launch_router_topk(ra, pa, L->cfg.act_dtype == MOE_BF16, s); });
     if (st != MOE_OK) return st;
     L->last_stream = s;
+    L->route_stream = s;
+    L->route_counts = r->counts;
     L->launched = true;
     r->T = T;
     return MOE_OK;

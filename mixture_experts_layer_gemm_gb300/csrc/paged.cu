@@ -5,7 +5,10 @@
 // expert replaced inside a set).  Each paged layer keeps its experts (in the
 // stored, packed layout) in pinned host memory; a forward pass
 //   1. copies the per-expert token counts to the host (the one host
-//      synchronisation of the call),
+//      synchronisation of the call), on the stream of the routing call that
+//      wrote them, so that routing issued ahead on a side stream lets the
+//      host look up and issue this layer's copies while earlier layers still
+//      compute,
 //   2. for each expert with tokens, in ascending id: looks it up in the set;
 //      on a miss, picks a free or the least recently used way, makes the copy
 //      stream wait until the compute that last read that slot has finished,
@@ -353,12 +356,21 @@ moe_status_t paged_forward(moe_layer *L, const void *x, const moe_routing_t *r, 
         L->fwd_pending = false;
     }
     PG_TRY(cudaEventRecord(L->fwd_t0, s));
-    PG_TRY(cudaMemcpyAsync(L->counts_host, r->counts, sizeof(int32_t) * c.E, cudaMemcpyDeviceToHost, s));
-    PG_TRY(cudaEventRecord(L->counts_ready, s));
+    // The counts are read on the stream of the routing call that wrote them
+    // (when these tables come from this layer's last routing call), so a
+    // caller that routes ahead on a side stream gets them without waiting for
+    // the compute queued on `s`, and the copy stream is fed without a gap;
+    // `s` then waits for that read before any expert reads the tables.
+    cudaStream_t rs = (L->route_stream && L->route_counts == r->counts) ? L->route_stream : s;
+    L->route_stream = nullptr;
+    L->route_counts = nullptr;
+    PG_TRY(cudaMemcpyAsync(L->counts_host, r->counts, sizeof(int32_t) * c.E, cudaMemcpyDeviceToHost, rs));
+    PG_TRY(cudaEventRecord(L->counts_ready, rs));
     {
         moe_status_t w = wait_event(L->counts_ready, L->host_timeout_ms, "the token counts");
         if (w != MOE_OK) return w;  // no slot state changed yet
     }
+    if (rs != s) PG_TRY(cudaStreamWaitEvent(s, L->counts_ready, 0));
 
     // the launch plan of a resident layer for the same T (bit-identical results)
     ExpertArgs a = make_expert_args(L, x, r);

@@ -158,6 +158,44 @@ def test_paged_step_time_within_overlap_bounds():
     moe.moe_pool_destroy(pool)
 
 
+def test_routing_ahead_on_a_side_stream():
+    """A step routes all its paged layers first on a side stream and then runs
+    their forward calls on the compute stream: each paged call reads its token
+    counts on the routing stream and the compute stream waits for that read.
+    Outputs equal resident layers' bit for bit and the lookups equal the
+    oracle's LRU replay."""
+    sets, ways, n_layers, T = 2, 2, 4, 8
+    eb = _expert_bytes(SHAPE)
+    pool = moe.moe_pool_create(eb * sets * ways, eb, ways, 0)
+    layers = [wl.make_layer(SHAPE, seed=600 + i) for i in range(n_layers)]
+    paged = [moe.MoELayer(layers[i], T, pool=pool, layer_id=i) for i in range(n_layers)]
+    resident = [moe.MoELayer(layers[i], T) for i in range(n_layers)]
+    side, main = torch.cuda.Stream(), torch.cuda.current_stream()
+    queries = []
+    for step in range(3):
+        xs = [to_device(wl.make_tokens(SHAPE, T, seed=700 + 10 * step + i)) for i in range(n_layers)]
+        ys = [torch.empty((T, SHAPE.m), dtype=torch.bfloat16, device="cuda") for _ in range(n_layers)]
+        side.wait_stream(main)  # inputs written, earlier forwards done with the tables
+        for ml, x in zip(paged, xs):
+            ml.route(x, stream=side)
+        for ml, x, y in zip(paged, xs, ys):
+            ml.forward(x, y, stream=main)
+        torch.cuda.synchronize()
+        for i, (ml, x, y) in enumerate(zip(paged, xs, ys)):
+            assert ml.sync_check()[0] == moe.MOE_OK
+            counts = ml.counts.cpu().numpy()
+            queries += [(i, e) for e in range(SHAPE.E) if counts[e] > 0]
+            yr = torch.empty_like(y)
+            resident[i].route(x)
+            resident[i].forward(x, yr)
+            torch.cuda.synchronize()
+            assert torch.equal(y.view(torch.int16), yr.view(torch.int16)), (step, i)
+    _check_log(queries, moe.moe_pool_query_log(pool), sets, ways)
+    for ml in paged + resident:
+        ml.close()
+    moe.moe_pool_destroy(pool)
+
+
 def _check_calls(schedule, counts, log, sets, ways, n_layers, prefetch, stats):
     lay, exp_, kind, slot = oracle.cache_replay_calls(sets, ways, [li for li, _ in schedule],
                                                       np.array(counts), n_layers, prefetch)
