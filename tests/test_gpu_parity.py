@@ -315,7 +315,8 @@ def test_int8_decode(T):
 
 @pytest.mark.parametrize("T", [1, 37, 200, 700])
 def test_int8_tensor_core(T):
-    """int8 codes widened to bf16 in tensor memory, row scale in the epilogue."""
+    """int8 codes widened in tensor memory (fp16 against fp16 token rows in the up
+    projection, bf16 in the down projection), scales in the epilogue."""
     run_and_check(I8, T, seed=16, regime=moe.REGIME_BATCH)
 
 
@@ -342,6 +343,33 @@ def test_int8_tensor_core_and_decode_paths_agree():
         ml.close()
     rel = np.linalg.norm(ys[0] - ys[1], axis=1) / np.linalg.norm(ys[1], axis=1)
     assert rel.max() <= 1e-2
+
+
+@pytest.mark.parametrize("regime,T", [(moe.REGIME_DECODE, 12), (moe.REGIME_BATCH, 12),
+                                       (moe.REGIME_BATCH, 200)])
+def test_int8_token_rows_of_extreme_magnitude(regime, T):
+    """The int8 paths run MMAs in fp16 on token rows (and, in the GEMV, hidden
+    rows) under a power-of-two scale per row.  Rows near 2^16 times N(0,1)
+    would overflow fp16 unscaled and rows near 2^-20 times N(0,1) would fall
+    into its subnormals; every third row is one of each, so a missing or wrong
+    row scale fails here while ordinary N(0,1) rows could not show it."""
+    layer = get_layer(I8, seed=21)
+    xf = wl.bf16_bits_to_f32(wl.make_tokens(I8, T, seed=22))
+    mag = np.where(np.arange(T) % 3 == 0, 2.0 ** 16, np.where(np.arange(T) % 3 == 1, 2.0 ** -20, 1.0))
+    x = wl.f32_to_bf16_bits(xf * mag[:, None].astype(np.float32))  # exact: powers of two
+    rng = np.random.default_rng(23)
+    ids = np.stack([rng.choice(I8.E, 2, replace=False) for _ in range(T)]).astype(np.int32)
+    w = np.tile(np.array([0.625, 0.375], np.float32), (T, 1))
+    ml = moe.MoELayer(layer, T)
+    ml.set_regime(regime)
+    run = Run(ml, x, routing="topk", ids=ids, w=w)
+    assert ml.sync_check()[0] == moe.MOE_OK
+    assert np.isfinite(f64(run.y_np)).all()
+    w64 = w.astype(np.float64)
+    rel, _ = max_token_rel_l2(run.y_np, oracle_y(layer, x, ids, w64))
+    rel_q, _ = max_token_rel_l2(run.y_np, oracle_y(layer, x, ids, w64, oracle_quantized(layer)))
+    assert rel_q <= 1e-2 and rel <= TOL["i8"], (rel_q, rel)
+    ml.close()
 
 
 # ---- edge cases ------------------------------------------------------------------------
