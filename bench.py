@@ -28,6 +28,7 @@ import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
+T_START = time.perf_counter()
 sys.path.insert(0, ROOT)
 
 TOKENS = (1, 4, 16, 64)
@@ -653,7 +654,8 @@ def run_ours(args, world, rank, local):
     # The metric's other halves, measured in the same run on the same layer
     # weights: the int8 repeat of the decode step, and the batch regime
     # (T = 512, 2048, 8192 with a Zipf(1.2) router bias), whose expert GEMMs
-    # are tensor-bound.  Each is its own timed region with its own clocks.
+    # are tensor-bound; then the Phi-3.5-MoE-shaped layer.  Each is its own
+    # timed region with its own clocks.
     subs = {}
     if headline_default and not args.no_sub:
         lay_i8 = dataclasses.replace(layer, shape=shape.with_weight("i8"))
@@ -665,6 +667,14 @@ def run_ours(args, world, rank, local):
         xb = make_tokens_for(zshape, bt, args.seed + rank, device)
         subs["batch"] = measure(args, world, local, zshape, lay_b, bt, xb, max(args.steps, 40),
                                 args.warmup, "bf16")
+        # the Phi-3.5-MoE-shaped layer (16 smaller experts), uniform routing,
+        # over the batch sizes of its configuration, decode to batch
+        pshape = wl.PHI35
+        lay_p = wl.make_layer(pshape, seed=args.seed + rank, device=device)
+        pt = wl.PHI_TOKENS
+        xp = make_tokens_for(pshape, pt, args.seed + rank, device)
+        subs["phi"] = measure(args, world, local, pshape, lay_p, pt, xp, max(args.steps, 40),
+                              args.warmup, "bf16")
 
     if rank == 0:
         line = {"metric": METRIC, "value": rec["value"], "unit": "tokens/s", "n_gpus": world,
@@ -688,6 +698,7 @@ def run_ours(args, world, rank, local):
         for name, sub in subs.items():
             sub["dtype"] = "i8->f16/bf16" if name == "int8_decode" else "bf16"
             line[name] = sub
+        line["wall_s"] = time.perf_counter() - T_START
         print(json.dumps(line), flush=True)
 
 

@@ -147,6 +147,30 @@ def destinations(ids_local: np.ndarray, rank: int, plan: RebalancePlan) -> np.nd
     return dest
 
 
+def library_compute(layer_k1, device="cuda"):
+    """ep_forward's compute through this library: the received pairs are
+    routed as a batch of one-slot tokens (route_from_topk with their expert
+    ids and routing weights) on a layer holding the same experts with k = 1,
+    whose forward pass returns weight * expert(row) for each.  Returns fp32
+    host rows (the layer's output type widened)."""
+    import torch
+
+    def compute(rows, experts, weights):
+        n = int(rows.shape[0])
+        if n == 0:
+            return torch.zeros((0, layer_k1.shape.m), dtype=torch.float32)
+        x = rows.to(device).contiguous()
+        ids = experts.to(torch.int32).to(device)
+        w = weights.to(torch.float32).to(device)
+        layer_k1.route_from_topk(ids, w, T=n)
+        y = torch.empty_like(x)
+        layer_k1.forward(x, y)
+        torch.cuda.synchronize(device)
+        return y.float().cpu()
+
+    return compute
+
+
 def ep_forward(x_local, ids_local, w_local, E: int, q: float, compute: Callable, group=None):
     """The six steps of the HARMOEny write-up (三 3.3) on one rank.
 
