@@ -772,14 +772,15 @@ def run_paged(args, world, rank, local):
     xs = torch.randn((S + 1, L, T, shape.m), generator=gen, device=dev).to(torch.bfloat16)
 
     # The trace's routing does not depend on the previous layer's output, so
-    # by default a step routes all its layers first on a side stream (after
-    # the previous step's compute, whose tables it overwrites); each paged
-    # forward then reads its counts there and issues its page copies while
-    # the earlier layers still compute.  --paged-route-inline routes each
-    # layer on the compute stream just before its forward, as a model whose
-    # next routing waits for this layer's output would.
+    # by default a step routes all its layers first on a side stream, each
+    # layer's routing after that layer's previous forward (which read the
+    # tables it overwrites); each paged forward then reads its counts there and
+    # issues its page copies while the earlier layers still compute.
+    # --paged-route-inline routes each layer on the compute stream just before
+    # its forward, as a model whose next routing waits for this layer's output
+    # would.
     route_stream = torch.cuda.Stream(device=dev)
-    step_done = torch.cuda.Event()
+    layer_done = [torch.cuda.Event() for _ in layers]
 
     def step(s):
         if args.paged_route_inline:
@@ -787,12 +788,12 @@ def run_paged(args, world, rank, local):
                 ml.route_from_topk(ids_d[s, l], w_d[s, l], T=T, stream=stream)
                 ml.forward(xs[s, l], y, stream=stream)
             return
-        route_stream.wait_event(step_done)
         for l, ml in enumerate(layers):
+            route_stream.wait_event(layer_done[l])
             ml.route_from_topk(ids_d[s, l], w_d[s, l], T=T, stream=route_stream)
         for l, ml in enumerate(layers):
             ml.forward(xs[s, l], y, stream=stream)
-        step_done.record(stream)
+            layer_done[l].record(stream)
 
     step(0)  # warm-up: kernels, tensor maps, first slot fills
     torch.cuda.synchronize()
