@@ -4,7 +4,9 @@
 // their owner).  The routing weight was applied in the down-projection
 // epilogue; a split-K down projection leaves `splits` partial rows, added
 // here first (in a fixed order over the splits), then the k slots (in
-// ascending j), in fp32, rounded once to the activation type.
+// ascending j), in fp32, rounded once to the activation type.  In the batch
+// regime the partial rows arrive rounded to bf16 (half the bytes to write and
+// read; one more rounding, which the tolerance of bf16 layers covers).
 // Deterministic: no atomics.
 //
 // The kernel is bound by HBM (the partial rows are read once): each thread
@@ -19,25 +21,47 @@ namespace moe {
 
 namespace {
 
-// W consecutive fp32 values of one partial row, loaded with 16-byte loads
-// that bypass L1 (each partial row is read once).
-template <int W>
+// W consecutive values of one partial row -- fp32, or bf16 (PB) where the batch
+// regime's down projection rounded its rows -- widened to fp32, loaded with
+// vector loads that bypass L1 (each partial row is read once).  `base` is the
+// partial buffer, `off` the element offset of the first value.
+template <int W, bool PB>
 struct Vec {
     float v[W];
-    __device__ __forceinline__ void load(const float *p) {
+    __device__ __forceinline__ void load(const void *base, size_t off) {
+        if constexpr (PB) {
+            const uint16_t *p = static_cast<const uint16_t *>(base) + off;
+            if constexpr (W == 8) {
+                const uint4 q = __ldcg(reinterpret_cast<const uint4 *>(p));
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int i = 0; i < W; i += 4) {
-            const float4 q = __ldcg(reinterpret_cast<const float4 *>(p + i));
-            v[i] = q.x;
-            v[i + 1] = q.y;
-            v[i + 2] = q.z;
-            v[i + 3] = q.w;
+                for (int i = 0; i < 4; ++i) {
+                    v[2 * i] = bf16lo(w[i]);
+                    v[2 * i + 1] = bf16hi(w[i]);
+                }
+            } else {
+                const uint2 q = __ldcg(reinterpret_cast<const uint2 *>(p));
+                v[0] = bf16lo(q.x);
+                v[1] = bf16hi(q.x);
+                v[2] = bf16lo(q.y);
+                v[3] = bf16hi(q.y);
+            }
+        } else {
+            const float *p = static_cast<const float *>(base) + off;
+#pragma unroll
+            for (int i = 0; i < W; i += 4) {
+                const float4 q = __ldcg(reinterpret_cast<const float4 *>(p + i));
+                v[i] = q.x;
+                v[i + 1] = q.y;
+                v[i + 2] = q.z;
+                v[i + 3] = q.w;
+            }
         }
     }
 };
 
 // W outputs per thread (4 or 8 consecutive features of one token); KMAX >= k.
-template <bool BF16, int KMAX, int W>
+template <bool BF16, int KMAX, int W, bool PB>
 __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
     pdl_wait();
     pdl_trigger();
@@ -63,12 +87,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 #pragma unroll
         for (int e = 0; e < W; ++e) y[e] = 0.0f;
         if (a.splits == 1) {
-            Vec<W> q[KMAX];
+            Vec<W, PB> q[KMAX];
 #pragma unroll
             for (int j = 0; j < KMAX; ++j) {
 #pragma unroll
                 for (int e = 0; e < W; ++e) q[j].v[e] = 0.0f;
-                if (pos[j] >= 0) q[j].load(a.ypart + static_cast<size_t>(pos[j]) * a.m + c);
+                if (pos[j] >= 0) q[j].load(a.ypart, static_cast<size_t>(pos[j]) * a.m + c);
             }
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
@@ -82,23 +106,23 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
                 // partial rows of the split reduction, four loads in flight at
                 // a time, added in a fixed order: ((p0 + p1) + (p2 + p3)) per
                 // group, groups in split order
-                const float *base = a.ypart + static_cast<size_t>(pos[j]) * a.m + c;
+                const size_t base = static_cast<size_t>(pos[j]) * a.m + c;
                 float v[W];
 #pragma unroll
                 for (int e = 0; e < W; ++e) v[e] = 0.0f;
                 int s = 0;
                 for (; s + 4 <= a.splits; s += 4) {
-                    Vec<W> p0, p1, p2, p3;
-                    p0.load(base + (s + 0) * a.split_stride);
-                    p1.load(base + (s + 1) * a.split_stride);
-                    p2.load(base + (s + 2) * a.split_stride);
-                    p3.load(base + (s + 3) * a.split_stride);
+                    Vec<W, PB> p0, p1, p2, p3;
+                    p0.load(a.ypart, base + (s + 0) * a.split_stride);
+                    p1.load(a.ypart, base + (s + 1) * a.split_stride);
+                    p2.load(a.ypart, base + (s + 2) * a.split_stride);
+                    p3.load(a.ypart, base + (s + 3) * a.split_stride);
 #pragma unroll
                     for (int e = 0; e < W; ++e) v[e] += (p0.v[e] + p1.v[e]) + (p2.v[e] + p3.v[e]);
                 }
                 for (; s < a.splits; ++s) {
-                    Vec<W> p;
-                    p.load(base + s * a.split_stride);
+                    Vec<W, PB> p;
+                    p.load(a.ypart, base + s * a.split_stride);
 #pragma unroll
                     for (int e = 0; e < W; ++e) v[e] += p.v[e];
                 }
@@ -124,20 +148,22 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
     }
 }
 
-template <bool BF16, int KMAX>
+template <bool BF16, int KMAX, bool PB>
 cudaError_t launch_w(const CombineArgs &a, cudaStream_t s) {
     const int w = (a.m % 8 == 0) ? 8 : 4;
     const long long n = static_cast<long long>(a.T) * (a.m / w);
     long long blocks = (n + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
     const dim3 grid(static_cast<unsigned>(blocks));
-    return w == 8 ? launch_pdl(combine_kernel<BF16, KMAX, 8>, grid, dim3(256), 0, s, a)
-                  : launch_pdl(combine_kernel<BF16, KMAX, 4>, grid, dim3(256), 0, s, a);
+    return w == 8 ? launch_pdl(combine_kernel<BF16, KMAX, 8, PB>, grid, dim3(256), 0, s, a)
+                  : launch_pdl(combine_kernel<BF16, KMAX, 4, PB>, grid, dim3(256), 0, s, a);
 }
 
 template <bool BF16>
 cudaError_t launch_k(const CombineArgs &a, cudaStream_t s) {
-    return a.k <= 2 ? launch_w<BF16, 2>(a, s) : launch_w<BF16, kMaxTopK>(a, s);
+    if (a.part_bf16)
+        return a.k <= 2 ? launch_w<BF16, 2, true>(a, s) : launch_w<BF16, kMaxTopK, true>(a, s);
+    return a.k <= 2 ? launch_w<BF16, 2, false>(a, s) : launch_w<BF16, kMaxTopK, false>(a, s);
 }
 
 }  // namespace

@@ -345,8 +345,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int tok = tok0 + c0 + j;
                         if (tok < t.q) {
                             const int pos = t.off + tok;
-                            a.ypart[(static_cast<size_t>(t.ks) * a.n_rows_cap + pos) * a.m + R] =
-                                s_w[lq][c0 + j] * (__uint_as_float(v[j]) * scale);
+                            const size_t o = (static_cast<size_t>(t.ks) * a.n_rows_cap + pos) * a.m + R;
+                            const float yv = s_w[lq][c0 + j] * (__uint_as_float(v[j]) * scale);
+                            if (a.ypart_bf16)
+                                reinterpret_cast<__nv_bfloat16 *>(a.ypart)[o] = __float2bfloat16_rn(yv);
+                            else
+                                a.ypart[o] = yv;
                         }
                     }
                 }

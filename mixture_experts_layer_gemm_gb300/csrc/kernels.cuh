@@ -84,7 +84,8 @@ struct ExpertArgs {
     const float *topk_w;         // [T*k]
     int T, k, E, m, p;
     void *h;                     // [T*k x p] act type (permuted order)
-    float *ypart;                // [splits x T*k x m] fp32 (permuted order)
+    float *ypart;                // [splits x T*k x m] fp32 (permuted order); bf16 where ypart_bf16
+    int ypart_bf16;              // batch regime: the down projection writes its rows rounded to bf16
     int n_rows_cap;              // T*k capacity of one ypart split
     float *gate_part;            // [splits_up x T*k x p] fp32 (decode split-K up only)
     float *up_part;              // same
@@ -151,14 +152,17 @@ cudaError_t launch_simt_up(const ExpertArgs &a, bool gated, cudaStream_t s);
 cudaError_t launch_simt_down(const ExpertArgs &a, cudaStream_t s);
 
 // Combine: y[t] = sum_j sum_s ypart[s][scatter[t*k+j]] in fp32, rounded once.
+// The partial rows are fp32, or bf16 where the batch regime's down projection
+// wrote them rounded (part_bf16).
 struct CombineArgs {
-    const float *ypart;
+    const void *ypart;
     int splits;
     size_t split_stride;         // elements between splits
     const int32_t *scatter;
     int T, k, m;
     void *y;
     uint32_t *err;
+    bool part_bf16;
 };
 cudaError_t launch_combine(const CombineArgs &a, bool act_bf16, cudaStream_t s);
 

@@ -100,7 +100,7 @@ moe_status_t wait_event(cudaEvent_t ev, int timeout_ms, const char *what);
 
 ExpertArgs make_expert_args(moe_layer *L, const void *x, const moe_routing_t *r);
 moe_status_t run_experts(moe_layer *L, ExpertArgs &a, int regime, int *splits_out, cudaStream_t s);
-moe_status_t run_combine(moe_layer *L, const moe_routing_t *r, int splits, int n_rows_cap, void *y,
+moe_status_t run_combine(moe_layer *L, const moe_routing_t *r, int splits, int n_rows_cap, bool part_bf16, void *y,
                          cudaStream_t s);
 
 // Workspace a layer of configuration c allocates at create time, and to which

@@ -784,6 +784,10 @@ static moe_status_t run_experts_tc(moe_layer_t *L, ExpertArgs &a, const moe_plan
     const int s_up = plan.splits_up, s_down = plan.splits_down;
     const bool pair_up = plan.pair_up != 0;
     a.n_rows_cap = static_cast<size_t>(rows) <= L->decode_rows_cap ? static_cast<int>(L->decode_rows_cap) : rows;
+    // batch regime (more rows than the decode cap): the down projection's
+    // output rows go to the combine rounded to bf16, halving their write and
+    // read; decode-sized calls keep fp32 partial sums
+    a.ypart_bf16 = (c.act_dtype == MOE_BF16 && static_cast<size_t>(rows) > L->decode_rows_cap) ? 1 : 0;
     const CUtensorMap *xm = nullptr, *hm = nullptr, *xm_half = nullptr, *hm_half = nullptr;
     moe_status_t st = tc_maps(L, N, &xm, &hm);
     if (st == MOE_OK && pair_up) st = tc_maps(L, N / 2, &xm_half, &hm_half);
@@ -870,9 +874,9 @@ moe_status_t run_experts(moe_layer_t *L, ExpertArgs &a, int regime, int *splits_
 }
 
 moe_status_t run_combine(moe_layer_t *L, const moe_routing_t *r, int splits, int n_rows_cap,
-                         void *y, cudaStream_t s) {
+                         bool part_bf16, void *y, cudaStream_t s) {
     CombineArgs ca{L->ypart, splits, static_cast<size_t>(n_rows_cap) * L->cfg.m, r->scatter_index,
-                   r->T, L->cfg.k, L->cfg.m, y, L->err_word};
+                   r->T, L->cfg.k, L->cfg.m, y, L->err_word, part_bf16};
     return launch_phase(L, MOE_PHASE_COMBINE, s, "combine",
                         [&] { return launch_combine(ca, L->cfg.act_dtype == MOE_BF16, s); });
 }
@@ -896,7 +900,7 @@ extern "C" moe_status_t moe_forward(moe_layer_t *L, const void *x, const moe_rou
     int splits = 1;
     st = run_experts(L, a, L->regime, &splits, s);
     if (st != MOE_OK) return st;
-    st = run_combine(L, r, splits, a.n_rows_cap, y, s);
+    st = run_combine(L, r, splits, a.n_rows_cap, a.ypart_bf16 != 0, y, s);
     if (st != MOE_OK) return st;
     L->last_stream = s;
     L->launched = true;

@@ -133,7 +133,7 @@ extern "C" moe_status_t moe_forward_static_scratch(moe_layer_t *L, const void *x
                           [&] { return launch_decode_down(a, wt, s_down, L->num_sms, s); });
     if (st != MOE_OK) return st;
     CombineArgs ca{a.ypart, s_down, static_cast<size_t>(rows) * c.m, r->scatter_index, r->T, c.k, c.m,
-                   y, L->err_word};
+                   y, L->err_word, false};
     st = launch_phase(L, MOE_PHASE_COMBINE, s, "combine",
                       [&] { return launch_combine(ca, true, s); });
     if (st != MOE_OK) return st;

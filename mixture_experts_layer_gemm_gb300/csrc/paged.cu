@@ -375,6 +375,7 @@ moe_status_t paged_forward(moe_layer *L, const void *x, const moe_routing_t *r, 
     // the launch plan of a resident layer for the same T (bit-identical results)
     ExpertArgs a = make_expert_args(L, x, r);
     int splits = 1, nrows_cap = 0;
+    bool part_bf16 = false;
     moe_status_t st = MOE_OK;
     bool first = true;
     for (int e = 0; e < c.E; ++e) {
@@ -416,13 +417,14 @@ moe_status_t paged_forward(moe_layer *L, const void *x, const moe_routing_t *r, 
         if (first) {
             splits = sp;
             nrows_cap = a.n_rows_cap;
+            part_bf16 = a.ypart_bf16 != 0;
             first = false;
         }
         PG_TRY(cudaEventRecord(slot.busy, s));
         slot.busy_recorded = true;
     }
     if (!first) {
-        st = run_combine(L, r, splits, nrows_cap, y, s);
+        st = run_combine(L, r, splits, nrows_cap, part_bf16, y, s);
         if (st != MOE_OK) return st;
     }
     st = pool_prefetch_next(P, L, L->counts_host, c.E);
