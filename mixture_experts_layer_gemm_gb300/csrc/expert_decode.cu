@@ -85,51 +85,94 @@ struct DecodeGeom {
     int bstage_bytes;
 };
 
+// n * ks < 2^31: n <= K / 64 reduction blocks, ks <= 16 splits
 __device__ __forceinline__ int split_begin(int n, int splits, int ks) {
-    return static_cast<int>((static_cast<long long>(n) * ks) / splits);
+    return static_cast<int>(static_cast<unsigned>(n * ks) / static_cast<unsigned>(splits));
 }
 
-// int8 weights: convert the staged bf16 token rows to fp16 in place, one warp
-// per row.  The row's largest magnitude sets a power-of-two scale 2^-s that
-// puts it in [2^14, 2^15): every bf16 value whose scaled magnitude is at least
+// int8 weights: convert the staged bf16 token rows 0 .. nrows-1 to fp16 in
+// place.  The row's largest magnitude sets a power-of-two scale 2^-s that puts
+// it in [2^14, 2^15): every bf16 value whose scaled magnitude is at least
 // 2^-14 is then an exact fp16 value (only values below the row maximum by a
 // factor of 2^28 or more round).  Records 2^s and the sum of the converted
-// values (fixed order) for the epilogue.  A row of zeros, or one holding an
-// infinity or NaN, keeps scale 1.
-template <int kTok>
-__device__ __forceinline__ void stage_rows_f16(uint8_t *bstage, int row_bytes, int vec_per_row, int warp,
-                                               int lane, float *s_xscale, float *s_xsum) {
-    for (int r = warp; r < kTok; r += kConsumerWarps) {
-        uint4 *row = reinterpret_cast<uint4 *>(bstage + static_cast<size_t>(r) * row_bytes);
-        float mx = 0.0f;
-        for (int v = lane; v < vec_per_row; v += 32) {
-            const uint4 q = row[v];
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+// values for the epilogue.  A row of zeros, or one holding an infinity or NaN,
+// keeps scale 1.
+//
+// A pass of a few rows (one or two at the smallest batches) is latency-bound:
+// each row goes to wpr warps, the largest power of two with nrows * wpr <= 8
+// (1 from five rows on), whose partial maxima and sums meet in s_red / s_red2
+// and are combined in warp order, so the sums are deterministic.
+// Rows past nrows are not touched: their MMA columns belong to no token.
+__device__ __forceinline__ void stage_rows_f16(uint8_t *bstage, int row_bytes, int vec_per_row, int nrows,
+                                               int warp, int lane, float *s_red, float *s_red2, float *s_xscale,
+                                               float *s_xsum) {
+    const int wpr = nrows >= 5 ? 1 : (nrows >= 3 ? 2 : (nrows == 2 ? 4 : 8));  // nrows * wpr <= 8 below 8 rows
+    const int ngroups = kConsumerWarps / wpr;
+    const int grp = warp / wpr, sub = warp % wpr;
+    const int j0 = sub * 32 + lane, stride = wpr * 32;
+    for (int r = grp; r < nrows; r += ngroups) {
+        const uint4 *row = reinterpret_cast<const uint4 *>(bstage + static_cast<size_t>(r) * row_bytes);
+        float m0 = 0.0f, m1 = 0.0f;
+        int v = j0;
+        for (; v + stride < vec_per_row; v += 2 * stride) {
+            const uint4 q0 = row[v], q1 = row[v + stride];
+            const uint32_t w0[4] = {q0.x, q0.y, q0.z, q0.w}, w1[4] = {q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fmaxf(fabsf(bf16lo(w[i])), fabsf(bf16hi(w[i]))));
+            for (int i = 0; i < 4; ++i) {
+                m0 = fmaxf(m0, fmaxf(fabsf(bf16lo(w0[i])), fabsf(bf16hi(w0[i]))));
+                m1 = fmaxf(m1, fmaxf(fabsf(bf16lo(w1[i])), fabsf(bf16hi(w1[i]))));
+            }
         }
+        if (v < vec_per_row) {
+            const uint4 q0 = row[v];
+            const uint32_t w0[4] = {q0.x, q0.y, q0.z, q0.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) m0 = fmaxf(m0, fmaxf(fabsf(bf16lo(w0[i])), fabsf(bf16hi(w0[i]))));
+        }
+        float mx = fmaxf(m0, m1);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) s_red[r * wpr + sub] = mx;
+    }
+    if (wpr > 1)
+        named_sync(kBarConsumers, kConsumers);
+    else
+        __syncwarp();
+    for (int r = grp; r < nrows; r += ngroups) {
+        float mx = s_red[r * wpr];
+        for (int w = 1; w < wpr; ++w) mx = fmaxf(mx, s_red[r * wpr + w]);
         const int sh = f16_row_shift(mx);
         const float down = pow2f(-sh);
-        float sum = 0.0f;
-        for (int v = lane; v < vec_per_row; v += 32) {
+        uint4 *row = reinterpret_cast<uint4 *>(bstage + static_cast<size_t>(r) * row_bytes);
+        float s0 = 0.0f, s1 = 0.0f;
+        for (int v = j0; v < vec_per_row; v += stride) {
             const uint4 q = row[v];
             uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const __half2 hv = __floats2half2_rn(bf16lo(w[i]) * down, bf16hi(w[i]) * down);
-                sum += __low2float(hv) + __high2float(hv);
+                s0 += __low2float(hv);
+                s1 += __high2float(hv);
                 w[i] = *reinterpret_cast<const uint32_t *>(&hv);
             }
             row[v] = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        sum = warp_sum(sum);
+        const float sum = warp_sum(s0 + s1);
         if (lane == 0) {
-            s_xscale[r] = pow2f(sh);
-            s_xsum[r] = sum;
+            s_red2[r * wpr + sub] = sum;
+            if (sub == 0) s_xscale[r] = pow2f(sh);
         }
     }
+    if (wpr > 1)
+        named_sync(kBarConsumers, kConsumers);
+    else
+        __syncwarp();
+    if (sub == 0 && lane == 0)
+        for (int r = grp; r < nrows; r += ngroups) {
+            float sum = s_red2[r * wpr];
+            for (int w = 1; w < wpr; ++w) sum += s_red2[r * wpr + w];
+            s_xsum[r] = sum;
+        }
 }
 
 // Work entries are (expert, token pass) pairs: an expert with more tokens
@@ -144,17 +187,23 @@ struct Unit {
     bool ok;
 };
 
-__device__ __forceinline__ Unit decode_unit(long long u, const int *s_act, const int *s_tp, const DecodeGeom &geo,
-                                            const ExpertArgs &a, int rows_total) {
+// Unit indices are 32-bit (the launcher checks the count fits): this runs on
+// the path to each CTA's first weight copy, where 64-bit divisions (a software
+// sequence each) cost about a microsecond.
+__device__ __forceinline__ Unit decode_unit(unsigned u, const int *s_act, const int *s_tp, const int *s_off,
+                                            const int *s_end, const DecodeGeom &geo, int rows_total) {
     Unit U;
-    U.g8 = static_cast<int>(u % geo.rg8);
-    U.ks = static_cast<int>((u / geo.rg8) % geo.splits);
-    const int entry = static_cast<int>(u / (static_cast<long long>(geo.rg8) * geo.splits));
+    const unsigned rg8 = static_cast<unsigned>(geo.rg8), sp = static_cast<unsigned>(geo.splits);
+    const unsigned q = u / rg8;
+    U.g8 = static_cast<int>(u - q * rg8);
+    const unsigned entry_u = q / sp;
+    U.ks = static_cast<int>(q - entry_u * sp);
+    const int entry = static_cast<int>(entry_u);
     U.e = s_act[entry];
     U.tp = s_tp[entry];
     U.nrg = min(8, geo.rg - 8 * U.g8);
-    U.off = a.offsets[U.e];
-    U.end = a.offsets[U.e + 1];
+    U.off = s_off[entry];
+    U.end = s_end[entry];
     U.ok = !(U.off < 0 || U.end > rows_total || U.end < U.off);
     U.kb0 = split_begin(geo.nkb, geo.splits, U.ks);
     U.kb1 = split_begin(geo.nkb, geo.splits, U.ks + 1);
@@ -170,9 +219,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
     __shared__ uint64_t rows_bar;  // token rows of the current (expert, split, pass) staged
     __shared__ int s_act[kMaxPassEntries], s_tp[kMaxPassEntries];  // (expert, pass) entries
+    __shared__ int s_off[kMaxPassEntries], s_end[kMaxPassEntries];  // the entry's expert segment
     __shared__ int s_nact;
     __shared__ volatile int s_abort;
     __shared__ float s_xscale[kTok], s_xsum[kTok];  // int8: per staged row, 2^s and sum of x 2^-s
+    __shared__ float s_red[kTok], s_red2[kTok];       // int8: per-warp partial maxima and sums
 
     uint8_t *ring = smem;
     uint8_t *bstage = smem + kStages * kStageBytes;
@@ -181,6 +232,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rows_total = a.T * a.k;
+    // The producer's weight pointers, copied from the launch parameters into
+    // shared memory before anything waits: parameters are not written by the
+    // predecessor, and their first reads in a CTA are slow (measured: the
+    // CTA's first weight copy about a microsecond earlier).
+    __shared__ const void *s_wptr[kExpertTableMax];
+    if (warp == kConsumerWarps)
+        for (int e = lane; e < kExpertTableMax; e += 32) s_wptr[e] = PHASE == kUp ? tab.w1[e] : tab.w2[e];
     // The up projection reads the routing its predecessor (the router) wrote.
     // The down projection's predecessor is the up projection: the routing is
     // two launches back and complete, so the weight stream starts at once and
@@ -193,17 +251,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // One warp lists the (expert, token pass) entries: lane l takes the
         // candidate experts l, l + 32 (all experts, or those of a.only, in
-        // order), so their offsets are read in one round trip.  A malformed
-        // segment keeps one entry, whose unit then reports it.
+        // order), so their offsets are read in one round trip; each entry
+        // keeps its expert's segment, so the producer and the consumers find
+        // it in shared memory instead of another global read before their
+        // first copy.  A malformed segment keeps one entry, whose unit then
+        // reports it.
         const bool only = a.n_only > 0;
         const int ncand = only ? min(a.n_only, kMaxExperts) : a.E;
         int n = 0;
         for (int c0 = 0; c0 < ncand; c0 += 32) {
             const int ci = c0 + lane;
-            int e = -1, np = 0;
+            int e = -1, np = 0, off = 0, end = 0;
             if (ci < ncand) {
                 e = only ? a.only[ci] : ci;
-                const int off = a.offsets[e], end = a.offsets[e + 1];
+                off = a.offsets[e];
+                end = a.offsets[e + 1];
                 const bool bad = off < 0 || end > rows_total || end < off;
                 if (only || end > off) np = ((bad ? 1 : end - off) + kTok - 1) / kTok;
             }
@@ -221,6 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 s_act[base + tp] = e;
                 s_tp[base + tp] = tp;
+                s_off[base + tp] = off;
+                s_end[base + tp] = end;
             }
             n += __shfl_sync(0xffffffffu, incl, 31);
         }
@@ -236,11 +300,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
-    const long long units = static_cast<long long>(s_nact) * geo.splits * geo.rg8;
+    const unsigned units = static_cast<unsigned>(s_nact) * geo.splits * geo.rg8;
     // each CTA takes a contiguous range of units, so that consecutive units
-    // share the expert and split and reuse the staged token rows
-    const long long u_begin = (units * blockIdx.x) / gridDim.x;
-    const long long u_end = (units * (blockIdx.x + 1)) / gridDim.x;
+    // share the expert and split and reuse the staged token rows: CTA b takes
+    // [floor(units b / grid), floor(units (b + 1) / grid)), the longer ranges
+    // spread evenly, computed in 32 bits as b u_per + floor(b u_rem / grid)
+    const unsigned u_per = units / gridDim.x, u_rem = units - u_per * gridDim.x;
+    const unsigned u_begin = blockIdx.x * u_per + (blockIdx.x * u_rem) / gridDim.x;
+    const unsigned u_end = (blockIdx.x + 1) * u_per + ((blockIdx.x + 1) * u_rem) / gridDim.x;
 
     // A slot is re-armed only after all consumer warps released it, which they
     // do only after seeing its copy land; so at any time each slot has at most
@@ -255,10 +322,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            for (long long u = u_begin; u < u_end && !s_abort; ++u) {
-                const Unit U = decode_unit(u, s_act, s_tp, geo, a, rows_total);
+            for (unsigned u = u_begin; u < u_end && !s_abort; ++u) {
+                const Unit U = decode_unit(u, s_act, s_tp, s_off, s_end, geo, rows_total);
                 if (!U.ok) continue;
-                const uint8_t *w = static_cast<const uint8_t *>(PHASE == kUp ? tab.w1[U.e] : tab.w2[U.e]);
+                const uint8_t *w = static_cast<const uint8_t *>(s_wptr[U.e]);
                 const uint32_t bytes = static_cast<uint32_t>(U.nrg) * kBlockBytes;
                 const int q = U.end - U.off;
                 {  // this unit's pass
@@ -296,10 +363,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     int staged_e = -1, staged_ks = -1, staged_tp = -1;
-    for (long long u = u_begin; u < u_end; ++u) {
+    for (unsigned u = u_begin; u < u_end; ++u) {
         // one decision for all consumer warps: the named barriers need all of them
         if (named_sync_or(kBarConsumers, kConsumers, s_abort)) break;
-        const Unit U = decode_unit(u, s_act, s_tp, geo, a, rows_total);
+        const Unit U = decode_unit(u, s_act, s_tp, s_off, s_end, geo, rows_total);
         if (!U.ok) {
             if (tid == 0) flag_error(a.err, kErrOffsets);
             continue;
@@ -357,7 +424,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 staged_ks = U.ks;
                 staged_tp = tp;
                 if constexpr (WT == WeightType::kI8) {
-                    stage_rows_f16<kTok>(bstage, geo.row_bytes, kcount / 8, warp, lane, s_xscale, s_xsum);
+                    const int nrows = min(kTok, U.end - (U.off + tp * kTok));
+                    stage_rows_f16(bstage, geo.row_bytes, kcount / 8, nrows, warp, lane, s_red, s_red2, s_xscale,
+                                   s_xsum);
                     named_sync(kBarConsumers, kConsumers);
                 }
             }
@@ -548,6 +617,10 @@ template <WeightType WT, int PHASE, bool GATED, int NT>
 cudaError_t launch_one(const ExpertArgs &a, int K, int rows, int splits, int num_sms,
                        cudaStream_t s) {
     const DecodeGeom geo = make_geom<WT>(K, rows, splits, NT);
+    // the kernel counts units (and splits of the reduction blocks) in 32 bits
+    if (static_cast<long long>(kMaxPassEntries) * splits * geo.rg8 >= (1LL << 31) ||
+        static_cast<long long>(geo.nkb) * splits >= (1LL << 31))
+        return cudaErrorInvalidValue;
     const size_t smem = static_cast<size_t>(kStages) * kStageBytes + geo.bstage_bytes;
     auto kern = decode_kernel<WT, PHASE, GATED, NT>;
     static int configured_smem = 0;  // per instantiation
