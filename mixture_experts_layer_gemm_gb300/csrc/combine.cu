@@ -63,6 +63,8 @@ struct Vec {
 // W outputs per thread (4 or 8 consecutive features of one token); KMAX >= k.
 template <bool BF16, int KMAX, int W, bool PB>
 __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
+    if (threadIdx.x == 0)
+        touch_params(a.ypart, a.splits, a.split_stride, a.scatter, a.T, a.k, a.m, a.y, a.err);
     pdl_wait();
     pdl_trigger();
     const int vec = a.m / W;
@@ -103,28 +105,33 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 #pragma unroll
             for (int j = 0; j < KMAX; ++j) {
                 if (pos[j] < 0) continue;
-                // partial rows of the split reduction, four loads in flight at
-                // a time, added in a fixed order: ((p0 + p1) + (p2 + p3)) per
-                // group, groups in split order
+                // partial rows of the split reduction, added in a fixed order
                 const size_t base = static_cast<size_t>(pos[j]) * a.m + c;
                 float v[W];
 #pragma unroll
                 for (int e = 0; e < W; ++e) v[e] = 0.0f;
-                int s = 0;
-                for (; s + 4 <= a.splits; s += 4) {
+                // groups of up to four splits, each group's loads issued
+                // together (a short last group too: one round trip instead of
+                // one per split); a full group adds ((p0 + p1) + (p2 + p3)),
+                // a short one its splits one at a time in split order
+                for (int s = 0; s < a.splits; s += 4) {
+                    const int n = a.splits - s < 4 ? a.splits - s : 4;
                     Vec<W, PB> p0, p1, p2, p3;
                     p0.load(a.ypart, base + (s + 0) * a.split_stride);
-                    p1.load(a.ypart, base + (s + 1) * a.split_stride);
-                    p2.load(a.ypart, base + (s + 2) * a.split_stride);
-                    p3.load(a.ypart, base + (s + 3) * a.split_stride);
+                    if (n > 1) p1.load(a.ypart, base + (s + 1) * a.split_stride);
+                    if (n > 2) p2.load(a.ypart, base + (s + 2) * a.split_stride);
+                    if (n > 3) p3.load(a.ypart, base + (s + 3) * a.split_stride);
+                    if (n == 4) {
 #pragma unroll
-                    for (int e = 0; e < W; ++e) v[e] += (p0.v[e] + p1.v[e]) + (p2.v[e] + p3.v[e]);
-                }
-                for (; s < a.splits; ++s) {
-                    Vec<W, PB> p;
-                    p.load(a.ypart, base + s * a.split_stride);
+                        for (int e = 0; e < W; ++e) v[e] += (p0.v[e] + p1.v[e]) + (p2.v[e] + p3.v[e]);
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < W; ++e) v[e] += p.v[e];
+                        for (int e = 0; e < W; ++e) {
+                            v[e] += p0.v[e];
+                            if (n > 1) v[e] += p1.v[e];
+                            if (n > 2) v[e] += p2.v[e];
+                        }
+                    }
                 }
 #pragma unroll
                 for (int e = 0; e < W; ++e) y[e] += v[e];

@@ -252,6 +252,31 @@ __device__ __forceinline__ void bulk_g2s_once(void *smem_dst, const void *gsrc, 
 // kernel can overlap only its immediate predecessor, and everything issued
 // two kernels back has completed when it starts.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch parameters are never written by a predecessor, but a CTA's first
+// reads of them go to memory (measured: about a microsecond).  A kernel names
+// the parameters it needs soon after its dependency wait in touch_params()
+// before that wait, so those reads are issued, and overlap the predecessor's
+// tail, instead of starting after it.
+__device__ __forceinline__ void touch_one(const void *p) { asm volatile("" ::"l"(p)); }
+__device__ __forceinline__ void touch_one(int v) { asm volatile("" ::"r"(v)); }
+__device__ __forceinline__ void touch_one(unsigned v) { asm volatile("" ::"r"(v)); }
+__device__ __forceinline__ void touch_one(size_t v) { asm volatile("" ::"l"(v)); }
+template <typename... Ts>
+__device__ __forceinline__ void touch_params(const Ts &...v) {
+    (touch_one(v), ...);
+}
+
+// Starts [p, p + bytes) on its way from global memory into L2, in 16 KB bulk
+// prefetches (no destination and nothing to wait for).  p 16-byte aligned,
+// bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *p, size_t bytes) {
+    const char *c = static_cast<const char *>(p);
+    for (size_t o = 0; o < bytes; o += 16384) {
+        const uint32_t n = static_cast<uint32_t>(bytes - o < 16384 ? bytes - o : 16384);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c + o), "r"(n) : "memory");
+    }
+}
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

@@ -239,6 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ const void *s_wptr[kExpertTableMax];
     if (warp == kConsumerWarps)
         for (int e = lane; e < kExpertTableMax; e += 32) s_wptr[e] = PHASE == kUp ? tab.w1[e] : tab.w2[e];
+    if (tid == 0)
+        touch_params(a.offsets, a.only[0], a.n_only, a.E, a.T, a.k, a.gather, a.x, a.h, a.topk_w, a.ypart, a.err);
     // The up projection reads the routing its predecessor (the router) wrote.
     // The down projection's predecessor is the up projection: the routing is
     // two launches back and complete, so the weight stream starts at once and

@@ -466,6 +466,14 @@ constexpr int router_warps() { return EMAX <= 16 ? 32 : (EMAX == 32 ? 16 : 8); }
 
 template <int EMAX>
 __global__ void __launch_bounds__(router_warps<EMAX>() * 32) router_mma_kernel(RouterArgs a, PermuteArgs pa) {
+    // Before the wait: the parameters, and the router matrix (read by every
+    // CTA; [EMAX x m] in the activation type) on its way into L2 -- neither is
+    // written by the predecessor.
+    if (threadIdx.x == 0) {
+        touch_params(a.x, a.wra, a.bias, a.T, a.m, a.E, a.k, a.ids, a.w, a.logits, a.ticket, a.err);
+        touch_params(pa.ids, pa.T, pa.k, pa.E, pa.counts, pa.offsets, pa.gather, pa.scatter, pa.cta_count);
+        if (blockIdx.x == 0) bulk_prefetch_l2(a.wra, static_cast<size_t>(EMAX) * a.m * 2);
+    }
     pdl_wait();
     pdl_trigger();
     constexpr int kRouterWarps = router_warps<EMAX>();
