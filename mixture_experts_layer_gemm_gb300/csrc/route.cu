@@ -52,6 +52,64 @@ __device__ __forceinline__ void select_topk(const float (&l)[EMAX], int E, int k
         if (j < k) w[j] = w[j] / denom;
 }
 
+// The same selection by one warp, for a token whose logits sit in shared
+// memory: lane l holds experts l and (EMAX = 64) l + 32, and each of the k
+// rounds is a warp reduction instead of a scan over all experts.  The choice
+// equals select_topk's scan in expert order: the largest logit left, the lower
+// id among equal ones; a NaN is chosen only when it is the first candidate
+// left (the scan starts from that candidate and no comparison replaces a NaN;
+// a NaN met later never replaces a number).  The weights are select_topk's
+// arithmetic on the same logits: exp(l_j - l_0) summed in round order, then
+// divided.  Lane j < k receives slot j: *id and *wt.
+template <int EMAX>
+__device__ __forceinline__ void select_topk_warp(const float *lg, int E, int k, int lane, int *id, float *wt) {
+    const float v0 = (lane < EMAX && lane < E) ? lg[lane] : 0.0f;
+    const float v1 = (EMAX > 32 && lane + 32 < E) ? lg[lane + 32] : 0.0f;
+    bool left0 = lane < EMAX && lane < E, left1 = EMAX > 32 && lane + 32 < E;  // untaken candidates
+    float l0 = 0.0f, denom = 0.0f, mine = 0.0f;
+    int my_id = -1;
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) {
+        const unsigned m0 = __ballot_sync(0xffffffffu, left0), m1 = __ballot_sync(0xffffffffu, left1);
+        const int first = m0 ? __ffs(m0) - 1 : 32 + __ffs(m1) - 1;
+        const float fv = __shfl_sync(0xffffffffu, first < 32 ? v0 : v1, first & 31);
+        int bi = first;
+        float bv = fv;
+        if (fv == fv) {
+            // this lane's best number left: (v0, lane) before (v1, lane + 32) on a tie
+            const bool h0 = left0 && v0 == v0, h1 = left1 && v1 == v1;
+            const bool pick0 = h0 && (!h1 || v0 >= v1);
+            bool has = h0 || h1;
+            float cv = pick0 ? v0 : v1;
+            int ci = pick0 ? lane : lane + 32;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, cv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, ci, o);
+                const bool oh = __shfl_xor_sync(0xffffffffu, has, o);
+                if (oh && (!has || ov > cv || (ov == cv && oi < ci))) {
+                    cv = ov;
+                    ci = oi;
+                    has = true;
+                }
+            }
+            bi = ci;
+            bv = cv;
+        }
+        if (bi == lane) left0 = false;
+        if (bi == lane + 32) left1 = false;
+        if (j == 0) l0 = bv;
+        const float ej = expf(bv - l0);
+        denom += ej;
+        if (lane == j) {
+            my_id = bi;
+            mine = ej;
+        }
+    }
+    *id = my_id;
+    *wt = mine / denom;
+}
+
 // Histogram, exclusive scan and stable scatter of the n = T*k flat indices by
 // expert, done by one CTA (any multiple of 32 threads up to 1024):
 //   pass 1: counts[e] by shared-memory integer atomics (order-free);
@@ -533,18 +591,13 @@ __global__ void __launch_bounds__(router_warps<EMAX>() * 32) router_mma_kernel(R
     __syncthreads();
     for (int tk = warp; tk < ntok; tk += kRouterWarps) {
         const int tok = t0 + tk;
-        float l[EMAX];
-#pragma unroll
-        for (int e = 0; e < EMAX; ++e) l[e] = (e < a.E) ? s_logit[tk][e] : 0.0f;
-        int ids[kMaxTopK];
-        float wts[kMaxTopK];
-        select_topk<EMAX>(l, a.E, a.k, ids, wts);
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j)
-            if (j < a.k && lane == j) {
-                a.ids[static_cast<size_t>(tok) * a.k + j] = ids[j];
-                a.w[static_cast<size_t>(tok) * a.k + j] = wts[j];
-            }
+        int id;
+        float wt;
+        select_topk_warp<EMAX>(s_logit[tk], a.E, a.k, lane, &id, &wt);
+        if (lane < a.k) {
+            a.ids[static_cast<size_t>(tok) * a.k + lane] = id;
+            a.w[static_cast<size_t>(tok) * a.k + lane] = wt;
+        }
     }
     if (gridDim.x == 1) {
         // the whole batch is in this CTA: no ticket; one warp permutes small batches
