@@ -146,6 +146,43 @@ def test_fused_router_selection_equals_oracle_topk_on_gpu_logits():
     ml.close()
 
 
+@pytest.mark.parametrize("shape", [SWIGLU_BF16, ODD_BF16, WIDE_E], ids=lambda s: s.name)
+def test_fused_router_choice_on_non_finite_logits_equals_the_scan(shape):
+    """Token rows holding infinities or NaNs give logits of +-inf and NaN.  The
+    fused router selects each token's top-k with warp reductions; route_from_
+    logits selects with a scan over the experts in order.  On the same logits
+    (the fused router writes the ones it used) both must choose the same
+    experts and weights: the largest logit left, the lower id on a tie, a NaN
+    only when it is the first candidate left.  E = 8, 5 (lanes without an
+    expert) and 64 (two experts per lane)."""
+    layer = get_layer(shape, seed=8)
+    T = 24
+    x = wl.make_tokens(shape, T, seed=9).copy()
+    pinf, ninf, nan = np.uint16(0x7F80), np.uint16(0xFF80), np.uint16(0x7FC0)
+    x[4, 0] = pinf                       # logits +-inf by the sign of each expert's weight
+    x[5, 0] = nan                        # every logit NaN
+    x[6, 0], x[6, 1] = pinf, ninf        # inf - inf: NaN for some experts, +-inf for others
+    x[7, 3] = ninf
+    x[8, :] = 0                          # all logits zero: ties everywhere
+    x[9, 2], x[9, 5] = pinf, pinf
+    fused = moe.MoELayer(layer, T, with_logits=True)
+    run = Run(fused, x, forward=False)
+    assert np.isinf(run.logits[4]).any() and (~np.isfinite(run.logits[4])).all()
+    assert np.isnan(run.logits[5]).all()
+    assert np.isnan(run.logits[6]).any() or np.isinf(run.logits[6]).any()
+    scan = moe.MoELayer(layer, T)
+    ref = Run(scan, x, routing="logits", logits=run.logits, forward=False)
+    np.testing.assert_array_equal(run.ids, ref.ids)
+    np.testing.assert_array_equal(run.w.view(np.uint32), ref.w.view(np.uint32))
+    check_permutation(run, shape.E)
+    # the finite rows also equal the oracle's top-k of those logits
+    fin = np.isfinite(run.logits).all(axis=1)
+    oids, _ = oracle.topk(run.logits[fin].astype(np.float64), shape.k)
+    np.testing.assert_array_equal(run.ids[fin], oids)
+    fused.close()
+    scan.close()
+
+
 # ---- bf16 layers through the decode kernels ------------------------------------------
 @pytest.mark.parametrize("T", [1, 4, 16, 37, 64, 200])
 def test_swiglu_bf16_decode(T):
