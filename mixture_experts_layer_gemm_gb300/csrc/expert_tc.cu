@@ -106,8 +106,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
+            int cur = 0;  // expert of the last tile (a role's tiles come in order)
             for (long long u = blockIdx.x; u < total && !s_abort; u += gridDim.x) {
-                const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
+                const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo, cur);
                 const uint8_t *w = static_cast<const uint8_t *>(PHASE == kUp ? tab.w1[t.e] : tab.w2[t.e]);
                 const int brow = t.off + t.tt * geo.N;
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
@@ -136,8 +137,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             int ntile = 0;
+            int cur = 0;  // expert of the last tile (a role's tiles come in order)
             for (long long u = blockIdx.x; u < total && !s_abort; u += gridDim.x, ++ntile) {
-                const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
+                const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo, cur);
                 const int buf = ntile & 1;
                 const uint32_t use_parity = (ntile >> 1) & 1;
                 if (!mbar_wait_spin(&tempty_bar[buf], use_parity ^ 1u)) {
@@ -183,10 +185,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int lq = warp & 3;            // TMEM lane quarter this warp may access
         const int row_in_tile = lq * 32 + lane;
         int ntile = 0;
+        int cur = 0;  // expert of the last tile (a role's tiles come in order)
         for (long long u = blockIdx.x; u < total; u += gridDim.x, ++ntile) {
             // warp-uniform decisions: tcgen05.ld below needs the whole warp
             if (__any_sync(0xffffffffu, s_abort)) break;
-            const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
+            const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo, cur);
             const int buf = ntile & 1;
             const uint32_t use_parity = (ntile >> 1) & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(&tfull_bar[buf], use_parity))) {
@@ -316,6 +319,7 @@ __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t
 template <int PHASE, bool GATED>
 cudaError_t launch_tc_t(const ExpertArgs &a, const TcGeom &g, const CUtensorMap &bmap, int num_sms,
                         cudaStream_t s) {
+    if (!tc_tiles_fit(a, g)) return cudaErrorInvalidValue;
     const size_t smem = 1024 + static_cast<size_t>(g.stages) * (kATileBytes + g.b_bytes);
     auto kern = tc_kernel<PHASE, GATED>;
     static int configured = 0;

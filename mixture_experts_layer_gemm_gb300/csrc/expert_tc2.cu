@@ -114,8 +114,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             const uint8_t *wbase = static_cast<const uint8_t *>(a.wbase);
+            int cur = 0;  // expert of the last tile (a role's tiles come in order)
             for (long long u = pair; u < total && !s_abort; u += npairs) {
-                const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
+                const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo, cur);
                 const uint8_t *w = static_cast<const uint8_t *>(tab.w1[t.e]);
                 const int nv = min(kN, (t.q - t.tt * kN + 31) / 32 * 32);
                 const int brow = t.off + t.tt * kN + static_cast<int>(rank) * (nv / 2);
@@ -148,8 +149,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             int ntile = 0;
+            int cur = 0;  // expert of the last tile (a role's tiles come in order)
             for (long long u = pair; u < total && !s_abort; u += npairs, ++ntile) {
-                const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
+                const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo, cur);
                 const int buf = ntile & 1;
                 const uint32_t use_parity = (ntile >> 1) & 1;
                 if (!mbar_wait_cluster_spin(&tempty_bar[buf], use_parity ^ 1u)) {
@@ -197,9 +199,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lq = warp & 3;
         const int row_in_tile = lq * 32 + lane;
         int ntile = 0;
+        int cur = 0;  // expert of the last tile (a role's tiles come in order)
         for (long long u = pair; u < total; u += npairs, ++ntile) {
             if (__any_sync(0xffffffffu, s_abort)) break;
-            const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
+            const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo, cur);
             const int buf = ntile & 1;
             const uint32_t use_parity = (ntile >> 1) & 1;
             if (!__all_sync(0xffffffffu, mbar_wait_cluster(&tfull_bar[buf], use_parity))) {
@@ -261,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool GATED>
 cudaError_t launch_t(const ExpertArgs &a, const TcGeom &g, const CUtensorMap &amap, const CUtensorMap &bmap,
                      int num_sms, cudaStream_t s) {
+    if (!tc_tiles_fit(a, g)) return cudaErrorInvalidValue;
     const size_t smem = 1024 + static_cast<size_t>(g.stages) * kStageBytes;
     auto kern = tc2_kernel<GATED>;
     static int configured = 0, pairs = 0;

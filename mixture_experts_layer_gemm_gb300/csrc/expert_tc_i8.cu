@@ -154,8 +154,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
+            int cur = 0;  // expert of the last tile (a role's tiles come in order)
             for (long long u = blockIdx.x; u < total && !s_abort; u += gridDim.x) {
-                const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
+                const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo, cur);
                 const uint8_t *w = static_cast<const uint8_t *>(PHASE == kUp ? tab.w1[t.e] : tab.w2[t.e]);
                 const int brow = t.off + t.tt * geo.N;
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
@@ -189,8 +190,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0, abuf = 0;
             uint32_t phase = 0, aphase = 0;
             int ntile = 0;
+            int cur = 0;  // expert of the last tile (a role's tiles come in order)
             for (long long u = blockIdx.x; u < total && !s_abort; u += gridDim.x, ++ntile) {
-                const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
+                const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo, cur);
                 const int buf = ntile & 1;
                 const uint32_t use_parity = (ntile >> 1) & 1;
                 if (!mbar_wait_spin(&tempty_bar[buf], use_parity ^ 1u)) {
@@ -256,9 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lq = warp & 3;
         const int row_in_tile = lq * 32 + lane;
         int ntile = 0;
+        int cur = 0;  // expert of the last tile (a role's tiles come in order)
         for (long long u = blockIdx.x; u < total; u += gridDim.x, ++ntile) {
             if (__any_sync(0xffffffffu, s_abort)) break;
-            const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
+            const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo, cur);
             const int buf = ntile & 1;
             const uint32_t use_parity = (ntile >> 1) & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(&tfull_bar[buf], use_parity))) {
@@ -371,9 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t row_off = static_cast<uint32_t>(rgl * kBlockBytes + G * 1024 + hk * 512);
         int stage = 0, abuf = 0;
         uint32_t phase = 0, aphase = 0;
+        int cur = 0;  // expert of the last tile (a role's tiles come in order)
         for (long long u = blockIdx.x; u < total; u += gridDim.x) {
             if (__any_sync(0xffffffffu, s_abort)) break;
-            const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo);
+            const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo, cur);
             bool ok = true;
             for (int kb = t.kb0; kb < t.kb1; ++kb) {
                 // warp-uniform waits: tcgen05.st below needs the whole warp
@@ -520,6 +524,7 @@ __global__ void __launch_bounds__(kGatherThreads)
 template <int PHASE, bool GATED>
 cudaError_t launch_t(const ExpertArgs &a, const TcGeom &g, const CUtensorMap &bmap, int num_sms,
                      cudaStream_t s) {
+    if (!tc_tiles_fit(a, g)) return cudaErrorInvalidValue;
     const size_t smem = 1024 + static_cast<size_t>(g.stages) * (kA8Bytes + 2 * g.b_bytes);
     auto kern = tc_i8_kernel<PHASE, GATED>;
     static int configured = 0;

@@ -30,23 +30,43 @@ struct TcTile {
     int e, ks, rb, tt, off, q, kb0, kb1;
 };
 
+// Tile u of the launch.  `cur` is the caller's cursor into the expert list:
+// a role walks its tiles in increasing order, so the search for u's expert
+// starts where the last one ended (a scan from the first expert costs a chain
+// of dependent shared-memory loads per tile with many experts).  The index
+// arithmetic is 32-bit (the launchers check that one expert's tiles fit): a
+// role's single thread runs it between two tiles, where 64-bit divisions
+// (software sequences) held the MMAs back about a microsecond per tile.
 __device__ __forceinline__ TcTile tc_tile(long long u, const long long *prefix, const int *act,
-                                          const int *offs, const int *qs, int nact, const TcGeom &g) {
-    int i = 0;
+                                          const int *offs, const int *qs, int nact, const TcGeom &g, int &cur) {
+    int i = cur;
     while (i + 1 < nact && u >= prefix[i + 1]) ++i;
-    const long long local = u - prefix[i];
-    const int ntt = (qs[i] + g.N - 1) / g.N;
+    cur = i;
+    const unsigned local = static_cast<unsigned>(u - prefix[i]);
+    const unsigned ntt = static_cast<unsigned>((qs[i] + g.N - 1) / g.N);
+    const unsigned nrb = static_cast<unsigned>(g.n_rb);
     TcTile t;
     t.e = act[i];
     t.off = offs[i];
     t.q = qs[i];
-    t.tt = static_cast<int>(local % ntt);
-    const long long rest = local / ntt;
-    t.rb = static_cast<int>(rest % g.n_rb);
-    t.ks = static_cast<int>(rest / g.n_rb);
-    t.kb0 = static_cast<int>((static_cast<long long>(g.nkb) * t.ks) / g.splits);
-    t.kb1 = static_cast<int>((static_cast<long long>(g.nkb) * (t.ks + 1)) / g.splits);
+    const unsigned rest = local / ntt;
+    t.tt = static_cast<int>(local - rest * ntt);
+    const unsigned ks = rest / nrb;
+    t.rb = static_cast<int>(rest - ks * nrb);
+    t.ks = static_cast<int>(ks);
+    const unsigned nkb = static_cast<unsigned>(g.nkb), sp = static_cast<unsigned>(g.splits);
+    t.kb0 = static_cast<int>((nkb * ks) / sp);
+    t.kb1 = static_cast<int>((nkb * (ks + 1)) / sp);
     return t;
+}
+
+// Host side: whether tc_tile's 32-bit arithmetic holds for a launch (one
+// expert's tiles, at most ceil(T k / N) token tiles, and nkb x splits below
+// 2^31); the launchers refuse a launch for which it does not.
+inline bool tc_tiles_fit(const ExpertArgs &a, const TcGeom &g) {
+    const long long ntt = (static_cast<long long>(a.T) * a.k + g.N - 1) / g.N;
+    return static_cast<long long>(g.splits) * g.n_rb * ntt < (1LL << 31) &&
+           static_cast<long long>(g.nkb) * (g.splits + 1) < (1LL << 31);
 }
 
 // One warp (all 32 lanes): list the experts this launch covers (all with
