@@ -350,6 +350,34 @@ def test_int8_decode(T):
     run_and_check(I8, T, seed=14, regime=moe.REGIME_DECODE)
 
 
+def test_int8_decode_passes_of_every_row_count():
+    """The int8 GEMV converts a pass's token rows to fp16 with several warps
+    per row when the pass has few rows (8 warps for one row, 4 for two, 2 for
+    three or four, 1 from five on).  Routing given so that experts 0-6 hold
+    1, 2, 3, 4, 5, 8 and 9 rows (the last in two passes of 8 + 1 with 8-token
+    passes): every form, against the oracle on its own int8 codes."""
+    layer = get_layer(I8, seed=18)
+    counts = [1, 2, 3, 4, 5, 8, 9, 0]
+    flat = np.repeat(np.arange(I8.E), counts)  # 32 pairs, sorted by expert
+    T = flat.size // 2
+    ids = np.stack([flat[:T], flat[T:]], axis=1).astype(np.int32)  # no expert twice in a token
+    assert (ids[:, 0] != ids[:, 1]).all()
+    rng = np.random.default_rng(19)
+    w = rng.random((T, 2)).astype(np.float32) + 0.1
+    w = (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
+    x = wl.make_tokens(I8, T, seed=20)
+    ml = moe.MoELayer(layer, T)
+    ml.set_regime(moe.REGIME_DECODE)
+    assert moe.PATHS[ml.plan(T).path] == "gemv" and ml.plan(T).tile_up == 8
+    run = Run(ml, x, routing="topk", ids=ids, w=w)
+    assert ml.sync_check()[0] == moe.MOE_OK
+    np.testing.assert_array_equal(run.counts, counts)
+    qref = oracle_y(layer, x, ids, w.astype(np.float64), oracle_quantized(layer))
+    rel, _ = max_token_rel_l2(run.y_np, qref)
+    assert rel <= 1e-2, rel
+    ml.close()
+
+
 @pytest.mark.parametrize("T", [1, 37, 200, 700])
 def test_int8_tensor_core(T):
     """int8 codes widened in tensor memory (fp16 against fp16 token rows in the up
