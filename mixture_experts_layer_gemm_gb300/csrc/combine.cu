@@ -31,13 +31,16 @@ struct Vec {
     __device__ __forceinline__ void load(const void *base, size_t off) {
         if constexpr (PB) {
             const uint16_t *p = static_cast<const uint16_t *>(base) + off;
-            if constexpr (W == 8) {
-                const uint4 q = __ldcg(reinterpret_cast<const uint4 *>(p));
-                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+            if constexpr (W >= 8) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    v[2 * i] = bf16lo(w[i]);
-                    v[2 * i + 1] = bf16hi(w[i]);
+                for (int h = 0; h < W / 8; ++h) {
+                    const uint4 q = __ldcg(reinterpret_cast<const uint4 *>(p + 8 * h));
+                    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        v[8 * h + 2 * i] = bf16lo(w[i]);
+                        v[8 * h + 2 * i + 1] = bf16hi(w[i]);
+                    }
                 }
             } else {
                 const uint2 q = __ldcg(reinterpret_cast<const uint2 *>(p));
@@ -60,7 +63,8 @@ struct Vec {
     }
 };
 
-// W outputs per thread (4 or 8 consecutive features of one token); KMAX >= k.
+// W outputs per thread (4, 8 or, with bf16 partial rows, 16 consecutive features
+// of one token); KMAX >= k.
 template <bool BF16, int KMAX, int W, bool PB>
 __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
     if (threadIdx.x == 0)
@@ -142,10 +146,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 #pragma unroll
             for (int e = 0; e < W / 2; ++e) o[e] = pack_bf16x2(y[2 * e], y[2 * e + 1]);
             __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.y) + static_cast<size_t>(t) * a.m + c;
-            if constexpr (W == 8)
-                *reinterpret_cast<uint4 *>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
-            else
+            if constexpr (W >= 8) {
+#pragma unroll
+                for (int h = 0; h < W / 8; ++h)
+                    *reinterpret_cast<uint4 *>(dst + 8 * h) =
+                        make_uint4(o[4 * h], o[4 * h + 1], o[4 * h + 2], o[4 * h + 3]);
+            } else {
                 *reinterpret_cast<uint2 *>(dst) = make_uint2(o[0], o[1]);
+            }
         } else {
             float *dst = static_cast<float *>(a.y) + static_cast<size_t>(t) * a.m + c;
 #pragma unroll
@@ -157,11 +165,23 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 
 template <bool BF16, int KMAX, bool PB>
 cudaError_t launch_w(const CombineArgs &a, cudaStream_t s) {
-    const int w = (a.m % 8 == 0) ? 8 : 4;
+    // bf16 partial rows of large batches: 16 features per thread.  Once the
+    // capped grid makes every thread loop over several chunks, the bytes each
+    // loop iteration has in flight set the rate; with 8 features of bf16 rows
+    // that is half of the fp32 rows' (Mixtral shape, T = 8192: 71 us, 30% of
+    // HBM, against 55 us for fp32 rows; 16 features: 62 us).  With one chunk per
+    // thread (T = 2048) more resident threads matter more: 8 features there
+    // (27 us against 31 us with 16).
+    constexpr long long kGridThreads = 152LL * 16 * 256;
+    const bool wide = PB && a.m % 16 == 0 && static_cast<long long>(a.T) * (a.m / 16) >= kGridThreads;
+    const int w = wide ? 16 : (a.m % 8 == 0) ? 8 : 4;
     const long long n = static_cast<long long>(a.T) * (a.m / w);
     long long blocks = (n + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks * 256 > kGridThreads) blocks = kGridThreads / 256;
     const dim3 grid(static_cast<unsigned>(blocks));
+    if constexpr (PB) {
+        if (w == 16) return launch_pdl(combine_kernel<BF16, KMAX, 16, PB>, grid, dim3(256), 0, s, a);
+    }
     return w == 8 ? launch_pdl(combine_kernel<BF16, KMAX, 8, PB>, grid, dim3(256), 0, s, a)
                   : launch_pdl(combine_kernel<BF16, KMAX, 4, PB>, grid, dim3(256), 0, s, a);
 }
