@@ -63,8 +63,86 @@ struct Vec {
     }
 };
 
-// W outputs per thread (4, 8 or, with bf16 partial rows, 16 consecutive features
-// of one token); KMAX >= k.
+// One output chunk: token t, features c .. c + W - 1, from the token's
+// permuted positions pos[j] (-1 for a slot past k or a bad position): the sum
+// over slots j, ascending, of the partial rows (the reduction splits added
+// first, in groups of four in split order), rounded once to the activation type.
+template <bool BF16, int KMAX, int W, bool PB>
+__device__ __forceinline__ void combine_item(const CombineArgs &a, int t, int c, const int (&pos)[KMAX]) {
+    float y[W];
+#pragma unroll
+    for (int e = 0; e < W; ++e) y[e] = 0.0f;
+    if (a.splits == 1) {
+        Vec<W, PB> q[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+#pragma unroll
+            for (int e = 0; e < W; ++e) q[j].v[e] = 0.0f;
+            if (pos[j] >= 0) q[j].load(a.ypart, static_cast<size_t>(pos[j]) * a.m + c);
+        }
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+            if (pos[j] >= 0)
+#pragma unroll
+                for (int e = 0; e < W; ++e) y[e] += 0.0f + q[j].v[e];
+    } else {
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            if (pos[j] < 0) continue;
+            // partial rows of the split reduction, added in a fixed order
+            const size_t base = static_cast<size_t>(pos[j]) * a.m + c;
+            float v[W];
+#pragma unroll
+            for (int e = 0; e < W; ++e) v[e] = 0.0f;
+            // groups of up to four splits, each group's loads issued
+            // together (a short last group too: one round trip instead of
+            // one per split); a full group adds ((p0 + p1) + (p2 + p3)),
+            // a short one its splits one at a time in split order
+            for (int s = 0; s < a.splits; s += 4) {
+                const int n = a.splits - s < 4 ? a.splits - s : 4;
+                Vec<W, PB> p0, p1, p2, p3;
+                p0.load(a.ypart, base + (s + 0) * a.split_stride);
+                if (n > 1) p1.load(a.ypart, base + (s + 1) * a.split_stride);
+                if (n > 2) p2.load(a.ypart, base + (s + 2) * a.split_stride);
+                if (n > 3) p3.load(a.ypart, base + (s + 3) * a.split_stride);
+                if (n == 4) {
+#pragma unroll
+                    for (int e = 0; e < W; ++e) v[e] += (p0.v[e] + p1.v[e]) + (p2.v[e] + p3.v[e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < W; ++e) {
+                        v[e] += p0.v[e];
+                        if (n > 1) v[e] += p1.v[e];
+                        if (n > 2) v[e] += p2.v[e];
+                    }
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < W; ++e) y[e] += v[e];
+        }
+    }
+    if (BF16) {
+        uint32_t o[W / 2];
+#pragma unroll
+        for (int e = 0; e < W / 2; ++e) o[e] = pack_bf16x2(y[2 * e], y[2 * e + 1]);
+        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.y) + static_cast<size_t>(t) * a.m + c;
+        if constexpr (W >= 8) {
+#pragma unroll
+            for (int h = 0; h < W / 8; ++h)
+                *reinterpret_cast<uint4 *>(dst + 8 * h) =
+                    make_uint4(o[4 * h], o[4 * h + 1], o[4 * h + 2], o[4 * h + 3]);
+        } else {
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(o[0], o[1]);
+        }
+    } else {
+        float *dst = static_cast<float *>(a.y) + static_cast<size_t>(t) * a.m + c;
+#pragma unroll
+        for (int e = 0; e < W; e += 4)
+            *reinterpret_cast<float4 *>(dst + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
+    }
+}
+
+// W outputs per thread (4 or 8 consecutive features of one token); KMAX >= k.
 template <bool BF16, int KMAX, int W, bool PB>
 __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
     if (threadIdx.x == 0)
@@ -89,99 +167,67 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
                     pos[j] = p;
             }
         }
-        float y[W];
-#pragma unroll
-        for (int e = 0; e < W; ++e) y[e] = 0.0f;
-        if (a.splits == 1) {
-            Vec<W, PB> q[KMAX];
-#pragma unroll
-            for (int j = 0; j < KMAX; ++j) {
-#pragma unroll
-                for (int e = 0; e < W; ++e) q[j].v[e] = 0.0f;
-                if (pos[j] >= 0) q[j].load(a.ypart, static_cast<size_t>(pos[j]) * a.m + c);
-            }
-#pragma unroll
-            for (int j = 0; j < KMAX; ++j)
-                if (pos[j] >= 0)
-#pragma unroll
-                    for (int e = 0; e < W; ++e) y[e] += 0.0f + q[j].v[e];
-        } else {
-#pragma unroll
-            for (int j = 0; j < KMAX; ++j) {
-                if (pos[j] < 0) continue;
-                // partial rows of the split reduction, added in a fixed order
-                const size_t base = static_cast<size_t>(pos[j]) * a.m + c;
-                float v[W];
-#pragma unroll
-                for (int e = 0; e < W; ++e) v[e] = 0.0f;
-                // groups of up to four splits, each group's loads issued
-                // together (a short last group too: one round trip instead of
-                // one per split); a full group adds ((p0 + p1) + (p2 + p3)),
-                // a short one its splits one at a time in split order
-                for (int s = 0; s < a.splits; s += 4) {
-                    const int n = a.splits - s < 4 ? a.splits - s : 4;
-                    Vec<W, PB> p0, p1, p2, p3;
-                    p0.load(a.ypart, base + (s + 0) * a.split_stride);
-                    if (n > 1) p1.load(a.ypart, base + (s + 1) * a.split_stride);
-                    if (n > 2) p2.load(a.ypart, base + (s + 2) * a.split_stride);
-                    if (n > 3) p3.load(a.ypart, base + (s + 3) * a.split_stride);
-                    if (n == 4) {
-#pragma unroll
-                        for (int e = 0; e < W; ++e) v[e] += (p0.v[e] + p1.v[e]) + (p2.v[e] + p3.v[e]);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < W; ++e) {
-                            v[e] += p0.v[e];
-                            if (n > 1) v[e] += p1.v[e];
-                            if (n > 2) v[e] += p2.v[e];
-                        }
-                    }
-                }
-#pragma unroll
-                for (int e = 0; e < W; ++e) y[e] += v[e];
-            }
+        combine_item<BF16, KMAX, W, PB>(a, t, c, pos);
+    }
+}
+
+// Batch-sized calls with bf16 partial rows: one warp per token.  The token's k
+// permuted positions are read once (lanes 0 .. k - 1) and shared by shuffle,
+// then the warp walks the token's features in chunks of 32 W (W per lane): no
+// dependent position load per chunk, so a lane's partial-row loads of
+// successive chunks are the only round trips.  Same arithmetic and order as
+// combine_kernel.
+template <bool BF16, int KMAX, int W, bool PB>
+__global__ void __launch_bounds__(256) combine_tokens_kernel(const CombineArgs a) {
+    if (threadIdx.x == 0)
+        touch_params(a.ypart, a.splits, a.split_stride, a.scatter, a.T, a.k, a.m, a.y, a.err);
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const long long warp0 = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+    const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+    const int rows = a.T * a.k;
+    for (long long tt = warp0; tt < a.T; tt += nwarps) {
+        const int t = static_cast<int>(tt);
+        int mine = -1;
+        if (lane < a.k) {
+            const int p = a.scatter[static_cast<size_t>(t) * a.k + lane];
+            if (p < 0 || p >= rows)
+                flag_error(a.err, kErrGatherIndex);
+            else
+                mine = p;
         }
-        if (BF16) {
-            uint32_t o[W / 2];
+        int pos[KMAX];
 #pragma unroll
-            for (int e = 0; e < W / 2; ++e) o[e] = pack_bf16x2(y[2 * e], y[2 * e + 1]);
-            __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.y) + static_cast<size_t>(t) * a.m + c;
-            if constexpr (W >= 8) {
-#pragma unroll
-                for (int h = 0; h < W / 8; ++h)
-                    *reinterpret_cast<uint4 *>(dst + 8 * h) =
-                        make_uint4(o[4 * h], o[4 * h + 1], o[4 * h + 2], o[4 * h + 3]);
-            } else {
-                *reinterpret_cast<uint2 *>(dst) = make_uint2(o[0], o[1]);
-            }
-        } else {
-            float *dst = static_cast<float *>(a.y) + static_cast<size_t>(t) * a.m + c;
-#pragma unroll
-            for (int e = 0; e < W; e += 4)
-                *reinterpret_cast<float4 *>(dst + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
-        }
+        for (int j = 0; j < KMAX; ++j) pos[j] = __shfl_sync(0xffffffffu, mine, j);
+#pragma unroll 2
+        for (int c = lane * W; c < a.m; c += 32 * W) combine_item<BF16, KMAX, W, PB>(a, t, c, pos);
     }
 }
 
 template <bool BF16, int KMAX, bool PB>
 cudaError_t launch_w(const CombineArgs &a, cudaStream_t s) {
-    // bf16 partial rows of large batches: 16 features per thread.  Once the
-    // capped grid makes every thread loop over several chunks, the bytes each
-    // loop iteration has in flight set the rate; with 8 features of bf16 rows
-    // that is half of the fp32 rows' (Mixtral shape, T = 8192: 71 us, 30% of
-    // HBM, against 55 us for fp32 rows; 16 features: 62 us).  With one chunk per
-    // thread (T = 2048) more resident threads matter more: 8 features there
-    // (27 us against 31 us with 16).
     constexpr long long kGridThreads = 152LL * 16 * 256;
-    const bool wide = PB && a.m % 16 == 0 && static_cast<long long>(a.T) * (a.m / 16) >= kGridThreads;
-    const int w = wide ? 16 : (a.m % 8 == 0) ? 8 : 4;
+    if constexpr (PB) {
+        // bf16 partial rows of a large batch (batch regime): a warp per token,
+        // 16 features per lane, so a lane has as many bytes in flight as with
+        // fp32 rows and 8 features, and no position load per chunk (Mixtral
+        // shape, T = 8192: 71 us with the per-chunk kernel and 8 features of
+        // bf16 rows, 30% of HBM; 56 us now).  Smaller batches give too few
+        // warps for it (T = 512: 16 us against 11 with the per-chunk kernel),
+        // so it takes batches of at least two blocks of warps per SM.
+        if (a.m % 16 == 0 && a.T >= 2 * 152 * 8) {
+            long long blocks = (static_cast<long long>(a.T) + 7) / 8;  // 8 warps per block
+            if (blocks * 256 > kGridThreads) blocks = kGridThreads / 256;
+            return launch_pdl(combine_tokens_kernel<BF16, KMAX, 16, PB>, dim3(static_cast<unsigned>(blocks)),
+                              dim3(256), 0, s, a);
+        }
+    }
+    const int w = (a.m % 8 == 0) ? 8 : 4;
     const long long n = static_cast<long long>(a.T) * (a.m / w);
     long long blocks = (n + 255) / 256;
     if (blocks * 256 > kGridThreads) blocks = kGridThreads / 256;
     const dim3 grid(static_cast<unsigned>(blocks));
-    if constexpr (PB) {
-        if (w == 16) return launch_pdl(combine_kernel<BF16, KMAX, 16, PB>, grid, dim3(256), 0, s, a);
-    }
     return w == 8 ? launch_pdl(combine_kernel<BF16, KMAX, 8, PB>, grid, dim3(256), 0, s, a)
                   : launch_pdl(combine_kernel<BF16, KMAX, 4, PB>, grid, dim3(256), 0, s, a);
 }
