@@ -205,9 +205,199 @@ __global__ void __launch_bounds__(256) combine_tokens_kernel(const CombineArgs a
     }
 }
 
+// Batch regime, bf16 partial rows, bf16 output: the partial rows staged in
+// shared memory by bulk copies.  A warp takes (token, chunk of kStagedCW
+// features) items in turn; lanes 0 .. k*splits-1 each copy one partial row's
+// chunk (the token's k positions read once per item and shared by shuffle)
+// into the warp's buffer, completing on its mbarrier, while the warp sums the
+// previous item from the other buffer.  The bytes in flight no longer cost
+// registers: the register-staged kernels above stay latency-bound on these
+// rows (a warp per token: 58% of HBM at T = 8192).  Same arithmetic and order
+// as combine_item.  Every wait is bounded; a warp that gives up flags the
+// error word and waits (bounded) for its own copies before leaving.
+constexpr int kStagedCW = 2048;      // features of one staged chunk (4 KB of a bf16 row)
+constexpr int kStagedMaxRows = 8;    // k x splits partial rows per item
+constexpr int kStagedMaxWarps = 8;
+
+template <int KMAX>
+__global__ void __launch_bounds__(kStagedMaxWarps * 32) combine_staged_kernel(const CombineArgs a) {
+    extern __shared__ __align__(128) uint8_t smem_cs[];
+    __shared__ uint64_t bar[kStagedMaxWarps][2];
+    if (threadIdx.x == 0)
+        touch_params(a.ypart, a.splits, a.split_stride, a.scatter, a.T, a.k, a.m, a.y, a.err);
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int R = a.k * a.splits;  // partial rows per item, <= kStagedMaxRows
+    const size_t buf_bytes = static_cast<size_t>(R) * kStagedCW * 2;
+    uint8_t *bufs = smem_cs + static_cast<size_t>(wib) * 2 * buf_bytes;
+    if (lane == 0) {
+        mbar_init(&bar[wib][0], 1);
+        mbar_init(&bar[wib][1], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    const int nch = (a.m + kStagedCW - 1) / kStagedCW;
+    const long long items = static_cast<long long>(a.T) * nch;
+    const long long step = static_cast<long long>(gridDim.x) * nw;
+    const int rows_total = a.T * a.k;
+    const uint16_t *part = static_cast<const uint16_t *>(a.ypart);
+    int pos[2][KMAX];
+    uint32_t phase[2] = {0u, 0u};
+    bool pending[2] = {false, false};
+    // copies of item `it` into buffer b (positions into pos[b])
+    auto issue = [&](long long it, int b) {
+        const int t = static_cast<int>(it / nch), c0 = static_cast<int>(it % nch) * kStagedCW;
+        const int cw = min(kStagedCW, a.m - c0);
+        int mine = -1;
+        if (lane < a.k) {
+            const int p = a.scatter[static_cast<size_t>(t) * a.k + lane];
+            if (p < 0 || p >= rows_total)
+                flag_error(a.err, kErrGatherIndex);
+            else
+                mine = p;
+        }
+        int valid = 0;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            pos[b][j] = __shfl_sync(0xffffffffu, mine, j);
+            valid += (j < a.k && pos[b][j] >= 0) ? 1 : 0;
+        }
+        uint8_t *dst = bufs + static_cast<size_t>(b) * buf_bytes;
+        if (lane == 0) mbar_arrive_expect_tx(&bar[wib][b], static_cast<uint32_t>(valid * a.splits * cw * 2));
+        __syncwarp();
+        if (lane < R) {
+            const int j = lane / a.splits, sp = lane - j * a.splits;
+            int pj = -1;
+#pragma unroll
+            for (int jj = 0; jj < KMAX; ++jj)
+                if (jj == j) pj = pos[b][jj];
+            if (pj >= 0)
+                bulk_g2s_once(dst + static_cast<size_t>(lane) * kStagedCW * 2,
+                              part + static_cast<size_t>(sp) * a.split_stride + static_cast<size_t>(pj) * a.m + c0,
+                              static_cast<uint32_t>(cw * 2), &bar[wib][b]);
+        }
+        pending[b] = true;
+    };
+    long long it = static_cast<long long>(blockIdx.x) * nw + wib;
+    int b = 0;
+    if (it < items) issue(it, 0);
+    bool ok = true;
+    for (; it < items; it += step, b ^= 1) {
+        const long long nxt = it + step;
+        if (nxt < items) {
+            // buffer b ^ 1 was read by every lane in the last iteration
+            fence_proxy_async_smem();
+            __syncwarp();
+            issue(nxt, b ^ 1);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar[wib][b], phase[b]))) {
+            if (lane == 0) flag_error(a.err, kErrWaitTimeout);
+            ok = false;
+            break;
+        }
+        phase[b] ^= 1u;
+        pending[b] = false;
+        const int t = static_cast<int>(it / nch), c0 = static_cast<int>(it % nch) * kStagedCW;
+        const int cw = min(kStagedCW, a.m - c0);
+        const uint8_t *src = bufs + static_cast<size_t>(b) * buf_bytes;
+        for (int f = lane * 8; f < cw; f += 256) {
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = 0.0f;
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                if (j >= a.k || pos[b][j] < 0) continue;
+                const uint8_t *row0 = src + static_cast<size_t>(j * a.splits) * kStagedCW * 2 + f * 2;
+                if (a.splits == 1) {
+                    const uint4 q = *reinterpret_cast<const uint4 *>(row0);
+                    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        y[2 * i] += 0.0f + bf16lo(w[i]);
+                        y[2 * i + 1] += 0.0f + bf16hi(w[i]);
+                    }
+                } else {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+                    for (int s0 = 0; s0 < a.splits; s0 += 4) {
+                        const int n = a.splits - s0 < 4 ? a.splits - s0 : 4;
+                        float pv[4][8];
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            if (g < n) {
+                                const uint4 q = *reinterpret_cast<const uint4 *>(
+                                    row0 + static_cast<size_t>(s0 + g) * kStagedCW * 2);
+                                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    pv[g][2 * i] = bf16lo(w[i]);
+                                    pv[g][2 * i + 1] = bf16hi(w[i]);
+                                }
+                            }
+                        }
+                        if (n == 4) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) v[e] += (pv[0][e] + pv[1][e]) + (pv[2][e] + pv[3][e]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                v[e] += pv[0][e];
+                                if (n > 1) v[e] += pv[1][e];
+                                if (n > 2) v[e] += pv[2][e];
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) y[e] += v[e];
+                }
+            }
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[e] = pack_bf16x2(y[2 * e], y[2 * e + 1]);
+            *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.y) + static_cast<size_t>(t) * a.m + c0 + f) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        __syncwarp();  // every lane is past its reads of buffer b before it is refilled
+    }
+    if (!ok) {
+        // copies this warp issued may still be landing in its buffers
+        for (int bb = 0; bb < 2; ++bb)
+            if (pending[bb] && lane == 0) mbar_wait(&bar[wib][bb], phase[bb]);
+        __syncwarp();
+    }
+}
+
 template <bool BF16, int KMAX, bool PB>
 cudaError_t launch_w(const CombineArgs &a, cudaStream_t s) {
     constexpr long long kGridThreads = 152LL * 16 * 256;
+    if constexpr (PB && BF16) {
+        // bf16 partial rows staged in shared memory by bulk copies (96 KB a
+        // block, two blocks an SM), for an unsplit down projection (Mixtral
+        // shape, Zipf 1.2: combine T = 512 11.8 -> 10.0 us, T = 8192 55.9 ->
+        // 40.9 us; with two splits (T = 2048) only three warps fit a block and
+        // it measured slower, 26.8 -> 33.3 us)
+        const int R = a.k * a.splits;
+        if (a.m % 8 == 0 && a.splits == 1 && R <= kStagedMaxRows) {
+            const size_t per_warp = 2 * static_cast<size_t>(R) * kStagedCW * 2;
+            int nw = static_cast<int>((96 * 1024) / per_warp);
+            nw = nw < 1 ? 1 : (nw > kStagedMaxWarps ? kStagedMaxWarps : nw);
+            const size_t smem = per_warp * nw;
+            auto kern = combine_staged_kernel<KMAX>;
+            static int configured = 0;
+            if (static_cast<int>(smem) > configured) {
+                const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                             static_cast<int>(smem));
+                if (err != cudaSuccess) return err;
+                configured = static_cast<int>(smem);
+            }
+            const long long items = static_cast<long long>(a.T) * ((a.m + kStagedCW - 1) / kStagedCW);
+            long long blocks = (items + nw - 1) / nw;
+            if (blocks > 2 * 152) blocks = 2 * 152;
+            return launch_pdl(kern, dim3(static_cast<unsigned>(blocks)), dim3(32 * nw), smem, s, a);
+        }
+    }
     if constexpr (PB) {
         // bf16 partial rows of a large batch (batch regime): a warp per token,
         // 16 features per lane, so a lane has as many bytes in flight as with
