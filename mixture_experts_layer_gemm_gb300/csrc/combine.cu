@@ -206,8 +206,8 @@ __global__ void __launch_bounds__(256) combine_tokens_kernel(const CombineArgs a
 }
 
 // Batch regime, bf16 partial rows, bf16 output: the partial rows staged in
-// shared memory by bulk copies.  A warp takes (token, chunk of kStagedCW
-// features) items in turn; lanes 0 .. k*splits-1 each copy one partial row's
+// shared memory by bulk copies.  A warp takes (token, chunk of
+// staged_chunk(R) features) items in turn; lanes 0 .. k*splits-1 each copy one partial row's
 // chunk (the token's k positions read once per item and shared by shuffle)
 // into the warp's buffer, completing on its mbarrier, while the warp sums the
 // previous item from the other buffer.  The bytes in flight no longer cost
@@ -215,9 +215,15 @@ __global__ void __launch_bounds__(256) combine_tokens_kernel(const CombineArgs a
 // rows (a warp per token: 58% of HBM at T = 8192).  Same arithmetic and order
 // as combine_item.  Every wait is bounded; a warp that gives up flags the
 // error word and waits (bounded) for its own copies before leaving.
-constexpr int kStagedCW = 2048;      // features of one staged chunk (4 KB of a bf16 row)
 constexpr int kStagedMaxRows = 8;    // k x splits partial rows per item
 constexpr int kStagedMaxWarps = 8;
+
+// Features of one staged chunk for R partial rows an item: R chunks of a
+// buffer hold 8 KB (a warp's double buffer 16 KB, six warps in 96 KB whatever
+// the split count), whole multiples of a warp's 256-feature pass.
+__host__ __device__ constexpr int staged_chunk(int R) {
+    return (4096 / R) / 256 * 256 < 256 ? 256 : (4096 / R) / 256 * 256;
+}
 
 template <int KMAX>
 __global__ void __launch_bounds__(kStagedMaxWarps * 32) combine_staged_kernel(const CombineArgs a) {
@@ -229,7 +235,8 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) combine_staged_kernel(co
     pdl_trigger();
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int R = a.k * a.splits;  // partial rows per item, <= kStagedMaxRows
-    const size_t buf_bytes = static_cast<size_t>(R) * kStagedCW * 2;
+    const int CW = staged_chunk(R);
+    const size_t buf_bytes = static_cast<size_t>(R) * CW * 2;
     uint8_t *bufs = smem_cs + static_cast<size_t>(wib) * 2 * buf_bytes;
     if (lane == 0) {
         mbar_init(&bar[wib][0], 1);
@@ -237,7 +244,7 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) combine_staged_kernel(co
         fence_barrier_init();
     }
     __syncwarp();
-    const int nch = (a.m + kStagedCW - 1) / kStagedCW;
+    const int nch = (a.m + CW - 1) / CW;
     const long long items = static_cast<long long>(a.T) * nch;
     const long long step = static_cast<long long>(gridDim.x) * nw;
     const int rows_total = a.T * a.k;
@@ -247,8 +254,8 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) combine_staged_kernel(co
     bool pending[2] = {false, false};
     // copies of item `it` into buffer b (positions into pos[b])
     auto issue = [&](long long it, int b) {
-        const int t = static_cast<int>(it / nch), c0 = static_cast<int>(it % nch) * kStagedCW;
-        const int cw = min(kStagedCW, a.m - c0);
+        const int t = static_cast<int>(it / nch), c0 = static_cast<int>(it % nch) * CW;
+        const int cw = min(CW, a.m - c0);
         int mine = -1;
         if (lane < a.k) {
             const int p = a.scatter[static_cast<size_t>(t) * a.k + lane];
@@ -273,7 +280,7 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) combine_staged_kernel(co
             for (int jj = 0; jj < KMAX; ++jj)
                 if (jj == j) pj = pos[b][jj];
             if (pj >= 0)
-                bulk_g2s_once(dst + static_cast<size_t>(lane) * kStagedCW * 2,
+                bulk_g2s_once(dst + static_cast<size_t>(lane) * CW * 2,
                               part + static_cast<size_t>(sp) * a.split_stride + static_cast<size_t>(pj) * a.m + c0,
                               static_cast<uint32_t>(cw * 2), &bar[wib][b]);
         }
@@ -298,8 +305,8 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) combine_staged_kernel(co
         }
         phase[b] ^= 1u;
         pending[b] = false;
-        const int t = static_cast<int>(it / nch), c0 = static_cast<int>(it % nch) * kStagedCW;
-        const int cw = min(kStagedCW, a.m - c0);
+        const int t = static_cast<int>(it / nch), c0 = static_cast<int>(it % nch) * CW;
+        const int cw = min(CW, a.m - c0);
         const uint8_t *src = bufs + static_cast<size_t>(b) * buf_bytes;
         for (int f = lane * 8; f < cw; f += 256) {
             float y[8];
@@ -308,7 +315,7 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) combine_staged_kernel(co
 #pragma unroll
             for (int j = 0; j < KMAX; ++j) {
                 if (j >= a.k || pos[b][j] < 0) continue;
-                const uint8_t *row0 = src + static_cast<size_t>(j * a.splits) * kStagedCW * 2 + f * 2;
+                const uint8_t *row0 = src + static_cast<size_t>(j * a.splits) * CW * 2 + f * 2;
                 if (a.splits == 1) {
                     const uint4 q = *reinterpret_cast<const uint4 *>(row0);
                     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
@@ -328,7 +335,7 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32) combine_staged_kernel(co
                         for (int g = 0; g < 4; ++g) {
                             if (g < n) {
                                 const uint4 q = *reinterpret_cast<const uint4 *>(
-                                    row0 + static_cast<size_t>(s0 + g) * kStagedCW * 2);
+                                    row0 + static_cast<size_t>(s0 + g) * CW * 2);
                                 const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                                 for (int i = 0; i < 4; ++i) {
@@ -376,11 +383,13 @@ cudaError_t launch_w(const CombineArgs &a, cudaStream_t s) {
         // bf16 partial rows staged in shared memory by bulk copies (96 KB a
         // block, two blocks an SM), for an unsplit down projection (Mixtral
         // shape, Zipf 1.2: combine T = 512 11.8 -> 10.0 us, T = 8192 55.9 ->
-        // 40.9 us; with two splits (T = 2048) only three warps fit a block and
-        // it measured slower, 26.8 -> 33.3 us)
+        // 40.9 us).  With two splits (T = 2048: four rows an item in
+        // 1024-feature chunks, six warps a block) it measured the same as the
+        // per-chunk kernel (26.6 us), which stays there.
         const int R = a.k * a.splits;
         if (a.m % 8 == 0 && a.splits == 1 && R <= kStagedMaxRows) {
-            const size_t per_warp = 2 * static_cast<size_t>(R) * kStagedCW * 2;
+            const int CW = staged_chunk(R);
+            const size_t per_warp = 2 * static_cast<size_t>(R) * CW * 2;
             int nw = static_cast<int>((96 * 1024) / per_warp);
             nw = nw < 1 ? 1 : (nw > kStagedMaxWarps ? kStagedMaxWarps : nw);
             const size_t smem = per_warp * nw;
@@ -392,7 +401,7 @@ cudaError_t launch_w(const CombineArgs &a, cudaStream_t s) {
                 if (err != cudaSuccess) return err;
                 configured = static_cast<int>(smem);
             }
-            const long long items = static_cast<long long>(a.T) * ((a.m + kStagedCW - 1) / kStagedCW);
+            const long long items = static_cast<long long>(a.T) * ((a.m + CW - 1) / CW);
             long long blocks = (items + nw - 1) / nw;
             if (blocks > 2 * 152) blocks = 2 * 152;
             return launch_pdl(kern, dim3(static_cast<unsigned>(blocks)), dim3(32 * nw), smem, s, a);

@@ -287,6 +287,35 @@ def test_every_token_to_every_expert(T, regime):
     np.testing.assert_allclose(run.w.sum(axis=1), 1.0, rtol=0, atol=1e-6)
 
 
+K3_WIDE = wl.LayerShape("k3-m1408", m=1408, p=256, E=6, k=3, expert=wl.SWIGLU, act="bf16",
+                        weight="bf16")
+K1_WIDE = wl.LayerShape("k1-m4352", m=4352, p=256, E=4, k=1, expert=wl.SWIGLU, act="bf16",
+                        weight="bf16")
+K4_WIDE = wl.LayerShape("k4-m1408", m=1408, p=512, E=8, k=4, expert=wl.SWIGLU, act="bf16",
+                        weight="bf16")
+
+
+@pytest.mark.parametrize("shape,T,splits", [(K3_WIDE, 200, 2), (K3_WIDE, 600, 1), (K1_WIDE, 600, 1),
+                                            (K4_WIDE, 600, 2)])
+def test_combine_of_bf16_partial_rows_in_ragged_chunks(shape, T, splits):
+    """Batches past the decode row cap write bf16 partial rows.  Of an
+    unsplit down projection the combine sums them from shared-memory chunks of
+    4096 / k features rounded down to 256, each case with a short last chunk
+    (k = 3: 1408 = 1280 + 128; k = 1: 4352 = 4096 + 256); with two splits
+    (k x splits = 6 and 8 rows a token) the per-chunk kernel sums them."""
+    layer = get_layer(shape, seed=44)
+    x = wl.make_tokens(shape, T, seed=45)
+    ml = moe.MoELayer(layer, T, with_logits=True)
+    ml.set_regime(moe.REGIME_BATCH)
+    assert ml.plan(T).splits_down == splits
+    run = Run(ml, x)
+    assert ml.sync_check()[0] == moe.MOE_OK
+    ids, w = check_routing(run, layer, x)
+    rel, glob = max_token_rel_l2(run.y_np, oracle_y(layer, x, ids, w))
+    assert rel <= TOL["bf16"], (rel, glob)
+    ml.close()
+
+
 def test_batch_beyond_the_gemv_on_a_shape_without_tensor_core_tiles_is_refused():
     """m = 320 has no 128-row blocks for the tensor-core path and T*k = 600 is
     more than the weight-streaming kernels take: the call is refused with
