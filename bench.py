@@ -521,6 +521,9 @@ def measure(args, world, local, shape, layer, tokens, xs_np, steps, warmup, weig
            "phase_ms_per_step": phase_ms,
            "ms_per_step_with_launch_events": ms_events / steps,
            "active_experts": active, "per_T": per_t,
+           "per_T_note": "layer_us_wall: route + forward of one batch timed as a whole (launches overlap "
+                         "as in the timed region); layer_us, up_us, down_us: sums of per-launch events, "
+                         "each of which ends the programmatic overlap of the launches around it",
            "gpu_launches": launches, "clocks": clk}
     if tensor_bound:
         rec["layer_tensor"] = {"achieved": layer_tf, "unit": "TFLOP/s",
@@ -688,7 +691,7 @@ def run_ours(args, world, rank, local):
                            "launch": "one CUDA graph per step, replayed" if args.graph
                            else "stream launches with programmatic dependent launch"}}
         for key in ("roofline", "layer_hbm", "layer_tensor", "layer_tflops", "phase_ms_per_step",
-                    "ms_per_step_with_launch_events", "active_experts", "per_T"):
+                    "ms_per_step_with_launch_events", "active_experts", "per_T", "per_T_note"):
             if key in rec:
                 line[key] = rec[key]
         line["cpu_baseline"] = cpu
