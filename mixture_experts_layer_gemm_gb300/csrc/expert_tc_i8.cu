@@ -113,6 +113,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nis = (4 * geo.N <= static_cast<int>(kTwoIssuerCols)) ? 2 : 1;
     const uint32_t a_col0 = static_cast<uint32_t>((2 * nis * geo.N + 63) / 64 * 64);
     const int nab = min(kMaxABufs, static_cast<int>((kTmemCols - a_col0) / 64));
+    // The weight and scale pointers, copied from the launch parameters into
+    // shared memory before the wait: the producer and the epilogue look them up
+    // at every tile, and a dynamically indexed parameter read can miss the
+    // constant cache.  Scales: gate rows s1, up rows s3 (SwiGLU); s1 (ReLU up);
+    // s2 (down).
+    __shared__ const void *s_wptr[kExpertTableMax];
+    __shared__ const float *s_sptr[2][kExpertTableMax];
+    if (warp == 2)
+        for (int e = lane; e < kExpertTableMax; e += 32) {
+            s_wptr[e] = PHASE == kUp ? tab.w1[e] : tab.w2[e];
+            s_sptr[0][e] = PHASE == kUp ? tab.s1[e] : tab.s2[e];
+            s_sptr[1][e] = tab.s3[e];
+        }
     pdl_wait();
     pdl_trigger();
 
@@ -157,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int cur = 0;  // expert of the last tile (a role's tiles come in order)
             for (long long u = blockIdx.x; u < total && !s_abort; u += gridDim.x) {
                 const TcTile t = tc_tile(u, s_prefix, s_act, s_off, s_q, nact, geo, cur);
-                const uint8_t *w = static_cast<const uint8_t *>(PHASE == kUp ? tab.w1[t.e] : tab.w2[t.e]);
+                const uint8_t *w = static_cast<const uint8_t *>(s_wptr[t.e]);
                 const int brow = t.off + t.tt * geo.N;
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1u)) {
@@ -277,11 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int f = (R >> 4) * 8 + (r16 & 7);
             float scale;
             if (PHASE == kUp && GATED)
-                scale = (r16 < 8) ? tab.s1[t.e][f] : tab.s3[t.e][f];
-            else if (PHASE == kUp)
-                scale = tab.s1[t.e][R];
+                scale = s_sptr[r16 < 8 ? 0 : 1][t.e][f];
             else
-                scale = tab.s2[t.e][R];
+                scale = s_sptr[0][t.e][R];
             const int tok0 = t.tt * geo.N;
             const int n_valid = min(geo.N, (t.q - tok0 + 15) / 16 * 16);
             if (PHASE == kDown)
