@@ -35,6 +35,7 @@
 #include "packing.h"
 #include "tc.cuh"
 #include "tc_tiles.cuh"
+#include "tile_trace.cuh"
 
 namespace moe {
 
@@ -69,6 +70,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t *b_slots = smem + geo.stages * kATileBytes;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    MOE_TRACE_ENTRY(PHASE);
     pdl_wait();
     pdl_trigger();
 
@@ -159,6 +161,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         s_abort = 1;
                         break;
                     }
+                    if (kb == t.kb0) MOE_TRACE_TILE_FIRST(PHASE, ntile, t.e, t.tt, n_valid, t.rb);
+                    if (kb == t.kb1 - 1) MOE_TRACE_TILE_LAST(PHASE, ntile);
                     tc_fence_after();
                     const uint32_t abase = smem_u32(a_slots + stage * kATileBytes);
                     const uint32_t bbase = smem_u32(b_slots + stage * geo.b_bytes);
@@ -376,3 +380,5 @@ cudaError_t launch_tc_down(const ExpertArgs &a, int splits, int N, const CUtenso
 }
 
 }  // namespace moe
+
+MOE_TRACE_READER(moe_tile_trace_tc)

@@ -40,6 +40,7 @@
 #include "packing.h"
 #include "tc.cuh"
 #include "tc_tiles.cuh"
+#include "tile_trace.cuh"
 
 namespace moe {
 
@@ -75,6 +76,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
     const long long pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    MOE_TRACE_ENTRY(0);
     pdl_wait();
     pdl_trigger();
 
@@ -169,6 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         s_abort = 1;
                         break;
                     }
+                    if (kb == t.kb0) MOE_TRACE_TILE_FIRST(0, ntile, t.e, t.tt, nv, t.rb);
+                    if (kb == t.kb1 - 1) MOE_TRACE_TILE_LAST(0, ntile);
                     tc_fence_after();
                     const uint32_t abase = smem_u32(smem + stage * kStageBytes);
                     const uint32_t bbase = abase + kHalfA;
@@ -326,3 +330,5 @@ cudaError_t launch_tc2_up(const ExpertArgs &a, bool gated, const CUtensorMap &wm
 }
 
 }  // namespace moe
+
+MOE_TRACE_READER(moe_tile_trace_tc2)
