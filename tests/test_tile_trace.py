@@ -4,10 +4,14 @@ The tool reads per-tile stamps from the trace build of the library and
 prints, per expert, the tiles' count, widths, median duration and window.
 These tests feed it hand-made records whose answers are known."""
 import io
+import os
+import shutil
 from contextlib import redirect_stdout
 
 import numpy as np
+import pytest
 
+from mixture_experts_layer_gemm_gb300 import build as lib_build
 from mixture_experts_layer_gemm_gb300 import tile_trace as tt
 
 
@@ -52,3 +56,15 @@ def test_no_records():
     with redirect_stdout(out):
         tt.summarize("up projection", np.zeros_like(t), t0, info, np.arange(2), np.array([1, 1]))
     assert "no tiles recorded" in out.getvalue()
+
+
+def test_trace_build_compiles_the_instrumented_kernels():
+    """The two instrumented kernel files compile with MOE_TILE_TRACE (nvcc
+    cross-compiles here; objects go to the trace build's own folder)."""
+    if not (shutil.which("nvcc") or os.path.exists("/usr/local/cuda/bin/nvcc")):
+        pytest.skip("nvcc not available")
+    os.makedirs(lib_build.BUILD_TRACE, exist_ok=True)
+    for name in ("expert_tc.cu", "expert_tc2.cu"):
+        obj, _ = lib_build._compile(os.path.join(lib_build.CSRC, name), ["-DMOE_TILE_TRACE"], False,
+                                    lib_build.BUILD_TRACE)
+        assert os.path.getsize(obj) > 0
