@@ -206,8 +206,8 @@ __global__ void __launch_bounds__(256) combine_tokens_kernel(const CombineArgs a
 }
 
 // Batch regime, bf16 partial rows, bf16 output: the partial rows staged in
-// shared memory by bulk copies.  A warp takes (token, chunk of
-// staged_chunk(R) features) items in turn; lanes 0 .. k*splits-1 each copy one partial row's
+// shared memory by bulk copies.  A warp takes (token, chunk of staged_chunk(R)
+// features) items in turn; lanes 0 .. k*splits-1 each copy one partial row's
 // chunk (the token's k positions read once per item and shared by shuffle)
 // into the warp's buffer, completing on its mbarrier, while the warp sums the
 // previous item from the other buffer.  The bytes in flight no longer cost
@@ -218,9 +218,10 @@ __global__ void __launch_bounds__(256) combine_tokens_kernel(const CombineArgs a
 constexpr int kStagedMaxRows = 8;    // k x splits partial rows per item
 constexpr int kStagedMaxWarps = 8;
 
-// Features of one staged chunk for R partial rows an item: R chunks of a
-// buffer hold 8 KB (a warp's double buffer 16 KB, six warps in 96 KB whatever
-// the split count), whole multiples of a warp's 256-feature pass.
+// Features of one staged chunk for R partial rows an item: R chunks fill at
+// most 8 KB, so a warp's double buffer is at most 16 KB and at least six warps
+// fit in 96 KB for any R; chunks are whole multiples of a warp's 256-feature
+// pass.
 __host__ __device__ constexpr int staged_chunk(int R) {
     return (4096 / R) / 256 * 256 < 256 ? 256 : (4096 / R) / 256 * 256;
 }
